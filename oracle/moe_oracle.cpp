@@ -1,0 +1,537 @@
+// CPU oracle of the single-GPU dropless top-k MoE layer (forward and backward).
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+// load this file; only the tests, the smoke check and the benchmark's CPU
+// baseline do.  It shares no code, header or table with the CUDA library.
+//
+// What it computes follows "Scalable Training of Mixture-of-Experts Models with
+// Megatron Core" (summary page, section "Method"): a router (learned linear
+// projection in FP32, softmax or sigmoid scoring, top-k selection), a
+// dispatcher that groups each expert's tokens contiguously, SwiGLU experts
+// ("GLU Variants Improve Transformer", cited on the index page under "Builds
+// on"), and a combine stage that sums the gate-weighted expert outputs.  The
+// layer is dropless (same page, "Method": sync-free dropless execution), so
+// every one of the T*k assignments is kept.
+//
+// The pages give no formulas; the readings taken here are:
+//  * top-k in descending key order, ties to the lower expert index;
+//  * softmax key = logit (+ selection bias), sigmoid key = sigmoid(logit)
+//    (+ selection bias); the bias never enters the gate values;
+//  * group-limited routing: contiguous groups of E/n_group experts, group
+//    score = sum of the two largest keys (or the max), keep topk_group groups
+//    (ties to the lower group id), then top-k inside them;
+//  * gates renormalised over the k winners (softmax over the selected logits,
+//    or s_j / sum s), then multiplied by gate_scale;
+//  * SwiGLU expert: y = W2 (silu(Wg x) * (Wu x)), no biases, silu(z)=z*sigmoid(z);
+//  * shared expert: always on, gate 1, added in the combine;
+//  * backward: the exact gradient of L = <dY, Y>, selection treated as
+//    piecewise constant (no gradient through top-k, groups or the bias).
+//
+// Arithmetic: every dot product accumulates in double.  In "mirror" mode the
+// values are rounded to bf16 (round-to-nearest-even) exactly where the GPU
+// path stores bf16 tensors (GU, A, Yperm, Y, dYperm, dGU, dXperm, dX, dW) and
+// nowhere else; in "pure" mode nothing is rounded (for finite differences).
+//
+// The dispatch maps are built by a plain stable counting sort over tokens in
+// increasing order, which the GPU path does not use.
+//
+// Parity pins live in tests/test_oracle_pins.py (brute-force selection, E=1
+// dense SwiGLU, identical experts, bijection invariants, gate sums, finite
+// differences, autograd).  Parity unpinned: values at the full workload sizes,
+// for which the pages print nothing; there the oracle itself is the reference.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+extern "C" {
+typedef struct {
+  int32_t T, H, E, k, F, F_shared;
+  int32_t score_fn;    // 0 softmax, 1 sigmoid
+  int32_t renorm;      // 1: renormalise the k gates
+  double gate_scale;   // multiplies the gates after renormalisation
+  int32_t n_group;     // 1: no group limit
+  int32_t topk_group;  // groups kept when n_group > 1
+  int32_t group_score; // 0: sum of the two largest keys, 1: the largest key
+  int32_t align;       // row alignment of each expert segment in the permuted buffer
+  int32_t BM;          // rows per M tile, for tile_offsets
+  int32_t mirror;      // 1: round to bf16 where the GPU stores bf16; 0: pure double
+  int32_t nthreads;    // 0: all host cores
+} ora_cfg;
+}
+
+namespace {
+
+inline double bf(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// Round a double to the nearest bf16 value (ties to even), returned as double.
+inline double rbf(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e;
+  double m = std::frexp(x, &e);               // x = m * 2^e, 0.5 <= |m| < 1
+  double q = std::nearbyint(std::ldexp(m, 8)); // 8 significant bits, default mode = ties-to-even
+  return std::ldexp(q, e - 8);
+}
+
+inline double maybe_r(const ora_cfg& c, double x) { return c.mirror ? rbf(x) : x; }
+
+inline double sigm(double z) { return 1.0 / (1.0 + std::exp(-z)); }
+inline double silu(double z) { return z * sigm(z); }
+inline double dsilu(double z) {
+  const double s = sigm(z);
+  return s * (1.0 + z * (1.0 - s));
+}
+
+int nthreads_of(const ora_cfg& c) {
+  if (c.nthreads > 0) return c.nthreads;
+  unsigned hc = std::thread::hardware_concurrency();
+  return hc ? (int)hc : 1;
+}
+
+template <typename Fn>
+void parallel_for(int64_t n, int nth, Fn fn) {
+  if (nth <= 1 || n <= 1) {
+    for (int64_t i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  std::atomic<int64_t> next{0};
+  std::vector<std::thread> th;
+  for (int w = 0; w < std::min<int64_t>(nth, n); ++w)
+    th.emplace_back([&] {
+      for (int64_t i; (i = next.fetch_add(1)) < n;) fn(i);
+    });
+  for (auto& t : th) t.join();
+}
+
+// Top-k selection with the optional group limit, on keys of type K.
+// Keys are formed by the caller; returns experts in descending key order,
+// ties to the lower index.
+template <typename K>
+void select_topk(const ora_cfg& c, const K* key, int32_t* out) {
+  const int E = c.E;
+  std::vector<char> allowed(E, 1);
+  if (c.n_group > 1) {
+    const int G = c.n_group, per = E / G;
+    std::vector<K> gs(G);
+    for (int g = 0; g < G; ++g) {
+      // largest key in the group, then the largest of the others
+      int i1 = g * per;
+      for (int e = g * per; e < (g + 1) * per; ++e)
+        if (key[e] > key[i1]) i1 = e;
+      if (c.group_score == 1 || per == 1) {
+        gs[g] = key[i1];
+      } else {
+        int i2 = -1;
+        for (int e = g * per; e < (g + 1) * per; ++e)
+          if (e != i1 && (i2 < 0 || key[e] > key[i2])) i2 = e;
+        gs[g] = key[i1] + key[i2];
+      }
+    }
+    std::vector<char> keep(G, 0);
+    for (int r = 0; r < c.topk_group; ++r) {
+      int best = -1;
+      for (int g = 0; g < G; ++g)
+        if (!keep[g] && (best < 0 || gs[g] > gs[best])) best = g;
+      keep[best] = 1;
+    }
+    for (int e = 0; e < E; ++e) allowed[e] = keep[e / per];
+  }
+  std::vector<char> taken(E, 0);
+  for (int j = 0; j < c.k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e)
+      if (allowed[e] && !taken[e] && (best < 0 || key[e] > key[best])) best = e;
+    taken[best] = 1;
+    out[j] = best;
+  }
+}
+
+// Gates of one token from its double logits and its selection.
+void token_gates(const ora_cfg& c, const double* l, const int32_t* sel, double* g) {
+  const int k = c.k, E = c.E;
+  if (c.score_fn == 0) {
+    if (c.renorm) {
+      double m = l[sel[0]];
+      for (int j = 1; j < k; ++j) m = std::max(m, l[sel[j]]);
+      double z = 0;
+      for (int j = 0; j < k; ++j) z += std::exp(l[sel[j]] - m);
+      for (int j = 0; j < k; ++j) g[j] = c.gate_scale * std::exp(l[sel[j]] - m) / z;
+    } else {
+      double m = l[0];
+      for (int e = 1; e < E; ++e) m = std::max(m, l[e]);
+      double z = 0;
+      for (int e = 0; e < E; ++e) z += std::exp(l[e] - m);
+      for (int j = 0; j < k; ++j) g[j] = c.gate_scale * std::exp(l[sel[j]] - m) / z;
+    }
+  } else {
+    double S = 0;
+    for (int j = 0; j < k; ++j) S += sigm(l[sel[j]]);
+    for (int j = 0; j < k; ++j) g[j] = c.gate_scale * sigm(l[sel[j]]) / (c.renorm ? S : 1.0);
+  }
+}
+
+// d(gates)/d(logits) applied to dg: exact gradient of token_gates for a fixed selection.
+void token_dlogits(const ora_cfg& c, const double* l, const int32_t* sel, const double* g,
+                   const double* dg, double* dl) {
+  const int k = c.k, E = c.E;
+  const double a = c.gate_scale;
+  for (int e = 0; e < E; ++e) dl[e] = 0.0;
+  if (c.score_fn == 0) {
+    if (c.renorm) {
+      // g_j = a * q_j, q = softmax over the selected logits
+      double s = 0;
+      for (int j = 0; j < k; ++j) s += (g[j] / a) * dg[j];
+      for (int j = 0; j < k; ++j) dl[sel[j]] = a * (g[j] / a) * (dg[j] - s);
+    } else {
+      // g_j = a * p[sel_j], p = softmax over all E logits
+      double m = l[0];
+      for (int e = 1; e < E; ++e) m = std::max(m, l[e]);
+      std::vector<double> p(E);
+      double z = 0;
+      for (int e = 0; e < E; ++e) z += (p[e] = std::exp(l[e] - m));
+      for (int e = 0; e < E; ++e) p[e] /= z;
+      double s = 0;
+      for (int j = 0; j < k; ++j) s += dg[j] * p[sel[j]];
+      for (int e = 0; e < E; ++e) dl[e] = -a * p[e] * s;
+      for (int j = 0; j < k; ++j) dl[sel[j]] += a * p[sel[j]] * dg[j];
+    }
+  } else {
+    if (c.renorm) {
+      // g_j = a * s_j / S, S = sum of the selected sigmoids
+      double S = 0, cc = 0;
+      for (int j = 0; j < k; ++j) S += sigm(l[sel[j]]);
+      for (int j = 0; j < k; ++j) cc += dg[j] * g[j] / a;
+      for (int j = 0; j < k; ++j) {
+        const double s = sigm(l[sel[j]]);
+        const double ds = (a / S) * (dg[j] - cc);
+        dl[sel[j]] = ds * s * (1.0 - s);
+      }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const double s = sigm(l[sel[j]]);
+        dl[sel[j]] = a * dg[j] * s * (1.0 - s);
+      }
+    }
+  }
+}
+
+// One SwiGLU expert applied to one token.  w13: [2F,H] (gate rows then up rows),
+// w2: [H,F].  Outputs (all length as named): gr,ur (F) = stored pre-activations,
+// ar (F) = stored activation, yr (H) = stored expert output.
+void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* x,
+                double* gr, double* ur, double* ar, double* yr) {
+  const int H = c.H;
+  for (int f = 0; f < F; ++f) {
+    double g = 0, u = 0;
+    const uint16_t* wg = w13 + (size_t)f * H;
+    const uint16_t* wu = w13 + (size_t)(F + f) * H;
+    for (int h = 0; h < H; ++h) {
+      g += bf(wg[h]) * x[h];
+      u += bf(wu[h]) * x[h];
+    }
+    gr[f] = maybe_r(c, g);
+    ur[f] = maybe_r(c, u);
+    ar[f] = maybe_r(c, silu(g) * u);  // the activation is formed from the unrounded g, u
+  }
+  for (int h = 0; h < H; ++h) {
+    double y = 0;
+    const uint16_t* w = w2 + (size_t)h * F;
+    for (int f = 0; f < F; ++f) y += bf(w[f]) * ar[f];
+    yr[h] = maybe_r(c, y);
+  }
+}
+
+// Backward of one expert for one token, given the upstream gradient dyp (H) of
+// its output.  Produces dG, dU (F, as stored) and dx (H, as stored).
+void expert_bwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* gr,
+                const double* ur, const double* dyp, double* dG, double* dU, double* dx) {
+  const int H = c.H;
+  std::vector<double> dA(F, 0.0);
+  for (int h = 0; h < H; ++h) {
+    const uint16_t* w = w2 + (size_t)h * F;
+    const double d = dyp[h];
+    for (int f = 0; f < F; ++f) dA[f] += bf(w[f]) * d;
+  }
+  for (int f = 0; f < F; ++f) {
+    dG[f] = maybe_r(c, dA[f] * ur[f] * dsilu(gr[f]));
+    dU[f] = maybe_r(c, dA[f] * silu(gr[f]));
+  }
+  for (int h = 0; h < H; ++h) dx[h] = 0.0;
+  for (int f = 0; f < F; ++f) {
+    const uint16_t* wg = w13 + (size_t)f * H;
+    const uint16_t* wu = w13 + (size_t)(F + f) * H;
+    const double a = dG[f], b = dU[f];
+    for (int h = 0; h < H; ++h) dx[h] += bf(wg[h]) * a + bf(wu[h]) * b;
+  }
+  for (int h = 0; h < H; ++h) dx[h] = maybe_r(c, dx[h]);
+}
+
+}  // namespace
+
+extern "C" {
+
+// Router logits and scores for all tokens: logits = X W_r^T (+ logit_bias),
+// scores = softmax over E (softmax mode) or sigmoid(logit) (sigmoid mode).
+void ora_router(const ora_cfg* cp, const uint16_t* X, const float* Wr, const float* logit_bias,
+                double* logits, double* scores) {
+  const ora_cfg c = *cp;
+  const int H = c.H, E = c.E;
+  parallel_for(c.T, nthreads_of(c), [&](int64_t t) {
+    double* l = logits + (size_t)t * E;
+    for (int e = 0; e < E; ++e) {
+      double s = 0;
+      for (int h = 0; h < H; ++h) s += bf(X[(size_t)t * H + h]) * (double)Wr[(size_t)e * H + h];
+      l[e] = s + (logit_bias ? (double)logit_bias[e] : 0.0);
+    }
+    double* s = scores + (size_t)t * E;
+    if (c.score_fn == 0) {
+      double m = l[0];
+      for (int e = 1; e < E; ++e) m = std::max(m, l[e]);
+      double z = 0;
+      for (int e = 0; e < E; ++e) z += (s[e] = std::exp(l[e] - m));
+      for (int e = 0; e < E; ++e) s[e] /= z;
+    } else {
+      for (int e = 0; e < E; ++e) s[e] = sigm(l[e]);
+    }
+  });
+}
+
+// Selection on double logits/scores (pure oracle routing).
+// key = logit (softmax) or score (sigmoid), plus sel_bias when given.
+void ora_select_f64(const ora_cfg* cp, const double* logits, const double* scores, const float* sel_bias,
+                    int32_t* topk_idx) {
+  const ora_cfg c = *cp;
+  parallel_for(c.T, nthreads_of(c), [&](int64_t t) {
+    std::vector<double> key(c.E);
+    const double* base = (c.score_fn == 0 ? logits : scores) + (size_t)t * c.E;
+    for (int e = 0; e < c.E; ++e) key[e] = base[e] + (sel_bias ? (double)sel_bias[e] : 0.0);
+    select_topk<double>(c, key.data(), topk_idx + (size_t)t * c.k);
+  });
+}
+
+// Selection on float32 logits/scores, keys and group sums formed in float32.
+// Used to run the oracle's selection on the exact scores another
+// implementation produced, so that selections can be compared bit for bit.
+void ora_select_f32(const ora_cfg* cp, const float* logits, const float* scores, const float* sel_bias,
+                    int32_t* topk_idx) {
+  const ora_cfg c = *cp;
+  parallel_for(c.T, nthreads_of(c), [&](int64_t t) {
+    std::vector<float> key(c.E);
+    const float* base = (c.score_fn == 0 ? logits : scores) + (size_t)t * c.E;
+    for (int e = 0; e < c.E; ++e) key[e] = base[e] + (sel_bias ? sel_bias[e] : 0.0f);
+    select_topk<float>(c, key.data(), topk_idx + (size_t)t * c.k);
+  });
+}
+
+// Gate values of all tokens from double logits and a given selection.
+void ora_gates(const ora_cfg* cp, const double* logits, const int32_t* topk_idx, double* gates) {
+  const ora_cfg c = *cp;
+  parallel_for(c.T, nthreads_of(c), [&](int64_t t) {
+    token_gates(c, logits + (size_t)t * c.E, topk_idx + (size_t)t * c.k, gates + (size_t)t * c.k);
+  });
+}
+
+// Dispatch maps by a stable counting sort.  slot_src has R entries; entries at
+// or beyond offsets[E] are left untouched.  Padding slots get -1.
+int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                 int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src, int64_t R) {
+  const ora_cfg c = *cp;
+  const int E = c.E, k = c.k;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t i = 0; i < (int64_t)c.T * k; ++i) counts[topk_idx[i]]++;
+  offsets[0] = 0;
+  tile_offsets[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    const int32_t padded = (counts[e] + c.align - 1) / c.align * c.align;
+    offsets[e + 1] = offsets[e] + padded;
+    tile_offsets[e + 1] = tile_offsets[e] + (counts[e] + c.BM - 1) / c.BM;
+  }
+  if ((int64_t)offsets[E] > R) return -1;
+  std::vector<int32_t> cursor(offsets, offsets + E);
+  for (int t = 0; t < c.T; ++t)
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[(size_t)t * k + j];
+      const int32_t slot = cursor[e]++;
+      row_id_map[(size_t)t * k + j] = slot;
+      slot_src[slot] = t * k + j;
+    }
+  for (int e = 0; e < E; ++e)
+    for (int32_t s = offsets[e] + counts[e]; s < offsets[e + 1]; ++s) slot_src[s] = -1;
+  return 0;
+}
+
+// Forward and backward of the listed tokens.  Per token t (index i in tok_list):
+//   Y[i]      = sum_j gates[t,j] * expert_{e_tj}(x_t) + shared(x_t)          (H)
+//   dgates[i] = <dY_t, expert_{e_tj}(x_t)>                                  (k)
+//   dlogits[i]= exact gradient of the gates w.r.t. the logits, applied to dgates (E)
+//   dX[i]     = sum_j d expert / dx + d shared / dx + dlogits W_r           (H)
+// logits are the double router logits of all T tokens; gates the double gates.
+// Any output may be null; dX/dgates/dlogits need dY.
+void ora_tokens(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                const uint16_t* W13s, const uint16_t* W2s, const float* Wr, const int32_t* topk_idx,
+                const double* logits, const double* gates, const uint16_t* dY, int64_t ntok,
+                const int64_t* tok_list, double* Y, double* dX, double* dgates_out, double* dlogits_out) {
+  const ora_cfg c = *cp;
+  const int H = c.H, F = c.F, Fs = c.F_shared, E = c.E, k = c.k;
+  const bool bwd = dY && (dX || dgates_out || dlogits_out);
+  parallel_for(ntok, nthreads_of(c), [&](int64_t i) {
+    const int64_t t = tok_list[i];
+    std::vector<double> x(H), y(H, 0.0), dx(H, 0.0), dy(H), dyp(H), ye(H), dxe(H);
+    const int Fm = std::max(F, Fs);
+    std::vector<double> gr(Fm), ur(Fm), ar(Fm), dG(Fm), dU(Fm);
+    std::vector<double> dg(k, 0.0), dl(E, 0.0);
+    for (int h = 0; h < H; ++h) x[h] = bf(X[(size_t)t * H + h]);
+    if (dY)
+      for (int h = 0; h < H; ++h) dy[h] = bf(dY[(size_t)t * H + h]);
+    const int32_t* sel = topk_idx + (size_t)t * k;
+    const double* gt = gates + (size_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = sel[j];
+      const uint16_t* w13 = W13 + (size_t)e * 2 * F * H;
+      const uint16_t* w2 = W2 + (size_t)e * H * F;
+      expert_fwd(c, F, w13, w2, x.data(), gr.data(), ur.data(), ar.data(), ye.data());
+      for (int h = 0; h < H; ++h) y[h] += gt[j] * ye[h];
+      if (bwd) {
+        double s = 0;
+        for (int h = 0; h < H; ++h) s += dy[h] * ye[h];
+        dg[j] = s;
+        for (int h = 0; h < H; ++h) dyp[h] = maybe_r(c, gt[j] * dy[h]);
+        expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dyp.data(), dG.data(), dU.data(), dxe.data());
+        for (int h = 0; h < H; ++h) dx[h] += dxe[h];
+      }
+    }
+    if (Fs > 0) {
+      expert_fwd(c, Fs, W13s, W2s, x.data(), gr.data(), ur.data(), ar.data(), ye.data());
+      for (int h = 0; h < H; ++h) y[h] += ye[h];
+      if (bwd) {
+        expert_bwd(c, Fs, W13s, W2s, gr.data(), ur.data(), dy.data(), dG.data(), dU.data(), dxe.data());
+        for (int h = 0; h < H; ++h) dx[h] += dxe[h];
+      }
+    }
+    if (Y)
+      for (int h = 0; h < H; ++h) Y[(size_t)i * H + h] = maybe_r(c, y[h]);
+    if (bwd) {
+      token_dlogits(c, logits + (size_t)t * E, sel, gt, dg.data(), dl.data());
+      for (int e = 0; e < E; ++e) {
+        if (dl[e] == 0.0) continue;
+        const float* w = Wr + (size_t)e * H;
+        for (int h = 0; h < H; ++h) dx[h] += dl[e] * (double)w[h];
+      }
+      if (dX)
+        for (int h = 0; h < H; ++h) dX[(size_t)i * H + h] = maybe_r(c, dx[h]);
+      if (dgates_out)
+        for (int j = 0; j < k; ++j) dgates_out[(size_t)i * k + j] = dg[j];
+      if (dlogits_out)
+        for (int e = 0; e < E; ++e) dlogits_out[(size_t)i * E + e] = dl[e];
+    }
+  });
+}
+
+// Weight gradients of one expert (expert = -1: the shared expert, which sees
+// every token with gate 1).  dW13: [2F,H] (gate rows then up rows), dW2: [H,F].
+void ora_expert_wgrad(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                      const uint16_t* W13s, const uint16_t* W2s, const int32_t* topk_idx,
+                      const double* gates, const uint16_t* dY, int32_t expert, double* dW13, double* dW2) {
+  const ora_cfg c = *cp;
+  const int H = c.H, k = c.k;
+  const int F = expert < 0 ? c.F_shared : c.F;
+  const uint16_t* w13 = expert < 0 ? W13s : W13 + (size_t)expert * 2 * F * H;
+  const uint16_t* w2 = expert < 0 ? W2s : W2 + (size_t)expert * H * F;
+  // the (token, gate) pairs routed to this expert, in token order
+  std::vector<int64_t> toks;
+  std::vector<double> gsel;
+  for (int64_t t = 0; t < c.T; ++t) {
+    if (expert < 0) {
+      toks.push_back(t);
+      gsel.push_back(1.0);
+      continue;
+    }
+    for (int j = 0; j < k; ++j)
+      if (topk_idx[t * k + j] == expert) {
+        toks.push_back(t);
+        gsel.push_back(gates[t * k + j]);
+      }
+  }
+  std::fill(dW13, dW13 + (size_t)2 * F * H, 0.0);
+  std::fill(dW2, dW2 + (size_t)H * F, 0.0);
+  const int64_t n = (int64_t)toks.size();
+  const int64_t chunk = 512;
+  std::vector<double> xs, dyps, as, dGs, dUs;
+  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+    const int64_t m = std::min(chunk, n - c0);
+    xs.assign((size_t)m * H, 0.0);
+    dyps.assign((size_t)m * H, 0.0);
+    as.assign((size_t)m * F, 0.0);
+    dGs.assign((size_t)m * F, 0.0);
+    dUs.assign((size_t)m * F, 0.0);
+    parallel_for(m, nthreads_of(c), [&](int64_t i) {
+      const int64_t t = toks[c0 + i];
+      std::vector<double> gr(F), ur(F), ye(H), dxe(H);
+      double* x = &xs[(size_t)i * H];
+      double* dyp = &dyps[(size_t)i * H];
+      for (int h = 0; h < H; ++h) x[h] = bf(X[(size_t)t * H + h]);
+      expert_fwd(c, F, w13, w2, x, gr.data(), ur.data(), &as[(size_t)i * F], ye.data());
+      for (int h = 0; h < H; ++h) dyp[h] = maybe_r(c, gsel[c0 + i] * bf(dY[(size_t)t * H + h]));
+      expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dyp, &dGs[(size_t)i * F], &dUs[(size_t)i * F], dxe.data());
+    });
+    // dW2[h,f] += dyp[h] a[f]; dWg[f,h] += dG[f] x[h]; dWu[f,h] += dU[f] x[h]
+    parallel_for(H, nthreads_of(c), [&](int64_t h) {
+      double* row = dW2 + (size_t)h * F;
+      for (int64_t i = 0; i < m; ++i) {
+        const double d = dyps[(size_t)i * H + h];
+        const double* a = &as[(size_t)i * F];
+        for (int f = 0; f < F; ++f) row[f] += d * a[f];
+      }
+    });
+    parallel_for(2 * (int64_t)F, nthreads_of(c), [&](int64_t r) {
+      double* row = dW13 + (size_t)r * H;
+      const bool up = r >= F;
+      const int f = (int)(up ? r - F : r);
+      for (int64_t i = 0; i < m; ++i) {
+        const double d = up ? dUs[(size_t)i * F + f] : dGs[(size_t)i * F + f];
+        const double* x = &xs[(size_t)i * H];
+        for (int h = 0; h < H; ++h) row[h] += d * x[h];
+      }
+    });
+  }
+  if (c.mirror) {
+    for (size_t i = 0; i < (size_t)2 * F * H; ++i) dW13[i] = rbf(dW13[i]);
+    for (size_t i = 0; i < (size_t)H * F; ++i) dW2[i] = rbf(dW2[i]);
+  }
+}
+
+// Router weight gradients from the double dlogits of all T tokens:
+// dW_r[e,h] = sum_t dl[t,e] x[t,h];  dlogit_bias[e] = sum_t dl[t,e].
+void ora_router_wgrad(const ora_cfg* cp, const uint16_t* X, const double* dlogits, double* dWr,
+                      double* dlogit_bias) {
+  const ora_cfg c = *cp;
+  const int H = c.H, E = c.E;
+  parallel_for(E, nthreads_of(c), [&](int64_t e) {
+    double* row = dWr + (size_t)e * H;
+    for (int h = 0; h < H; ++h) row[h] = 0.0;
+    double sb = 0;
+    for (int64_t t = 0; t < c.T; ++t) {
+      const double d = dlogits[(size_t)t * E + e];
+      sb += d;
+      if (d == 0.0) continue;
+      for (int h = 0; h < H; ++h) row[h] += d * bf(X[(size_t)t * H + h]);
+    }
+    if (dlogit_bias) dlogit_bias[e] = sb;
+  });
+}
+
+// bf16 rounding as used in mirror mode, exposed for its own test.
+void ora_round_bf16(const double* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = rbf(in[i]);
+}
+
+}  // extern "C"
