@@ -1,0 +1,425 @@
+"""Benchmark: one MoE layer forward+backward step on GB300, tokens/s.
+
+Workload (default): the Mixtral-style layer, T=4096 tokens, H=4096, E=8 experts,
+top-2 softmax router with renormalised gates, SwiGLU FFN=14336, BF16 tokens and
+expert weights, FP32 router; seeded synthetic inputs.  A step is one pass of
+the whole layer: route, permute, grouped SwiGLU MLP, combine, and their
+backwards (dX, grouped dgrad and wgrad, router gradient).
+
+Prints one JSON line.  `value` is tokens/s with inputs resident in HBM; `e2e`
+is the same metric through the C ABI with the step's inputs copied in from
+pinned host memory and its outputs (Y, dX) copied back inside the timed region.
+The grouped GEMM is the dominant kernel; its roofline is reported against the
+measured dense BF16 peak.  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as S  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "MoE layer fwd+bwd tokens/s and grouped-GEMM TFLOPS (% BF16 peak) on 1 GB300"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- inputs
+
+
+def upload_normal_bf16(shape, seed, tid, std, device, chunk_elems=1 << 27):
+    import torch
+    n = int(np.prod(shape))
+    out = torch.empty(n, dtype=torch.bfloat16, device=device)
+    stage = torch.empty(min(n, chunk_elems), dtype=torch.bfloat16, pin_memory=True)
+    for s in range(0, n, chunk_elems):
+        m = min(chunk_elems, n - s)
+        S.fill_normal_bf16(stage.data_ptr(), m, seed, tid, std, start=s)
+        out[s:s + m].copy_(stage[:m], non_blocking=False)
+    return out.view(*shape)
+
+
+def device_inputs(w, seed, device):
+    import torch
+    import mixture_experts_layer_topk_gb300 as M
+    T, H, E, F = w.T, w.H, w.E, w.F
+    W_r = torch.from_numpy(S.normal_f32(E * H, seed, S.TID_WR, w.wr_std)).view(E, H).to(device)
+    lb = torch.from_numpy(S.skew_logit_bias(E)).to(device) if w.skew else None
+    sb = torch.from_numpy(S.normal_f32(E, seed, S.TID_SEL_BIAS, 0.1)).to(device) if w.sel_bias else None
+    W13 = upload_normal_bf16((E, 2 * F, H), seed, S.TID_W13, w.w_std, device)
+    W2 = upload_normal_bf16((E, H, F), seed, S.TID_W2, w.w_std, device)
+    W13s = W2s = None
+    if w.F_shared:
+        W13s = upload_normal_bf16((2 * w.F_shared, H), seed, S.TID_W13S, w.w_std, device)
+        W2s = upload_normal_bf16((H, w.F_shared), seed, S.TID_W2S, w.w_std, device)
+    weights = M.LayerWeights(W_r=W_r, W13=W13, W2=W2, logit_bias=lb, sel_bias=sb, W13_s=W13s, W2_s=W2s)
+    X = upload_normal_bf16((T, H), seed, S.TID_X, w.x_std, device)
+    dY = upload_normal_bf16((T, H), seed, S.TID_DY, w.dy_std, device)
+    return weights, X, dY
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ---------------------------------------------------------------- our arm
+
+
+STAGES = ["router", "permute", "gemm_fwd", "combine", "combine_bwd", "gemm_bwd", "router_bwd", "permute_bwd"]
+
+
+def run_step(layer, X, dY, ev=None):
+    """One forward+backward through the C ABI; ev: list of len(STAGES)+1 events."""
+    import mixture_experts_layer_topk_gb300 as M
+    c, w = layer.cfg, layer.w
+    rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+    rec(0)
+    M.moe_router_topk(c, X, w.W_r, w.logit_bias, w.sel_bias, layer.logits, layer.scores, layer.topk_idx,
+                      layer.gates, layer.counts, layer.ws)
+    rec(1)
+    M.moe_permute(c, X, layer.topk_idx, layer.counts, layer.offsets, layer.tile_offsets, layer.row_id_map,
+                  layer.slot_src, layer.Xperm, layer.ws)
+    rec(2)
+    M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
+                             layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
+                             layer.Yshared, layer.ws)
+    rec(3)
+    M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, layer.gates, layer.Yshared, layer.Y)
+    rec(4)
+    M.moe_unpermute_combine_bwd(c, dY, layer.Yperm, layer.row_id_map, layer.gates, layer.offsets, layer.counts,
+                                layer.dYperm, layer.dgates)
+    rec(5)
+    M.moe_grouped_swiglu_mlp_bwd(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, w.W13, w.W2,
+                                 layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm, layer.dW13, layer.dW2,
+                                 X if c.F_shared else None, dY if c.F_shared else None, w.W13_s, w.W2_s,
+                                 layer.GU_s, layer.A_s, layer.dGU_s, layer.dX_shared, layer.dW13_s, layer.dW2_s,
+                                 layer.ws)
+    rec(6)
+    M.moe_router_topk_bwd(c, X, w.W_r, layer.logits, layer.scores, layer.topk_idx, layer.gates, layer.dgates,
+                          layer.dW_r, layer.dlogit_bias if w.logit_bias is not None else None, layer.dX_router,
+                          layer.ws)
+    rec(7)
+    M.moe_permute_bwd(c, layer.dXperm, layer.row_id_map, layer.dX_router, layer.dX_shared, layer.dX)
+    rec(8)
+
+
+def launches_per_step(w):
+    """Kernels of ours launched by run_step (memsets are not counted)."""
+    n = 1                         # router
+    n += 3                        # chunk histogram, scan, scatter
+    n += 2 + (2 if w.F_shared else 0)      # FC1 (+SwiGLU), FC2
+    n += 1 + 1                    # combine, combine backward
+    n += 4 + (4 if w.F_shared else 0)      # FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad
+    n += 1 + (1 if w.skew else 0) + 2      # dlogits, (bias column sums), dW_r, dX_router
+    n += 1                        # permute backward
+    return n
+
+
+def hbm_bytes(w):
+    """Algorithmic bytes of the HBM-bound stages (index maps excluded)."""
+    T, H, S_ = w.T, w.H, w.T * w.k
+    sh = w.F_shared > 0
+    return {
+        "permute": T * H * 2 + S_ * H * 2,
+        "combine": S_ * H * 2 + T * H * 2 + (T * H * 2 if sh else 0),
+        "combine_bwd": T * H * 2 + 2 * S_ * H * 2,
+        "permute_bwd": S_ * H * 2 + T * H * 4 + T * H * 2 + (T * H * 2 if sh else 0),
+    }
+
+
+def traffic_record(kernel, workload):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        rec = d.get(f"{kernel}:{workload}")
+        if not rec:
+            return None
+        from mixture_experts_layer_topk_gb300 import build as B
+        if rec.get("source_digest") != B._digest():
+            return None
+        return rec.get("bytes_per_step")
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, seed, budget_s=15.0):
+    """The CPU oracle's whole-layer forward+backward on the first n tokens of the same workload."""
+    import oracle as O
+    inp = S.host_inputs(w, seed=seed)
+
+    def one(n):
+        sub = w.replace(T=n)
+        si = dict(inp)
+        si["X"] = inp["X"][:n]
+        si["dY"] = inp["dY"][:n]
+        t0 = time.perf_counter()
+        O.full_layer(sub, si, mirror=True)
+        return time.perf_counter() - t0
+
+    n0 = 2
+    t0 = one(n0)
+    n = max(1, min(w.T, int(n0 * budget_s / max(t0, 1e-3))))
+    t = one(n)
+    return {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"full layer forward+backward (router, dispatch, all {w.E} experts' dgrad and wgrad) of the "
+                      f"first {n} of {w.T} tokens, double accumulation, {t:.1f} s wall"}
+
+
+def bench_ours(args, w):
+    import torch
+    import mixture_experts_layer_topk_gb300 as M
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    weights, X, dY = device_inputs(w, args.seed, dev)
+    cfg = M.config_from(w)
+    layer = M.MoELayer(cfg, weights, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if ws_ > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        run_step(layer, X, dY)
+    barrier()
+    if layer.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # timed region: K steps, events around every stage on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        run_step(layer, X, dY, evs[i])
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = {s: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j, s in enumerate(STAGES)}
+    if layer.device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+
+    # end to end through the C ABI with host buffers
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    dYh = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
+    Xh.copy_(X)
+    dYh.copy_(dY)
+    Yh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Xd = torch.empty_like(X)
+    dYd = torch.empty_like(dY)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        Xd.copy_(Xh, non_blocking=True)
+        dYd.copy_(dYh, non_blocking=True)
+        run_step(layer, Xd, dYd)
+        Yh.copy_(layer.Y, non_blocking=True)
+        dXh.copy_(layer.dX, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    t_local = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t_local[0]), float(t_local[1])
+    if rank != 0:
+        return None
+
+    ms_per_step = total_ms / args.steps
+    tokens = w.T * ws_
+    value = tokens / (ms_per_step / 1e3)
+    pk, pk_kind = peaks()
+    gemm_flop = M.gemm_flops(cfg)
+    gemm_ms = stage_ms["gemm_fwd"] + stage_ms["gemm_bwd"]
+    gemm_tflops = gemm_flop / (gemm_ms / 1e3) / 1e12
+    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    traffic = traffic_record("k_grouped_gemm", w.name)
+    hb = hbm_bytes(w)
+    hbm = {}
+    for s, b in hb.items():
+        gbs = b / (stage_ms[s] / 1e3) / 1e9
+        hbm[s] = {"achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 3),
+                  "ms": round(stage_ms[s], 4)}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs)",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared,
+                   "router": ("softmax" if w.score_fn == 0 else "sigmoid") + (", renorm" if w.renorm else ""),
+                   "l2": "inputs larger than L2 (expert weights %.2f GB re-read every step)" %
+                         (w.E * 3 * w.F * w.H * 2 / 1e9),
+                   "parallelism": "replicas" if ws_ > 1 else "single GPU"},
+        "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_bf16_peak": round(gemm_tflops / peak_t, 3),
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "roofline": {"kernel": "k_grouped_gemm (FC1+SwiGLU, FC2, FC2 dgrad+dSwiGLU, FC2 wgrad, FC1 dgrad, FC1 wgrad)",
+                     "bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / peak_t, 3), "peak_source": f"{pk_kind} bf16 sustained",
+                     "traffic": traffic},
+        "hbm_stages": hbm,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "e2e": {"value": round(tokens / (e2e_ms / args.steps / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * X.numel() * 2, "d2h_bytes_per_step": 2 * X.numel() * 2},
+    }
+    if ws_ == 1 and not args.no_cpu_baseline:
+        del layer, weights, X, dY
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = cpu_baseline(w, args.seed)
+    return line
+
+
+def bench_reference(args, w):
+    """The CPU oracle as the reference arm: each step is the oracle's whole-layer
+    forward+backward on a bounded sample of the workload's tokens."""
+    import oracle as O
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    inp = S.host_inputs(w, seed=args.seed)
+
+    def step(n, off):
+        sub = w.replace(T=n)
+        si = dict(inp)
+        si["X"] = np.ascontiguousarray(inp["X"][off:off + n])
+        si["dY"] = np.ascontiguousarray(inp["dY"][off:off + n])
+        O.full_layer(sub, si, mirror=True)
+
+    t0 = time.perf_counter()
+    step(2, 0)
+    t_probe = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(w.T, int(2 * budget / max(t_probe, 1e-3))))
+    for i in range(args.warmup):
+        step(n, (i * n) % max(1, w.T - n))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(n, (i * n) % max(1, w.T - n))
+    dt = time.perf_counter() - t0
+    v = n * args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": ws_,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normal inputs)",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared},
+            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{n} of {w.T} tokens per step, whole-layer forward+backward"},
+            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = S.WORKLOADS[args.workload]
+    line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/* C ABI of the single-GPU dropless top-k mixture-of-experts layer (sm_103a).
+ *
+ * The layer runs four stages, as laid out in "Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core" (summary page, section
+ * "Method"): Route (a linear router kept in FP32 with softmax or sigmoid
+ * scoring and top-k selection), Dispatch (permute tokens so that each
+ * expert's tokens are contiguous), Compute (all experts run as one grouped
+ * GEMM) and Combine (gate-weighted unpermute and sum).  The same section names
+ * the compute recipes this library follows: grouped GEMM, kernel fusion and
+ * sync-free dropless execution that CUDA Graphs can capture.
+ *
+ * Conventions for every entry point below:
+ *  - Pointers marked (device) point to GPU memory; the caller allocates and
+ *    owns every buffer, including the workspace.  The library never
+ *    allocates, frees or synchronises on these calls.
+ *  - bf16 tensors are passed as raw 16-bit patterns (moe_bf16).  All tensors
+ *    are dense row-major with the shapes given, and 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, or NULL for the
+ *    legacy default stream) and can be captured into a CUDA Graph: no call
+ *    reads a device value back to the host.
+ *  - Arguments are checked on the host before any launch; a bad argument
+ *    returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a valid but
+ *    unsupported shape) and launches nothing.  A launch failure returns
+ *    MOE_ERR_CUDA.  Faults found inside kernels (a pipeline wait that ran out
+ *    of time, inconsistent routing inputs) set an error word in the
+ *    workspace, read by moe_read_device_error().
+ *
+ * Notation: T tokens, H hidden size, E experts, k experts per token, F expert
+ * FFN size, Fs shared-expert FFN size, S = T*k assignments, and R =
+ * moe_max_rows() rows in the permuted buffers (S plus per-expert padding).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_CUDA = 4,
+  MOE_ERR_TIMEOUT = 5,
+  MOE_ERR_DEVICE = 6
+} moe_status;
+
+/* Layer configuration (plain data, passed by pointer, read only during the call).
+ *  T, H, E, k, F  sizes; H and F must be multiples of 128, 1 <= k <= E <= 256, k <= 32.
+ *  F_shared       size of the always-on shared expert (0: none); multiple of 128.
+ *  score_fn       0: softmax over the E logits; 1: sigmoid of each logit.
+ *  renorm         1: gates renormalised over the k selected experts.
+ *  gate_scale     multiplies every gate after renormalisation (e.g. 2.5).
+ *  n_group        >1: group-limited routing over n_group contiguous groups of E/n_group experts.
+ *  topk_group     groups kept when n_group > 1 (topk_group * E/n_group >= k).
+ *  group_score    0: group score = sum of the group's two largest keys; 1: its largest key.
+ *  align          row alignment of every expert segment in the permuted buffers:
+ *                 128 for the grouped GEMM; 1 is accepted by the routing/permute calls only.
+ */
+typedef struct {
+  int32_t T, H, E, k, F, F_shared;
+  int32_t score_fn;
+  int32_t renorm;
+  float gate_scale;
+  int32_t n_group, topk_group, group_score;
+  int32_t align;
+  int32_t reserved;
+} moe_config;
+
+/* Short text for a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* R: rows of every permuted buffer (Xperm, GU, A, Yperm, dYperm, dGU, dXperm)
+ * and entries of slot_src: T*k + E*(align-1).  Rows from offsets[E] to R are never written. */
+moe_status moe_max_rows(const moe_config* cfg, int64_t* R);
+
+/* Bytes of device workspace all calls of this configuration need.  The
+ * workspace holds the device error word, per-chunk routing histograms and the
+ * router-gradient scratch.  Initialise it once with moe_workspace_init(). */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Zeroes the workspace (including the error word), asynchronously on stream. */
+moe_status moe_workspace_init(const moe_config* cfg, void* ws, void* stream);
+
+/* Synchronises `stream`, then returns the device error word (0 = none; else a
+ * moe_status value) and clears it.  Not for use inside a graph capture. */
+moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
+
+/* Route.  ("Method": the router is a learned linear projection, optionally kept
+ * in FP32, followed by softmax or sigmoid scoring and top-k selection.)
+ *  X        [T,H] bf16 (device)      tokens
+ *  W_r      [E,H] fp32 (device)      router weight
+ *  logit_bias [E] fp32 (device, nullable)  added to the logits (enters gates and gradients)
+ *  sel_bias [E] fp32 (device, nullable)    added to the selection key only
+ *  logits   [T,E] fp32 out           X W_r^T + logit_bias, FP32 accumulation
+ *  scores   [T,E] fp32 out           softmax(logits) or sigmoid(logits)
+ *  topk_idx [T,k] int32 out          selected experts in descending key order,
+ *                                    key = logit + sel_bias (softmax) or score + sel_bias (sigmoid),
+ *                                    exact ties to the lower expert index
+ *  gates    [T,k] fp32 out           combine weights (renormalised, times gate_scale)
+ *  counts   [E] int32 out            tokens per expert */
+moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float* W_r,
+                           const float* logit_bias, const float* sel_bias, float* logits, float* scores,
+                           int32_t* topk_idx, float* gates, int32_t* counts, void* ws, void* stream);
+
+/* Dispatch.  ("Method": the dispatcher permutes tokens so that the tokens of
+ * one expert are contiguous, as the grouped GEMM needs; dropless, no capacity.)
+ *  X            [T,H] bf16 (device)
+ *  topk_idx     [T,k] int32 (device), counts [E] int32 (device): from moe_router_topk
+ *  offsets      [E+1] int32 out   segment starts; offsets[e+1]-offsets[e] = counts[e] rounded up to align
+ *  tile_offsets [E+1] int32 out   prefix sums of ceil(counts[e]/128) (the grouped GEMM's M-tile schedule)
+ *  row_id_map   [T,k] int32 out   permuted row of assignment (t,j); tokens keep their order within an expert
+ *  slot_src     [R] int32 out     inverse map: row -> t*k+j, or -1 for a padding row
+ *  Xperm        [R,H] bf16 out    permuted tokens; padding rows are zero */
+moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
+                       moe_bf16* Xperm, void* ws, void* stream);
+
+/* Compute: all experts' SwiGLU MLPs in two grouped GEMM launches.  ("Method":
+ * all local experts run in one grouped GEMM call; SwiGLU is the GLU variant of
+ * "GLU Variants Improve Transformer", cited on the index page.)
+ *  Xperm   [R,H] bf16 (device)       offsets, tile_offsets: from moe_permute
+ *  W13     [E,2F,H] bf16 (device)    rows 0..F-1 = W_gate, rows F..2F-1 = W_up
+ *  W2      [E,H,F] bf16 (device)     W_down
+ *  GU      [R,2F] bf16 out           pre-activations [g | u] (saved for backward)
+ *  A       [R,F] bf16 out            silu(g) * u, formed from the FP32 accumulators
+ *  Yperm   [R,H] bf16 out            expert outputs
+ * Shared expert (only when F_shared > 0; all six pointers must then be non-null):
+ *  X [T,H] bf16, W13_s [2Fs,H], W2_s [H,Fs] (device); GU_s [T,2Fs], A_s [T,Fs], Yshared [T,H] out. */
+moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                  const int32_t* tile_offsets, const moe_bf16* W13, const moe_bf16* W2,
+                                  moe_bf16* GU, moe_bf16* A, moe_bf16* Yperm, const moe_bf16* X,
+                                  const moe_bf16* W13_s, const moe_bf16* W2_s, moe_bf16* GU_s, moe_bf16* A_s,
+                                  moe_bf16* Yshared, void* ws, void* stream);
+
+/* Combine.  ("Method": the fourth stage sums each token's gate-weighted expert outputs.)
+ *  Y[t] = sum_j gates[t,j] * Yperm[row_id_map[t,j]] (+ Yshared[t]), FP32 sum, one bf16 rounding.
+ *  Yshared [T,H] bf16 (device, nullable);  Y [T,H] bf16 out. */
+moe_status moe_unpermute_combine(const moe_config* cfg, const moe_bf16* Yperm, const int32_t* row_id_map,
+                                 const float* gates, const moe_bf16* Yshared, moe_bf16* Y, void* stream);
+
+/* Backward of the combine for upstream gradient dY [T,H] bf16:
+ *  dYperm[row_id_map[t,j]] = bf16(gates[t,j] * dY[t]); padding rows of dYperm are zeroed
+ *    (offsets, counts locate them);
+ *  dgates[t,j] = <dY[t], Yperm[row_id_map[t,j]]>, FP32 accumulation.
+ *  dYperm [R,H] bf16 out; dgates [T,k] fp32 out. */
+moe_status moe_unpermute_combine_bwd(const moe_config* cfg, const moe_bf16* dY, const moe_bf16* Yperm,
+                                     const int32_t* row_id_map, const float* gates, const int32_t* offsets,
+                                     const int32_t* counts, moe_bf16* dYperm, float* dgates, void* stream);
+
+/* Backward of the experts (four grouped GEMM launches, plus four for the shared expert):
+ *  dGU    [R,2F] bf16 out   dA = dYperm_e W2_e; dG = dA*u*silu'(g), dU = dA*silu(g) (fused epilogue)
+ *  dXperm [R,H] bf16 out    dGU_e W13_e
+ *  dW2    [E,H,F] bf16 out  dYperm_e^T A_e   (FP32 accumulation; an expert with no tokens gets 0)
+ *  dW13   [E,2F,H] bf16 out dGU_e^T Xperm_e
+ * Shared expert (F_shared > 0): X, dY [T,H], W13_s, W2_s, GU_s, A_s (device) in;
+ *  dGU_s [T,2Fs], dX_shared [T,H], dW13_s [2Fs,H], dW2_s [H,Fs] bf16 out. */
+moe_status moe_grouped_swiglu_mlp_bwd(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                      const int32_t* tile_offsets, const int32_t* counts, const moe_bf16* W13,
+                                      const moe_bf16* W2, const moe_bf16* GU, const moe_bf16* A,
+                                      const moe_bf16* dYperm, moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* dW13,
+                                      moe_bf16* dW2, const moe_bf16* X, const moe_bf16* dY,
+                                      const moe_bf16* W13_s, const moe_bf16* W2_s, const moe_bf16* GU_s,
+                                      const moe_bf16* A_s, moe_bf16* dGU_s, moe_bf16* dX_shared,
+                                      moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws, void* stream);
+
+/* Backward of the router.  dlogits = exact gradient of the gates w.r.t. the
+ * logits for the fixed selection (zero for unselected experts when renorm=1);
+ * no gradient flows through the selection or sel_bias.
+ *  logits, scores [T,E] fp32, topk_idx [T,k], gates, dgates [T,k] fp32 (device) in
+ *  dW_r [E,H] fp32 out = dlogits^T X;  dlogit_bias [E] fp32 out (nullable) = column sums of dlogits;
+ *  dX_router [T,H] fp32 out = dlogits W_r. */
+moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const float* W_r, const float* logits,
+                               const float* scores, const int32_t* topk_idx, const float* gates,
+                               const float* dgates, float* dW_r, float* dlogit_bias, float* dX_router, void* ws,
+                               void* stream);
+
+/* Backward of the dispatch: dX[t] = sum_j dXperm[row_id_map[t,j]] + dX_router[t] + dX_shared[t],
+ * FP32 sum, one bf16 rounding.  dX_router [T,H] fp32 and dX_shared [T,H] bf16 are nullable. */
+moe_status moe_permute_bwd(const moe_config* cfg, const moe_bf16* dXperm, const int32_t* row_id_map,
+                           const float* dX_router, const moe_bf16* dX_shared, moe_bf16* dX, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

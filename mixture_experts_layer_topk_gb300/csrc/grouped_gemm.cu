@@ -1,0 +1,539 @@
+// Compute stage: the experts' SwiGLU MLPs as persistent grouped GEMMs on the
+// sm_100-family tensor cores (tcgen05.mma, accumulators in tensor memory,
+// operands staged by TMA), forward and backward.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (summary
+// page, "Method"): all local experts run in a single grouped GEMM call; the
+// compute recipes are grouped GEMM, kernel fusion and sync-free execution.
+// Here each of the six expert GEMMs of a training step is one launch over all
+// experts; the expert segments and the M-tile schedule are read on the device
+// (offsets / tile_offsets written by the dispatch), so nothing goes back to
+// the host.  SwiGLU ("GLU Variants Improve Transformer", cited on the index
+// page) is fused into the FC1 epilogue, and its backward into the FC2-dgrad
+// epilogue.
+//
+// One CTA per SM, 6 warps: warp 0 issues TMA loads into a ring of shared
+// memory stages, warp 1 allocates tensor memory and issues tcgen05.mma from
+// one thread, warps 2-5 drain the double-buffered accumulator (tcgen05.ld),
+// apply the epilogue and store bf16.  Tiles are 128 x BN x 64 (bf16, 128-byte
+// swizzle).  Every wait is bounded; a wait that runs out records
+// MOE_ERR_TIMEOUT in the device error word and the CTA unwinds.
+//
+// The three operand layouts:
+//   FWD   D[m,n] = sum_k A[m,k] B[n,k]  A K-major (rows of a permuted buffer), B K-major (weights)
+//   DGRAD D[m,n] = sum_k A[m,k] B[k,n]  A K-major, B MN-major (weights used transposed)
+//   WGRAD D[m,n] = sum_r A[r,m] B[r,n]  both MN-major, K = the expert's rows (ragged)
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int kThreads = 192;
+
+enum { MODE_FWD = 0, MODE_DGRAD = 1, MODE_WGRAD = 2 };
+enum { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+
+struct GemmArgs {
+  int E;
+  int K;           // FWD / DGRAD: reduction length
+  int n_tiles;     // tiles along N
+  int m_tiles;     // WGRAD: tiles along M of one expert's output
+  int dense_rows;  // > 0: a single dense segment of this many rows (the shared expert)
+  const int32_t* seg_off;   // [E+1] segment starts in the permuted buffers
+  const int32_t* tile_off;  // [E+1] prefix of M tiles per expert
+  const int32_t* counts;    // [E] rows per expert
+  uint16_t* D;
+  int64_t ldd;
+  int64_t d_estride;        // WGRAD: elements between experts' outputs
+  uint16_t* D2;             // EPI_SWIGLU: activation output
+  int64_t ldd2;
+  const uint16_t* GU;       // EPI_DSWIGLU: saved pre-activations
+  int64_t ldgu;
+  int F;                    // SWIGLU / DSWIGLU: column offset of the "up" half
+  int* err;
+};
+
+struct Tile {
+  int e, m0, n0, k0, kb;
+};
+
+template <int MODE, int EPI, int BN>
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
+                                            const int* s_cnt) {
+  Tile r;
+  if constexpr (MODE != MODE_WGRAD) {
+    int e = 0, m, n;
+    if (g.dense_rows > 0) {
+      const int mt = (g.dense_rows + BM - 1) / BM;
+      n = t / mt;
+      m = t % mt;
+      r.m0 = m * BM;
+    } else {
+      int lo = 0, hi = g.E;  // s_tile[lo]*nt <= t < s_tile[hi]*nt
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tile[mid] * g.n_tiles <= t)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      e = lo;
+      const int local = t - s_tile[e] * g.n_tiles;
+      const int mt = s_tile[e + 1] - s_tile[e];
+      n = local / mt;
+      m = local % mt;
+      r.m0 = s_seg[e] + m * BM;
+    }
+    r.e = e;
+    r.n0 = n * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+    r.k0 = 0;
+    r.kb = g.K / BK;
+  } else {
+    const int per = g.m_tiles * g.n_tiles;
+    const int e = t / per, local = t % per;
+    r.e = e;
+    r.m0 = (local % g.m_tiles) * BM;
+    r.n0 = (local / g.m_tiles) * BN;
+    if (g.dense_rows > 0) {
+      r.k0 = 0;
+      r.kb = (g.dense_rows + BK - 1) / BK;
+    } else {
+      r.k0 = s_seg[e];
+      r.kb = (s_cnt[e] + BK - 1) / BK;
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
+}
+
+template <int MODE, int EPI, int BN, int ST>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const GemmArgs g) {
+  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * STAGE);
+  uint64_t* empty = full + ST;
+  uint64_t* acc_full = empty + ST;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  int* s_seg = reinterpret_cast<int*>(tmem_holder + 4);
+  int* s_tile = s_seg + 260;
+  int* s_cnt = s_tile + 260;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (g.dense_rows <= 0) {
+    for (int i = threadIdx.x; i <= g.E; i += kThreads) {
+      s_seg[i] = g.seg_off[i];
+      if (MODE != MODE_WGRAD) s_tile[i] = g.tile_off[i];
+      if (MODE == MODE_WGRAD && i < g.E) s_cnt[i] = g.counts[i];
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  int total;
+  if constexpr (MODE != MODE_WGRAD) {
+    const int mt = g.dense_rows > 0 ? (g.dense_rows + BM - 1) / BM : s_tile[g.E];
+    total = mt * g.n_tiles;
+  } else {
+    total = (g.dense_rows > 0 ? 1 : g.E) * g.m_tiles * g.n_tiles;
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+        for (int kb = 0; kb < tl.kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = tiles + stage * STAGE;
+          uint8_t* sb = sa + A_BYTES;
+          uint64_t* bar = &full[stage];
+          mbar_arrive_expect_tx(bar, STAGE);
+          const int kc = kb * BK;
+          if constexpr (MODE == MODE_WGRAD) {
+            tma_load_2d(sa, &mapA, bar, tl.m0, tl.k0 + kc);
+            tma_load_2d(sa + 8192, &mapA, bar, tl.m0 + 64, tl.k0 + kc);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, tl.k0 + kc);
+          } else {
+            tma_load_2d(sa, &mapA, bar, kc, tl.m0);
+            if constexpr (MODE == MODE_FWD) {
+              if constexpr (EPI == EPI_SWIGLU) {
+                tma_load_3d(sb, &mapB, bar, kc, tl.n0, tl.e);
+                tma_load_3d(sb + B_BYTES / 2, &mapB, bar, kc, g.F + tl.n0, tl.e);
+              } else {
+                tma_load_3d(sb, &mapB, bar, kc, tl.n0, tl.e);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, kc, tl.e);
+            }
+          }
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == ST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // nothing may still be landing in shared memory when the CTA exits
+      for (int s = 0; s < ST; ++s)
+        if (used >> s & 1)
+          if (!mbar_wait(&full[s], last_par >> s & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+        if (tl.kb == 0) continue;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+          set_device_error(g.err, MOE_ERR_TIMEOUT, 3);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < tl.kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            set_device_error(g.err, MOE_ERR_TIMEOUT, 4);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + stage * STAGE);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                                   : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = MODE == MODE_FWD ? smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                                 : smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+            umma_f16(d, ad, bd, IDESC, (kb | kk) != 0);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == ST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // every issued MMA has finished before tensor memory is released
+      umma_commit(done_bar);
+      if (!mbar_wait(done_bar, 0)) set_device_error(g.err, MOE_ERR_TIMEOUT, 5);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // row within the tile = tensor-memory lane
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+      if (tl.kb == 0) {
+        // an expert without rows: its weight gradient is zero
+        uint16_t* out = g.D + (int64_t)tl.e * g.d_estride + (int64_t)(tl.m0 + r) * g.ldd + tl.n0;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < BN / 8; ++i) reinterpret_cast<uint4*>(out)[i] = z;
+        continue;
+      }
+      if (!mbar_wait(&acc_full[acc], acc_phase)) {
+        set_device_error(g.err, MOE_ERR_TIMEOUT, 6);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const int64_t row = tl.m0 + r;
+      const bool valid = g.dense_rows <= 0 || MODE == MODE_WGRAD || row < g.dense_rows;
+      if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32(tbase + c * 32, gr);
+          tmem_ld32(tbase + BN / 2 + c * 32, ur);
+          tmem_ld_wait();
+          if (valid) {
+            float gv[32], uv[32], av[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              gv[i] = __uint_as_float(gr[i]);
+              uv[i] = __uint_as_float(ur[i]);
+              av[i] = gv[i] / (1.0f + __expf(-gv[i])) * uv[i];
+            }
+            const int col = tl.n0 + c * 32;
+            store32(g.D + row * g.ldd + col, gv);
+            store32(g.D + row * g.ldd + g.F + col, uv);
+            store32(g.D2 + row * g.ldd2 + col, av);
+          }
+        }
+      } else if constexpr (EPI == EPI_DSWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(tbase + c * 32, dr);
+          tmem_ld_wait();
+          if (valid) {
+            const int col = tl.n0 + c * 32;
+            const uint4* gp = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + col);
+            const uint4* up = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + g.F + col);
+            float dg[32], du[32];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float gf[8], uf[8];
+              unpack8(gp[v], gf);
+              unpack8(up[v], uf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float da = __uint_as_float(dr[8 * v + i]);
+                const float s = 1.0f / (1.0f + __expf(-gf[i]));
+                const float sl = gf[i] * s;
+                dg[8 * v + i] = da * uf[i] * (s * (1.0f + gf[i] * (1.0f - s)));
+                du[8 * v + i] = da * sl;
+              }
+            }
+            store32(g.D + row * g.ldd + col, dg);
+            store32(g.D + row * g.ldd + g.F + col, du);
+          }
+        }
+      } else {
+        uint16_t* out = g.D + (int64_t)tl.e * g.d_estride + row * g.ldd + tl.n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t vr[32];
+          tmem_ld32(tbase + c * 32, vr);
+          tmem_ld_wait();
+          if (valid) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
+            store32(out + c * 32, v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int MODE, int EPI, int BN>
+struct Kern {
+  static constexpr int ST = BN == 256 ? 4 : 6;
+  static constexpr int STAGE = (BM + BN) * BK * 2;
+  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + (2 * ST + 5) * 8 + 16 + 3 * 260 * 4;
+};
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle.  dims/strides innermost first (strides in elements).
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_elems,
+              uint32_t box0, uint32_t box1) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bd[3] = {box0, box1, 1}, es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gd[i] = dims[i];
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_elems[i] * 2;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t b0, uint32_t b1) {
+  const uint64_t dims[2] = {inner, outer}, st[1] = {inner};
+  return make_map(m, base, 2, dims, st, b0, b1);
+}
+bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer, uint32_t b0,
+           uint32_t b1) {
+  const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
+  return make_map(m, base, 3, dims, st, b0, b1);
+}
+
+template <int MODE, int EPI, int BN>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int max_tiles, int nsm,
+                   cudaStream_t st) {
+  using K = Kern<MODE, EPI, BN>;
+  static bool attr = false;
+  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST>;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  if (max_tiles <= 0) return cudaSuccess;
+  const int grid = max_tiles < nsm ? max_tiles : nsm;
+  kern<<<grid, kThreads, K::smem, st>>>(a, b, g);
+  return cudaGetLastError();
+}
+
+inline int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
+
+}  // namespace
+
+// X1 = rows of A [rows, K] (Xperm or X), W13 [E, 2F, K]: GU [rows, 2F], A [rows, F].
+cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
+                           int* err, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, X1, s.H, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 128))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = GU; g.ldd = 2 * (int64_t)s.F; g.D2 = Aact; g.ldd2 = s.F; g.F = s.F; g.err = err;
+  return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+// A [rows, F], W2 [E, H, F]: Y [rows, H].
+cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
+                           cudaStream_t st) {
+  const int bn = pick_bn(s.H);
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, Aact, s.F, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, bn)) return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = Y; g.ldd = s.H; g.err = err;
+  return bn == 256 ? launch<MODE_FWD, EPI_STORE, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_FWD, EPI_STORE, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+// dY [rows, H], W2 [E, H, F], GU [rows, 2F]: dGU [rows, 2F].
+cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
+                             uint16_t* dGU, int* err, cudaStream_t st) {
+  const int bn = pick_bn(s.F);
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, dYp, s.H, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, 64)) return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.H; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dGU; g.ldd = 2 * (int64_t)s.F; g.GU = GU; g.ldgu = 2 * (int64_t)s.F; g.F = s.F; g.err = err;
+  return bn == 256 ? launch<MODE_DGRAD, EPI_DSWIGLU, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_DGRAD, EPI_DSWIGLU, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+// dGU [rows, 2F], W13 [E, 2F, H]: dX [rows, H].
+cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* W13, uint16_t* dX1, int* err,
+                             cudaStream_t st) {
+  const int bn = pick_bn(s.H);
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 64))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = 2 * s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dX1; g.ldd = s.H; g.err = err;
+  return bn == 256 ? launch<MODE_DGRAD, EPI_STORE, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_DGRAD, EPI_STORE, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+// dW2 [E, H, F] = dY^T A per expert.
+cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* Aact, uint16_t* dW2, int* err,
+                             cudaStream_t st) {
+  const int bn = pick_bn(s.F);
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, dYp, s.H, s.rows, 64, 64) || !map2d(&mb, Aact, s.F, s.rows, 64, 64)) return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.m_tiles = s.H / 128; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
+  const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, g, tiles, s.nsm, st)
+                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, g, tiles, s.nsm, st);
+}
+
+// dW13 [E, 2F, H] = dGU^T X per expert.
+cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
+                             cudaStream_t st) {
+  const int bn = pick_bn(s.H);
+  CUtensorMap ma, mb;
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !map2d(&mb, X1, s.H, s.rows, 64, 64))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.m_tiles = 2 * s.F / 128; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
+  const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, g, tiles, s.nsm, st)
+                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, g, tiles, s.nsm, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,53 @@
+// Internal launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Sizes of one grouped GEMM launch.
+struct GemmShape {
+  int E, H, F;                  // F: expert FFN size (Fs for the shared expert)
+  int64_t rows;                 // rows of the row-indexed operands (R, or T for the dense segment)
+  int dense_rows;               // > 0: one dense segment of this many rows (the shared expert)
+  int max_mtiles;               // host-known upper bound on M tiles (grid sizing)
+  const int32_t* offsets;       // [E+1] (device)
+  const int32_t* tile_offsets;  // [E+1] (device)
+  const int32_t* counts;        // [E] (device)
+  int nsm;
+};
+
+cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
+                               const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
+                               int32_t* counts, cudaStream_t st, int nsm);
+cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
+                              const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
+                              float* dlogit_bias, float* dX_router, float* dl, cudaStream_t st);
+cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
+                           int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
+                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, cudaStream_t st);
+cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int32_t* row_id_map, const float* gates,
+                           const uint16_t* Ysh, uint16_t* Y, cudaStream_t st);
+cudaError_t launch_combine_bwd(const moe_config& c, const uint16_t* dY, const uint16_t* Yperm,
+                               const int32_t* row_id_map, const float* gates, const int32_t* offsets,
+                               const int32_t* counts, uint16_t* dYperm, float* dgates, cudaStream_t st);
+cudaError_t launch_permute_bwd(const moe_config& c, const uint16_t* dXperm, const int32_t* row_id_map,
+                               const float* dXr, const uint16_t* dXs, uint16_t* dX, cudaStream_t st);
+
+cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
+                           int* err, cudaStream_t st);
+cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
+                           cudaStream_t st);
+cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
+                             uint16_t* dGU, int* err, cudaStream_t st);
+cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* W13, uint16_t* dX1, int* err,
+                             cudaStream_t st);
+cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* Aact, uint16_t* dW2, int* err,
+                             cudaStream_t st);
+cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
+                             cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,604 @@
+// Route stage and its backward.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (summary
+// page, "Method"): the router is a learned linear projection of the hidden
+// states, kept in FP32, followed by softmax or sigmoid scoring and top-k
+// selection.  The kernels here fuse the projection (an FP32 GEMV / skinny
+// GEMM), the scoring, the optional group limit, the top-k (warp shuffles) and
+// the gate computation into one launch.
+//
+// Selection rule: key = logit (+ sel_bias) for softmax, sigmoid(logit)
+// (+ sel_bias) for sigmoid, formed in FP32; the k experts are listed in
+// descending key order, exact ties going to the lower expert index.  With
+// n_group > 1 the experts form contiguous groups; a group's score is the sum
+// of its two largest keys (or its largest key), the topk_group best groups
+// are kept (ties to the lower group id) and top-k runs inside them.
+#include <float.h>
+
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+struct RouteArgs {
+  const uint16_t* X;
+  const float* Wr;
+  const float* logit_bias;
+  const float* sel_bias;
+  float* logits;
+  float* scores;
+  int32_t* topk_idx;
+  float* gates;
+  int32_t* counts;
+  int T, H, E, k;
+  int score_fn, renorm;
+  float gate_scale;
+  int n_group, topk_group, group_score;
+};
+
+// (value, index) maximum over the warp; ties to the lower index.  Lanes with
+// no candidate pass (-inf, INT_MAX).
+__device__ __forceinline__ void warp_argmax(float& v, int& e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
+    if (ov > v || (ov == v && oe < e)) {
+      v = ov;
+      e = oe;
+    }
+  }
+}
+
+// Scores, selection and gates of token t by one warp.  lrow: the token's E
+// logits (bias included) in shared memory.  hist: per-CTA expert histogram.
+template <int V>
+__device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* hist) {
+  const int lane = threadIdx.x & 31;
+  const int E = a.E;
+  float l[V], key[V];
+  uint32_t excl = 0;
+  float lmax = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    const bool valid = e < E;
+    l[i] = valid ? lrow[e] : -FLT_MAX;
+    if (!valid) excl |= 1u << i;
+    lmax = fmaxf(lmax, l[i]);
+  }
+  // scores
+  float M = 0.f, Zinv = 0.f;
+  if (a.score_fn == 0) {
+    M = warp_max(lmax);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (!(excl >> i & 1)) z += expf(l[i] - M);
+    Zinv = 1.0f / warp_sum(z);
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float s = a.score_fn == 0 ? expf(l[i] - M) * Zinv : 1.0f / (1.0f + expf(-l[i]));
+      a.logits[(size_t)t * E + e] = l[i];
+      a.scores[(size_t)t * E + e] = s;
+      const float base = a.score_fn == 0 ? l[i] : s;
+      key[i] = a.sel_bias ? base + a.sel_bias[e] : base;
+    } else {
+      key[i] = -FLT_MAX;
+    }
+  }
+  // group limit
+  if (a.n_group > 1) {
+    const int per = E / a.n_group;
+    float my_gs = -FLT_MAX;
+    for (int g = 0; g < a.n_group; ++g) {
+      float v1 = -FLT_MAX;
+      int e1 = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane + 32 * i;
+        if (!(excl >> i & 1) && e / per == g && (key[i] > v1 || (key[i] == v1 && e < e1))) {
+          v1 = key[i];
+          e1 = e;
+        }
+      }
+      warp_argmax(v1, e1);
+      float gs = v1;
+      if (a.group_score == 0 && per > 1) {
+        float v2 = -FLT_MAX;
+        int e2 = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          const int e = lane + 32 * i;
+          if (!(excl >> i & 1) && e / per == g && e != e1 && (key[i] > v2 || (key[i] == v2 && e < e2))) {
+            v2 = key[i];
+            e2 = e;
+          }
+        }
+        warp_argmax(v2, e2);
+        gs = v1 + v2;
+      }
+      if (lane == g) my_gs = gs;
+    }
+    uint32_t keep = 0;
+    for (int r = 0; r < a.topk_group; ++r) {
+      float v = (lane < a.n_group && !(keep >> lane & 1)) ? my_gs : -FLT_MAX;
+      int g = (lane < a.n_group && !(keep >> lane & 1)) ? lane : INT_MAX;
+      warp_argmax(v, g);
+      keep |= 1u << g;
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(keep >> (e / per) & 1)) excl |= 1u << i;
+    }
+  }
+  // top-k: lane j ends up holding the j-th selected expert
+  int my_e = -1;
+  for (int j = 0; j < a.k; ++j) {
+    float v = -FLT_MAX;
+    int e = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int ee = lane + 32 * i;
+      if (!(excl >> i & 1) && (key[i] > v || (key[i] == v && ee < e))) {
+        v = key[i];
+        e = ee;
+      }
+    }
+    warp_argmax(v, e);
+    if (lane == j) my_e = e;
+    if ((e & 31) == lane) excl |= 1u << (e >> 5);
+  }
+  // gates
+  const bool act = lane < a.k;
+  const float lj = act ? lrow[my_e] : -FLT_MAX;
+  float g = 0.f;
+  if (a.score_fn == 0) {
+    if (a.renorm) {
+      const float m = warp_max(lj);
+      const float ex = act ? expf(lj - m) : 0.f;
+      g = a.gate_scale * ex / warp_sum(ex);
+    } else {
+      g = act ? a.gate_scale * expf(lj - M) * Zinv : 0.f;
+    }
+  } else {
+    const float s = act ? 1.0f / (1.0f + expf(-lj)) : 0.f;
+    g = a.renorm ? a.gate_scale * s / warp_sum(s) : a.gate_scale * s;
+  }
+  if (act) {
+    a.topk_idx[(size_t)t * a.k + lane] = my_e;
+    a.gates[(size_t)t * a.k + lane] = g;
+    atomicAdd(&hist[my_e], 1);
+  }
+}
+
+// E <= 32: one warp per token (TPW tokens at a time), lanes split H.
+template <int EMAX, int TPW>
+__global__ void __launch_bounds__(256) k_router_small(RouteArgs a) {
+  __shared__ float lrows[8][TPW][EMAX];
+  __shared__ int hist[EMAX];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < EMAX; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int H = a.H, E = a.E;
+  const int nvec = H / 8;  // 16-byte vectors per row
+  const int gw = blockIdx.x * 8 + warp, nw = gridDim.x * 8;
+  for (int t0 = gw * TPW; t0 < a.T; t0 += nw * TPW) {
+    float acc[TPW][EMAX];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) acc[u][e] = 0.f;
+    for (int c = lane; c < nvec; c += 32) {
+      float x[TPW][8];
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) {
+        if (t0 + u < a.T) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + u) * H) + c);
+          unpack8(v, x[u]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[u][q] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        if (e < E) {
+          const float4* w = reinterpret_cast<const float4*>(a.Wr + (size_t)e * H) + 2 * c;
+          const float4 w0 = __ldg(w), w1 = __ldg(w + 1);
+#pragma unroll
+          for (int u = 0; u < TPW; ++u) {
+            float s = acc[u][e];
+            s = fmaf(x[u][0], w0.x, s);
+            s = fmaf(x[u][1], w0.y, s);
+            s = fmaf(x[u][2], w0.z, s);
+            s = fmaf(x[u][3], w0.w, s);
+            s = fmaf(x[u][4], w1.x, s);
+            s = fmaf(x[u][5], w1.y, s);
+            s = fmaf(x[u][6], w1.z, s);
+            s = fmaf(x[u][7], w1.w, s);
+            acc[u][e] = s;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < TPW; ++u)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) acc[u][e] = warp_sum(acc[u][e]);
+    if (lane == 0) {
+#pragma unroll
+      for (int u = 0; u < TPW; ++u)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+          if (e < E) lrows[warp][u][e] = acc[u][e] + (a.logit_bias ? a.logit_bias[e] : 0.f);
+    }
+    __syncwarp();
+    for (int u = 0; u < TPW; ++u)
+      if (t0 + u < a.T) route_token<1>(a, t0 + u, lrows[warp][u], hist);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
+}
+
+// 32 < E <= EP: a CTA computes the logits of BT tokens for all experts with a
+// register-tiled FP32 GEMM (TM tokens x 8 experts per thread), then its warps
+// route the tokens.
+template <int EP, int TM>
+struct LargeCfg {
+  static constexpr int TC = EP / 8;     // threads along experts
+  static constexpr int TR = 256 / TC;   // threads along tokens
+  static constexpr int BT = TR * TM;    // tokens per CTA
+  static constexpr int BK = 16;
+  static constexpr int LS = EP + 1;     // logits row stride in shared memory
+  static constexpr size_t smem = sizeof(float) * ((size_t)BK * BT + (size_t)BK * EP + (size_t)BT * LS) +
+                                 sizeof(int) * EP;
+};
+
+template <int EP, int TM>
+__global__ void __launch_bounds__(256) k_router_large(RouteArgs a) {
+  using C = LargeCfg<EP, TM>;
+  extern __shared__ __align__(16) float sm[];
+  float* Xs = sm;                        // [BK][BT]
+  float* Ws = Xs + C::BK * C::BT;        // [BK][EP]
+  float* Ls = Ws + C::BK * EP;           // [BT][LS]
+  int* hist = reinterpret_cast<int*>(Ls + C::BT * C::LS);
+  const int tid = threadIdx.x;
+  const int tr = tid / C::TC, tc = tid % C::TC;
+  const int t0 = blockIdx.x * C::BT;
+  const int H = a.H, E = a.E;
+  for (int i = tid; i < EP; i += 256) hist[i] = 0;
+  float acc[TM][8];
+#pragma unroll
+  for (int m = 0; m < TM; ++m)
+#pragma unroll
+    for (int n = 0; n < 8; ++n) acc[m][n] = 0.f;
+  for (int k0 = 0; k0 < H; k0 += C::BK) {
+    // X tile: BT rows x 16 columns of bf16 = 2 vectors of 8 per row
+    for (int i = tid; i < C::BT * 2; i += 256) {
+      const int tt = i >> 1, half = i & 1;
+      float x[8];
+      if (t0 + tt < a.T) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + tt) * H + k0) + half);
+        unpack8(v, x);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) Xs[(half * 8 + q) * C::BT + tt] = x[q];
+    }
+    // W tile: EP rows x 16 fp32 columns = 4 float4 per row
+    for (int i = tid; i < EP * 4; i += 256) {
+      const int e = i % EP, q4 = i / EP;
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) w = __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)e * H + k0) + q4);
+      Ws[(4 * q4 + 0) * EP + e] = w.x;
+      Ws[(4 * q4 + 1) * EP + e] = w.y;
+      Ws[(4 * q4 + 2) * EP + e] = w.z;
+      Ws[(4 * q4 + 3) * EP + e] = w.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < C::BK; ++kk) {
+      float xa[TM];
+#pragma unroll
+      for (int m = 0; m < TM; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&Xs[kk * C::BT + tr * TM + m]);
+        xa[m] = v.x;
+        xa[m + 1] = v.y;
+        xa[m + 2] = v.z;
+        xa[m + 3] = v.w;
+      }
+      const float4 b0 = *reinterpret_cast<const float4*>(&Ws[kk * EP + tc * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Ws[kk * EP + tc * 8 + 4]);
+      const float wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int n = 0; n < 8; ++n) acc[m][n] = fmaf(xa[m], wb[n], acc[m][n]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int m = 0; m < TM; ++m)
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const int e = tc * 8 + n;
+      Ls[(tr * TM + m) * C::LS + e] = acc[m][n] + ((a.logit_bias && e < E) ? a.logit_bias[e] : 0.f);
+    }
+  __syncthreads();
+  const int warp = tid >> 5;
+  for (int tt = warp; tt < C::BT; tt += 8)
+    if (t0 + tt < a.T) route_token<EP / 32>(a, t0 + tt, Ls + tt * C::LS, hist);
+  __syncthreads();
+  for (int e = tid; e < E; e += 256)
+    if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
+}
+
+template <int EP, int TM>
+cudaError_t launch_large(const RouteArgs& a, cudaStream_t st) {
+  using C = LargeCfg<EP, TM>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_router_large<EP, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (a.T + C::BT - 1) / C::BT;
+  k_router_large<EP, TM><<<grid, 256, C::smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int EMAX, int TPW>
+cudaError_t launch_small(const RouteArgs& a, cudaStream_t st, int nsm) {
+  const int warps_needed = (a.T + TPW - 1) / TPW;
+  int grid = (warps_needed + 7) / 8;
+  grid = grid < 4 * nsm ? grid : 4 * nsm;
+  k_router_small<EMAX, TPW><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- backward
+
+struct RouteBwdArgs {
+  const float* logits;
+  const int32_t* topk_idx;
+  const float* gates;
+  const float* dgates;
+  float* dl;  // [T,E]
+  int T, E, k;
+  int score_fn, renorm;
+  float gate_scale;
+};
+
+// dlogits of one token per warp: the exact gradient of the gates with respect
+// to the logits for the fixed selection, applied to dgates.
+template <int V>
+__global__ void __launch_bounds__(256) k_router_dlogits(RouteBwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int E = a.E, k = a.k;
+  const float al = a.gate_scale;
+  const bool act = lane < k;
+  const int ej = act ? a.topk_idx[(size_t)t * k + lane] : 0;
+  const float gj = act ? a.gates[(size_t)t * k + lane] : 0.f;
+  const float dgj = act ? a.dgates[(size_t)t * k + lane] : 0.f;
+  const float lj = act ? a.logits[(size_t)t * E + ej] : 0.f;
+  const float* lrow = a.logits + (size_t)t * E;
+  float dlj = 0.f;        // gradient at the selected expert held by lane j
+  float dense_s = 0.f;    // softmax without renorm: sum_j dg_j p_j
+  float M = 0.f, Zinv = 0.f;
+  if (a.score_fn == 0) {
+    if (a.renorm) {
+      const float q = gj / al;
+      const float s = warp_sum(act ? q * dgj : 0.f);
+      dlj = al * q * (dgj - s);
+    } else {
+      float lmax = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) lmax = fmaxf(lmax, lrow[e]);
+      }
+      M = warp_max(lmax);
+      float z = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) z += expf(lrow[e] - M);
+      }
+      Zinv = 1.0f / warp_sum(z);
+      const float pj = act ? expf(lj - M) * Zinv : 0.f;
+      dense_s = warp_sum(act ? dgj * pj : 0.f);
+    }
+  } else {
+    const float sj = act ? 1.0f / (1.0f + expf(-lj)) : 0.f;
+    if (a.renorm) {
+      const float S = warp_sum(sj);
+      const float c = warp_sum(act ? dgj * gj : 0.f) / al;
+      dlj = (al / S) * (dgj - c) * sj * (1.0f - sj);
+    } else {
+      dlj = al * dgj * sj * (1.0f - sj);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    float v = 0.f, dgm = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej2 = __shfl_sync(0xffffffffu, ej, j);
+      const float d2 = __shfl_sync(0xffffffffu, dlj, j);
+      const float g2 = __shfl_sync(0xffffffffu, dgj, j);
+      if (ej2 == e) {
+        v = d2;
+        dgm = g2;
+      }
+    }
+    if (a.score_fn == 0 && !a.renorm && e < E) {
+      const float p = expf(lrow[e] - M) * Zinv;
+      v = al * p * (dgm - dense_s);
+    }
+    if (e < E) a.dl[(size_t)t * E + e] = v;
+  }
+}
+
+// dlogit_bias[e] = sum_t dl[t,e]; one CTA per expert, fixed summation order.
+__global__ void __launch_bounds__(256) k_colsum(const float* dl, int T, int E, float* out) {
+  const int e = blockIdx.x;
+  float s = 0.f;
+  for (int t = threadIdx.x; t < T; t += 256) s += dl[(size_t)t * E + e];
+  __shared__ float red[8];
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = 0.f;
+    for (int i = 0; i < 8; ++i) r += red[i];
+    out[e] = r;
+  }
+}
+
+// C[M,N] = sum_k A(m,k) B(k,n), FP32, 128x128 tiles, 8x8 per thread.
+// A(m,k) = A[m*lda + k] (A_KM=false) or A[k*lda + m] (A_KM=true); B(k,n) = B[k*ldb + n].
+template <bool A_KM, typename TB>
+__global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, const float* __restrict__ A, int64_t lda,
+                                               const TB* __restrict__ B, int64_t ldb, float* __restrict__ Cm,
+                                               int64_t ldc) {
+  __shared__ __align__(16) float As[8][128 + 4];
+  __shared__ __align__(16) float Bs[8][128 + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 8) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tid + 256 * r;  // 0..1023
+      int mm, kk;
+      if (A_KM) {
+        mm = i & 127;
+        kk = i >> 7;
+      } else {
+        kk = i & 7;
+        mm = i >> 3;
+      }
+      const int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < M && gk < K) v = A_KM ? A[(int64_t)gk * lda + gm] : A[(int64_t)gm * lda + gk];
+      As[kk][mm] = v;
+      const int nn = i & 127, kb = i >> 7;
+      const int gn = n0 + nn, gk2 = k0 + kb;
+      float w = 0.f;
+      if (gn < N && gk2 < K) w = (float)B[(int64_t)gk2 * ldb + gn];
+      Bs[kb][nn] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      float av[8], bv[8];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
+      av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+      av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+      bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+      bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+      if (gn < N) Cm[(int64_t)gm * ldc + gn] = acc[i][j];
+    }
+  }
+}
+
+struct Bf16In {
+  uint16_t v;
+  __device__ __forceinline__ explicit operator float() const { return __uint_as_float((uint32_t)v << 16); }
+};
+
+}  // namespace
+
+cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
+                               const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
+                               int32_t* counts, cudaStream_t st, int nsm) {
+  RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
+              c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
+              c.group_score};
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
+  if (e != cudaSuccess) return e;
+  if (c.T == 0) return cudaSuccess;
+  if (c.E <= 8) return launch_small<8, 4>(a, st, nsm);
+  if (c.E <= 16) return launch_small<16, 2>(a, st, nsm);
+  if (c.E <= 32) return launch_small<32, 1>(a, st, nsm);
+  if (c.E <= 64) return launch_large<64, 4>(a, st);
+  if (c.E <= 128) return launch_large<128, 4>(a, st);
+  return launch_large<256, 4>(a, st);
+}
+
+cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
+                              const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
+                              float* dlogit_bias, float* dX_router, float* dl, cudaStream_t st) {
+  if (c.T == 0) {
+    cudaError_t e = cudaMemsetAsync(dW_r, 0, sizeof(float) * c.E * c.H, st);
+    if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, sizeof(float) * c.E, st);
+    return e;
+  }
+  RouteBwdArgs a{logits, topk_idx, gates, dgates, dl, c.T, c.E, c.k, c.score_fn, c.renorm, c.gate_scale};
+  const int grid = (c.T + 7) / 8;
+  if (c.E <= 32)
+    k_router_dlogits<1><<<grid, 256, 0, st>>>(a);
+  else if (c.E <= 64)
+    k_router_dlogits<2><<<grid, 256, 0, st>>>(a);
+  else if (c.E <= 128)
+    k_router_dlogits<4><<<grid, 256, 0, st>>>(a);
+  else
+    k_router_dlogits<8><<<grid, 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dlogit_bias) {
+    k_colsum<<<c.E, 256, 0, st>>>(dl, c.T, c.E, dlogit_bias);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // dW_r[E,H] = dl^T X : M=E, N=H, K=T, A(m=e,k=t) = dl[t*E+e]
+  {
+    dim3 grid2((c.H + 127) / 128, (c.E + 127) / 128);
+    k_sgemm<true, Bf16In><<<grid2, 256, 0, st>>>(c.E, c.H, c.T, dl, c.E, reinterpret_cast<const Bf16In*>(X),
+                                                  c.H, dW_r, c.H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // dX_r[T,H] = dl W_r : M=T, N=H, K=E
+  {
+    dim3 grid3((c.H + 127) / 128, (c.T + 127) / 128);
+    k_sgemm<false, float><<<grid3, 256, 0, st>>>(c.T, c.H, c.E, dl, c.E, Wr, c.H, dX_router, c.H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe

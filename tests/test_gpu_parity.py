@@ -1,0 +1,199 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
+
+Protocol:
+  * routing: GPU logits/scores vs the oracle's double values (1e-5, slice-relative);
+    the oracle's selection run in float32 on the GPU's own logits/scores must give
+    bit-identical topk_idx; counts, offsets, tile_offsets, row_id_map and slot_src
+    must equal the oracle's counting-sort maps bit for bit;
+  * values: the oracle (mirror mode, double accumulation) on the GPU's selection;
+    Y, dX, dW13, dW2, dgates, dW_r, dlogit_bias within 2e-2 slice-relative error,
+    gates within 1e-5.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as S
+import oracle as O
+from helpers import host_f64, make_layer, slice_rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_ROUTER = 1e-5
+
+CASES = {
+    "tiny": S.WORKLOADS["tiny"],
+    # several M tiles per expert, a ragged token count, F with an odd number of 128-column tiles
+    "ragged-softmax": S.Workload("ragged-softmax", T=1000, H=256, E=8, k=2, F=384),
+    # sigmoid router, selection bias, 4 groups / top-2 groups, gate scale, shared expert (large-E router path)
+    "dsv3-mini": S.Workload("dsv3-mini", T=520, H=256, E=64, k=6, F=256, F_shared=256, score_fn=1, gate_scale=2.5,
+                            n_group=8, topk_group=4, sel_bias=True),
+    # 128 experts, top-8 (router large-E path), no renormalisation
+    "e128-norenorm": S.Workload("e128-norenorm", T=384, H=128, E=128, k=8, F=128, renorm=0),
+    # 256 experts, skewed logit bias leaving empty experts
+    "e256-skew": S.Workload("e256-skew", T=640, H=128, E=256, k=4, F=256, skew=True),
+    # 16 experts, sigmoid without renorm, small-E router path with groups
+    "e16-sigmoid": S.Workload("e16-sigmoid", T=300, H=384, E=16, k=3, F=128, score_fn=1, renorm=0, n_group=4,
+                              topk_group=2),
+    # edge cases
+    "e1-k1": S.Workload("e1-k1", T=200, H=128, E=1, k=1, F=128),
+    "k-equals-e": S.Workload("k-equals-e", T=130, H=128, E=4, k=4, F=256),
+}
+
+
+def run_layer(w, inp):
+    layer = make_layer(w, inp)
+    X = to_dev(inp["X"])
+    dY = to_dev(inp["dY"])
+    layer.forward(X)
+    layer.backward(dY)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    return layer
+
+
+def check_routing(w, inp, layer, c):
+    lg = layer.logits.cpu().numpy()
+    sc = layer.scores.cpu().numpy()
+    logits, scores = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
+    assert slice_rel_err(lg, logits) < TOL_ROUTER
+    assert slice_rel_err(sc, scores) < TOL_ROUTER
+    idx_gpu = layer.topk_idx.cpu().numpy()
+    idx_ora = O.select(c, lg, sc, inp.get("sel_bias"))
+    assert np.array_equal(idx_gpu, idx_ora), np.argwhere(idx_gpu != idx_ora)[:5]
+    g_ora = O.gates(c, logits, idx_gpu)
+    assert slice_rel_err(layer.gates.cpu().numpy(), g_ora) < TOL_ROUTER
+    d = O.dispatch(c, idx_gpu, R=layer.R)
+    n_used = int(d["offsets"][-1])
+    assert np.array_equal(layer.counts.cpu().numpy(), d["counts"])
+    assert np.array_equal(layer.offsets.cpu().numpy(), d["offsets"])
+    assert np.array_equal(layer.tile_offsets.cpu().numpy(), d["tile_offsets"])
+    assert np.array_equal(layer.row_id_map.cpu().numpy(), d["row_id_map"])
+    assert np.array_equal(layer.slot_src.cpu().numpy()[:n_used], d["slot_src"][:n_used])
+    return logits, idx_gpu, g_ora, d
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_parity(name):
+    w = CASES[name]
+    inp = S.host_inputs(w)
+    layer = run_layer(w, inp)
+    c = O.cfg(w, mirror=True)
+    logits, idx, g, d = check_routing(w, inp, layer, c)
+    n_used = int(d["offsets"][-1])
+    # permuted tokens: exact copies, zero padding rows
+    xp = layer.Xperm.view(torch.int16).cpu().numpy().view(np.uint16)[:n_used]
+    src = d["slot_src"][:n_used]
+    real = src >= 0
+    assert np.array_equal(xp[real], inp["X"][src[real] // w.k])
+    assert (xp[~real] == 0).all()
+    # layer values
+    tk = O.tokens(c, inp, idx, logits, g)
+    assert slice_rel_err(host_f64(layer.Y), tk["Y"]) < TOL_BF16
+    assert slice_rel_err(layer.dgates.cpu().numpy(), tk["dgates"]) < TOL_BF16
+    assert slice_rel_err(host_f64(layer.dX), tk["dX"]) < TOL_BF16
+    for e in range(w.E):
+        dW13, dW2 = O.expert_wgrad(c, inp, idx, g, e)
+        assert slice_rel_err(host_f64(layer.dW13[e]), dW13, 2) < TOL_BF16, e
+        assert slice_rel_err(host_f64(layer.dW2[e]), dW2, 2) < TOL_BF16, e
+    if w.F_shared:
+        dW13s, dW2s = O.expert_wgrad(c, inp, idx, g, -1)
+        assert slice_rel_err(host_f64(layer.dW13_s), dW13s, 2) < TOL_BF16
+        assert slice_rel_err(host_f64(layer.dW2_s), dW2s, 2) < TOL_BF16
+    dWr, dlb = O.router_wgrad(c, inp["X"], tk["dlogits"])
+    assert slice_rel_err(layer.dW_r.cpu().numpy(), dWr) < TOL_BF16
+    if inp.get("logit_bias") is not None:
+        assert slice_rel_err(layer.dlogit_bias.cpu().numpy(), dlb) < TOL_BF16
+
+
+def _seg_matmul(A, B, off, cnt):
+    """Per expert e: rows [off[e], off[e]+cnt[e]) of A times B[e]^T (torch fp32)."""
+    out = torch.zeros(A.shape[0], B.shape[1], dtype=torch.float32, device=A.device)
+    for e in range(B.shape[0]):
+        r0, r1 = int(off[e]), int(off[e]) + int(cnt[e])
+        if r1 > r0:
+            out[r0:r1] = A[r0:r1].float() @ B[e].float().T
+    return out
+
+
+def test_grouped_gemm_modes_match_torch_fp32():
+    """Each of the six expert GEMMs (three tcgen05 operand layouts, three epilogues)
+    against a plain PyTorch fp32 reference computed from the kernel's own inputs."""
+    w = CASES["ragged-softmax"]
+    inp = S.host_inputs(w)
+    L = run_layer(w, inp)
+    F = w.F
+    off = L.offsets.cpu().numpy()
+    cnt = L.counts.cpu().numpy()
+    rows = np.concatenate([np.arange(off[e], off[e] + cnt[e]) for e in range(w.E)])
+    ri = torch.from_numpy(rows).cuda()
+
+    def err(gpu, ref):
+        return slice_rel_err(host_f64(gpu[ri]), host_f64(ref[ri]))
+
+    gu = _seg_matmul(L.Xperm, L.w.W13, off, cnt)
+    errs = {"fc1_fwd(GU)": err(L.GU, gu)}
+    g, u = L.GU[:, :F].float(), L.GU[:, F:].float()
+    errs["fc1_fwd(A)"] = err(L.A, torch.nn.functional.silu(gu[:, :F]) * gu[:, F:])
+    errs["fc2_fwd"] = err(L.Yperm, _seg_matmul(L.A, L.w.W2, off, cnt))
+    dA = _seg_matmul(L.dYperm, L.w.W2.transpose(1, 2).contiguous(), off, cnt)
+    sg = torch.sigmoid(g)
+    dgu = torch.cat([dA * u * sg * (1 + g * (1 - sg)), dA * g * sg], dim=1)
+    errs["fc2_dgrad+dswiglu"] = err(L.dGU, dgu)
+    errs["fc1_dgrad"] = err(L.dXperm, _seg_matmul(L.dGU, L.w.W13.transpose(1, 2).contiguous(), off, cnt))
+    for e in range(w.E):
+        r0, r1 = int(off[e]), int(off[e]) + int(cnt[e])
+        ref2 = L.dYperm[r0:r1].float().T @ L.A[r0:r1].float()
+        ref13 = L.dGU[r0:r1].float().T @ L.Xperm[r0:r1].float()
+        errs[f"fc2_wgrad[{e}]"] = slice_rel_err(host_f64(L.dW2[e]), host_f64(ref2), 2)
+        errs[f"fc1_wgrad[{e}]"] = slice_rel_err(host_f64(L.dW13[e]), host_f64(ref13), 2)
+    bad = {k: v for k, v in errs.items() if not v < 1e-2}
+    assert not bad, bad
+
+
+def test_cuda_graph_replay_follows_new_routing():
+    """The whole forward+backward is captured once; replaying it on new token
+    values (so the routing and every expert size change) matches eager runs."""
+    w = CASES["dsv3-mini"]
+    inp = S.host_inputs(w)
+    layer = make_layer(w, inp)
+    X = to_dev(inp["X"])
+    dY = to_dev(inp["dY"])
+    layer.forward(X)
+    layer.backward(dY)
+    torch.cuda.synchronize()
+    first_idx = layer.topk_idx.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(X)
+            layer.backward(dY)
+    torch.cuda.synchronize()
+    inp2 = S.host_inputs(w, seed=5)
+    X.copy_(to_dev(inp2["X"]))
+    g.replay()
+    torch.cuda.synchronize()
+    got = {k: getattr(layer, k).clone() for k in ["topk_idx", "counts", "row_id_map", "Y", "dX", "dW13", "dW_r"]}
+    eager = make_layer(w, inp)
+    eager.forward(X)
+    eager.backward(dY)
+    torch.cuda.synchronize()
+    assert not torch.equal(got["topk_idx"], first_idx)  # the replay really re-routed
+    for k, v in got.items():
+        assert torch.equal(v, getattr(eager, k)), k
+    assert layer.device_error() == 0
+
+
+def test_empty_tokens():
+    w = S.Workload("empty", T=0, H=128, E=8, k=2, F=128)
+    inp = S.host_inputs(w)
+    layer = make_layer(w, inp)
+    layer.forward(to_dev(inp["X"]).reshape(0, 128))
+    layer.backward(to_dev(inp["dY"]).reshape(0, 128))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert (layer.offsets.cpu() == 0).all()
+    assert (layer.dW13.float().abs().sum() == 0).item() and (layer.dW2.float().abs().sum() == 0).item()
