@@ -172,9 +172,11 @@ moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* 
   if (!aligned16(X) || !aligned16(Xperm)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*cfg);
+  const int nsm = num_sms();
+  if (nsm <= 0) return MOE_ERR_CUDA;
   return cuda_status(launch_permute(*cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm,
                                     ws_ptr<int32_t>(ws, L.chunk_counts), ws_ptr<int32_t>(ws, L.chunk_base),
-                                    ws_ptr<int>(ws, L.err), (cudaStream_t)stream));
+                                    ws_ptr<int>(ws, L.err), nsm, (cudaStream_t)stream));
 }
 
 moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
@@ -294,7 +296,8 @@ moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const f
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*cfg);
   return cuda_status(launch_router_bwd(*cfg, X, W_r, logits, topk_idx, gates, dgates, dW_r, dlogit_bias, dX_router,
-                                       ws_ptr<float>(ws, L.dlogits), (cudaStream_t)stream));
+                                       ws_ptr<float>(ws, L.dlogits), ws_ptr<float>(ws, L.rbwd_part), L.rbwd_splits,
+                                       (cudaStream_t)stream));
 }
 
 moe_status moe_permute_bwd(const moe_config* cfg, const moe_bf16* dXperm, const int32_t* row_id_map,

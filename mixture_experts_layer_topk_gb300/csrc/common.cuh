@@ -19,12 +19,29 @@ struct WsLayout {
   size_t chunk_counts;  // int32[nchunks * E]
   size_t chunk_base;    // int32[nchunks * E]
   size_t dlogits;       // float[T * E]
+  size_t rbwd_part;     // float[splits * E * H]: split-K partials of dW_r
+  int rbwd_splits;
   size_t total;
 };
 
 constexpr int kChunk = 128;  // tokens per dispatch chunk
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Token splits of the router weight gradient dW_r = dlogits^T X (a reduction
+// over T): enough CTAs to fill the GPU, partials summed in a fixed order.
+inline int router_bwd_splits(const moe_config& c) {
+  if (c.T <= 0) return 1;
+  if (c.E <= 32) {
+    const int s = (c.T + 63) / 64;
+    return s < 64 ? s : 64;
+  }
+  const int tiles = ((c.H + 127) / 128) * ((c.E + 127) / 128);
+  int s = (304 + tiles - 1) / tiles;
+  s = s < 16 ? s : 16;
+  const int kmax = (c.T + 7) / 8;
+  return s < kmax ? s : kmax;
+}
 
 inline WsLayout ws_layout(const moe_config& c) {
   WsLayout L;
@@ -38,6 +55,9 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + nch * c.E * sizeof(int32_t));
   L.dlogits = o;
   o = align256(o + (size_t)c.T * c.E * sizeof(float));
+  L.rbwd_splits = router_bwd_splits(c);
+  L.rbwd_part = o;
+  o = align256(o + (size_t)L.rbwd_splits * c.E * c.H * sizeof(float));
   L.total = o;
   return L;
 }

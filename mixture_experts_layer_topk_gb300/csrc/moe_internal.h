@@ -25,10 +25,12 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
                                int32_t* counts, cudaStream_t st, int nsm);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
-                              float* dlogit_bias, float* dX_router, float* dl, cudaStream_t st);
+                              float* dlogit_bias, float* dX_router, float* dl, float* part, int splits,
+                              cudaStream_t st);
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
                            int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
-                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, cudaStream_t st);
+                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, int nsm,
+                           cudaStream_t st);
 cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int32_t* row_id_map, const float* gates,
                            const uint16_t* Ysh, uint16_t* Y, cudaStream_t st);
 cudaError_t launch_combine_bwd(const moe_config& c, const uint16_t* dY, const uint16_t* Yperm,

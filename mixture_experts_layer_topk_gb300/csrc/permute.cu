@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
   }
 }
 
-// Chunk CTAs (blockIdx < nch): rank assignments, write the maps, copy rows.
+// Chunk CTAs (blockIdx < nch): rank assignments and write the maps.
 // Padding CTAs (blockIdx >= nch): zero expert (blockIdx - nch)'s padding rows.
 __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx,
                                                  const int32_t* __restrict__ chunk_base,
@@ -139,16 +139,21 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
       __syncwarp();
     }
   }
-  __syncthreads();
-  // copy: one warp per token, the row read once and written k times
-  for (int tt = warp; tt < t1 - t0; tt += 8) {
-    const uint4* src = reinterpret_cast<const uint4*>(X + (size_t)(t0 + tt) * H);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 x = __ldg(src + v);
-      for (int j = 0; j < k; ++j) {
-        const int slot = slot_of[tt * k + j];
-        if (slot >= 0) reinterpret_cast<uint4*>(Xperm + (size_t)slot * H)[v] = x;
-      }
+}
+
+// Xperm[row_id_map[t,j]] = X[t]: 16-byte vectors over the whole grid, each
+// token vector read once and written to its k rows.
+__global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ X,
+                                                   const int32_t* __restrict__ row_id_map, int T, int H, int k,
+                                                   uint16_t* __restrict__ Xperm) {
+  const int nvec = H / 8;
+  const int64_t total = (int64_t)T * nvec;
+  for (int64_t v = blockIdx.x * 256LL + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
+    const int t = (int)(v / nvec), c = (int)(v % nvec);
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(X + (size_t)t * H) + c);
+    for (int j = 0; j < k; ++j) {
+      const int slot = __ldg(row_id_map + (size_t)t * k + j);
+      if (slot >= 0) reinterpret_cast<uint4*>(Xperm + (size_t)slot * H)[c] = x;
     }
   }
 }
@@ -280,7 +285,8 @@ __global__ void __launch_bounds__(256) k_permute_bwd(const uint16_t* __restrict_
 
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
                            int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
-                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, cudaStream_t st) {
+                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, int nsm,
+                           cudaStream_t st) {
   const int nch = (c.T + kChunk - 1) / kChunk;
   cudaError_t e;
   if (nch > 0) {
@@ -291,7 +297,15 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_scatter<<<nch + c.E, 256, 0, st>>>(X, topk_idx, chunk_base, counts, offsets, c.T, c.H, c.E, c.k, nch,
                                        row_id_map, slot_src, Xperm);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (c.T > 0) {
+    const int64_t vec = (int64_t)c.T * (c.H / 8);
+    int64_t blocks = (vec + 255) / 256;
+    if (blocks > 8LL * nsm) blocks = 8LL * nsm;
+    k_copy_rows<<<(int)blocks, 256, 0, st>>>(X, row_id_map, c.T, c.H, c.k, Xperm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int32_t* row_id_map, const float* gates,

@@ -471,20 +471,24 @@ __global__ void __launch_bounds__(256) k_colsum(const float* dl, int T, int E, f
 
 // C[M,N] = sum_k A(m,k) B(k,n), FP32, 128x128 tiles, 8x8 per thread.
 // A(m,k) = A[m*lda + k] (A_KM=false) or A[k*lda + m] (A_KM=true); B(k,n) = B[k*ldb + n].
+// Split-K over blockIdx.z: split z covers k in [z*kps, (z+1)*kps) and writes C + z*c_zstride.
 template <bool A_KM, typename TB>
 __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, const float* __restrict__ A, int64_t lda,
                                                const TB* __restrict__ B, int64_t ldb, float* __restrict__ Cm,
-                                               int64_t ldc) {
+                                               int64_t ldc, int kps, int64_t c_zstride) {
   __shared__ __align__(16) float As[8][128 + 4];
   __shared__ __align__(16) float Bs[8][128 + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const int kbeg = blockIdx.z * kps;
+  const int kend = min(K, kbeg + kps);
+  Cm += blockIdx.z * c_zstride;
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += 8) {
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int i = tid + 256 * r;  // 0..1023
@@ -498,12 +502,12 @@ __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, const float*
       }
       const int gm = m0 + mm, gk = k0 + kk;
       float v = 0.f;
-      if (gm < M && gk < K) v = A_KM ? A[(int64_t)gk * lda + gm] : A[(int64_t)gm * lda + gk];
+      if (gm < M && gk < kend) v = A_KM ? A[(int64_t)gk * lda + gm] : A[(int64_t)gm * lda + gk];
       As[kk][mm] = v;
       const int nn = i & 127, kb = i >> 7;
       const int gn = n0 + nn, gk2 = k0 + kb;
       float w = 0.f;
-      if (gn < N && gk2 < K) w = (float)B[(int64_t)gk2 * ldb + gn];
+      if (gn < N && gk2 < kend) w = (float)B[(int64_t)gk2 * ldb + gn];
       Bs[kb][nn] = w;
     }
     __syncthreads();
@@ -537,6 +541,55 @@ __global__ void __launch_bounds__(256) k_sgemm(int M, int N, int K, const float*
   }
 }
 
+// Partial dW_r for E <= EM <= 32 over one token split: each thread owns two
+// columns of H and all E rows; dlogits of 64 tokens at a time in shared memory.
+template <int EM>
+__global__ void __launch_bounds__(256) k_dwr_small(const float* __restrict__ dl, const uint16_t* __restrict__ X,
+                                                   int T, int H, int E, int tps, float* __restrict__ part) {
+  __shared__ float dls[64][EM];
+  const int split = blockIdx.y;
+  const int h0 = (blockIdx.x * 256 + threadIdx.x) * 2;
+  const int t0 = split * tps, t1 = min(T, t0 + tps);
+  float acc[EM][2];
+#pragma unroll
+  for (int e = 0; e < EM; ++e) acc[e][0] = acc[e][1] = 0.f;
+  for (int tb = t0; tb < t1; tb += 64) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * EM; i += 256) {
+      const int tt = i / EM, e = i % EM;
+      dls[tt][e] = (tb + tt < t1 && e < E) ? dl[(size_t)(tb + tt) * E + e] : 0.f;
+    }
+    __syncthreads();
+    if (h0 < H) {
+      const int nt = min(64, t1 - tb);
+      for (int tt = 0; tt < nt; ++tt) {
+        const uint32_t xv = __ldg(reinterpret_cast<const uint32_t*>(X + (size_t)(tb + tt) * H + h0));
+        const float x0 = bf16_lo(xv), x1 = bf16_hi(xv);
+#pragma unroll
+        for (int e = 0; e < EM; ++e) {
+          acc[e][0] = fmaf(dls[tt][e], x0, acc[e][0]);
+          acc[e][1] = fmaf(dls[tt][e], x1, acc[e][1]);
+        }
+      }
+    }
+  }
+  if (h0 < H)
+#pragma unroll
+    for (int e = 0; e < EM; ++e)
+      if (e < E)
+        *reinterpret_cast<float2*>(part + ((size_t)split * E + e) * H + h0) = make_float2(acc[e][0], acc[e][1]);
+}
+
+// out[i] = sum over splits s (in order) of part[s*n + i].
+__global__ void __launch_bounds__(256) k_reduce_splits(const float* __restrict__ part, int splits, int64_t n,
+                                                       float* __restrict__ out) {
+  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += part[(int64_t)z * n + i];
+    out[i] = s;
+  }
+}
+
 struct Bf16In {
   uint16_t v;
   __device__ __forceinline__ explicit operator float() const { return __uint_as_float((uint32_t)v << 16); }
@@ -563,7 +616,8 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
 
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
-                              float* dlogit_bias, float* dX_router, float* dl, cudaStream_t st) {
+                              float* dlogit_bias, float* dX_router, float* dl, float* part, int splits,
+                              cudaStream_t st) {
   if (c.T == 0) {
     cudaError_t e = cudaMemsetAsync(dW_r, 0, sizeof(float) * c.E * c.H, st);
     if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, sizeof(float) * c.E, st);
@@ -585,17 +639,36 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
     k_colsum<<<c.E, 256, 0, st>>>(dl, c.T, c.E, dlogit_bias);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // dW_r[E,H] = dl^T X : M=E, N=H, K=T, A(m=e,k=t) = dl[t*E+e]
+  // dW_r[E,H] = dl^T X : a reduction over the T tokens, split over `splits` token ranges
   {
-    dim3 grid2((c.H + 127) / 128, (c.E + 127) / 128);
-    k_sgemm<true, Bf16In><<<grid2, 256, 0, st>>>(c.E, c.H, c.T, dl, c.E, reinterpret_cast<const Bf16In*>(X),
-                                                  c.H, dW_r, c.H);
+    const int tps = (c.T + splits - 1) / splits;
+    float* dst = splits > 1 ? part : dW_r;
+    if (c.E <= 8) {
+      k_dwr_small<8><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
+    } else if (c.E <= 16) {
+      k_dwr_small<16><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
+    } else if (c.E <= 32) {
+      k_dwr_small<32><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
+    } else {
+      // M=E, N=H, K=T, A(m=e,k=t) = dl[t*E+e]; split-K with 8-aligned token ranges
+      const int kps = ((tps + 7) / 8) * 8;
+      dim3 grid2((c.H + 127) / 128, (c.E + 127) / 128, splits);
+      k_sgemm<true, Bf16In><<<grid2, 256, 0, st>>>(c.E, c.H, c.T, dl, c.E, reinterpret_cast<const Bf16In*>(X), c.H,
+                                                    dst, c.H, kps, (int64_t)c.E * c.H);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (splits > 1) {
+      const int64_t n = (int64_t)c.E * c.H;
+      int blocks = (int)((n + 255) / 256);
+      blocks = blocks < 2048 ? blocks : 2048;
+      k_reduce_splits<<<blocks, 256, 0, st>>>(part, splits, n, dW_r);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   // dX_r[T,H] = dl W_r : M=T, N=H, K=E
   {
     dim3 grid3((c.H + 127) / 128, (c.T + 127) / 128);
-    k_sgemm<false, float><<<grid3, 256, 0, st>>>(c.T, c.H, c.E, dl, c.E, Wr, c.H, dX_router, c.H);
+    k_sgemm<false, float><<<grid3, 256, 0, st>>>(c.T, c.H, c.E, dl, c.E, Wr, c.H, dX_router, c.H, c.E, 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -42,6 +42,20 @@ def slice_rel_err(gpu: np.ndarray, ref: np.ndarray, slice_axes=1) -> float:
     return float(out.max()) if len(out) else 0.0
 
 
+def logit_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
+    """Router logits: per token, max|gpu-ref| over the experts divided by the
+    larger of that token's max|ref| and the RMS of all reference logits.  A
+    token whose logits all cancel to near zero (E=1 makes this common) is thus
+    measured against the typical logit size instead of its own tiny value."""
+    g = np.asarray(gpu, np.float64).reshape(len(gpu), -1)
+    r = np.asarray(ref, np.float64).reshape(len(ref), -1)
+    if r.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(r * r)))
+    den = np.maximum(np.abs(r).max(axis=1), rms)
+    return float((np.abs(g - r).max(axis=1) / den).max())
+
+
 def make_layer(w: S.Workload, inp: dict, device="cuda"):
     import mixture_experts_layer_topk_gb300 as M
     cfg = M.config_from(w)

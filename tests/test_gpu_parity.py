@@ -15,7 +15,7 @@ import torch
 
 import moe_synth as S
 import oracle as O
-from helpers import host_f64, make_layer, slice_rel_err, to_dev
+from helpers import host_f64, logit_rel_err, make_layer, slice_rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +57,7 @@ def check_routing(w, inp, layer, c):
     lg = layer.logits.cpu().numpy()
     sc = layer.scores.cpu().numpy()
     logits, scores = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
-    assert slice_rel_err(lg, logits) < TOL_ROUTER
+    assert logit_rel_err(lg, logits) < TOL_ROUTER
     assert slice_rel_err(sc, scores) < TOL_ROUTER
     idx_gpu = layer.topk_idx.cpu().numpy()
     idx_ora = O.select(c, lg, sc, inp.get("sel_bias"))
