@@ -122,6 +122,10 @@ WORKLOADS = {
     "dsv3-fp8": Workload("dsv3-fp8", T=8192, H=7168, E=256, k=8, F=2048, F_shared=2048, score_fn=1,
                          renorm=1, gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True, fp8=True),
     "skew": Workload("skew", T=32768, H=4096, E=64, k=4, F=2048, skew=True),
+    # profiling stand-in: the Mixtral-style layer with a narrower FFN (same per-tile
+    # shapes along K for FC1, 0.4 GB of expert weights: larger than L2, small enough
+    # for a multi-pass profiler capture)
+    "mixtral-small": Workload("mixtral-small", T=4096, H=4096, E=8, k=2, F=2048),
 }
 
 SKEW_BETA = 2.0
