@@ -186,6 +186,28 @@ moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const f
 moe_status moe_permute_bwd(const moe_config* cfg, const moe_bf16* dXperm, const int32_t* row_id_map,
                            const float* dX_router, const moe_bf16* dX_shared, moe_bf16* dX, void* stream);
 
+/* Dispatch without a workspace, for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call; it exists because moe_permute
+ * needs a caller-provided workspace, and some callers cannot provide one: code
+ * running inside a memory arena sized once at start-up, a plugin that is handed
+ * only its inputs and outputs, or a caller in the middle of recording a CUDA
+ * graph (where cudaMalloc is not allowed).
+ * Same arguments, outputs and results as moe_permute, minus `ws`.  The scratch
+ * it needs lives in a static device array built into the library (512 KiB +
+ * 256 B, held by every GPU that loads the library until the process exits),
+ * which limits it to ceil(T/128) * E <= 65536 (for example T = 32768 with
+ * E = 256); larger configurations return MOE_ERR_WORKSPACE and launch nothing.
+ * The first call on each device looks up the array's device address with
+ * that device current, so make the first call on a device before any stream
+ * capture.  Every call shares the one array: calls whose kernels can overlap
+ * on the GPU (different streams with no ordering between them) race and must
+ * not be issued.  Device-side consistency checks of this variant are not
+ * reported (there is no workspace error word to read); host-side argument
+ * checks are the same as moe_permute's.  Allocates, frees and syncs nothing. */
+moe_status moe_permute_noalloc(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx,
+                               const int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
+                               int32_t* row_id_map, int32_t* slot_src, moe_bf16* Xperm, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

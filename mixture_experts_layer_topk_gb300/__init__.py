@@ -26,12 +26,12 @@ from . import build as _build
 __all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
     "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd", "moe_router_topk_bwd", "moe_permute_bwd",
-    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows"]
+    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc"]
 
 EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_workspace_init",
             "moe_read_device_error", "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp",
             "moe_unpermute_combine", "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd",
-            "moe_router_topk_bwd", "moe_permute_bwd"]
+            "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -74,6 +74,7 @@ def load(build: bool = True):
                 "moe_grouped_swiglu_mlp_bwd": [cfgp] + [vp] * 25,
                 "moe_router_topk_bwd": [cfgp] + [vp] * 12,
                 "moe_permute_bwd": [cfgp] + [vp] * 6,
+                "moe_permute_noalloc": [cfgp] + [vp] * 9,
             }
             for name, args in sigs.items():
                 f = getattr(lib, name)
@@ -162,6 +163,15 @@ def moe_permute(cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slo
     _dev(X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, ws)
     _call("moe_permute", cfg, *map(_ptr, (X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm,
                                            ws)), _stream(stream))
+
+
+def moe_permute_noalloc(cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory (the scratch lives in a static device array inside the library; see
+    include/moe.h for its size limit and the rule that calls must not overlap)."""
+    _dev(X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm)
+    _call("moe_permute_noalloc", cfg, *map(_ptr, (X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src,
+                                                   Xperm)), _stream(stream))
 
 
 def moe_grouped_swiglu_mlp(cfg, Xperm, offsets, tile_offsets, W13, W2, GU, A, Yperm, X=None, W13_s=None, W2_s=None,
