@@ -36,11 +36,12 @@ def test_fullsize_sampled_parity(name):
     lg, sc = layer.logits.cpu().numpy(), layer.scores.cpu().numpy()
     logits, scores = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
     assert logit_rel_err(lg, logits) < 1e-5
-    assert slice_rel_err(sc, scores) < 1e-5
+    tol_s = 1e-5 * max(1.0, float(np.abs(logits).max()))  # exp carries the logit error over
+    assert slice_rel_err(sc, scores) < tol_s
     idx = layer.topk_idx.cpu().numpy()
     assert np.array_equal(idx, O.select(c, lg, sc, inp.get("sel_bias")))
     g = O.gates(c, logits, idx)
-    assert slice_rel_err(layer.gates.cpu().numpy(), g) < 1e-5
+    assert slice_rel_err(layer.gates.cpu().numpy(), g) < 2 * tol_s
     d = O.dispatch(c, idx, R=layer.R)
     n_used = int(d["offsets"][-1])
     for k in ["counts", "offsets", "tile_offsets", "row_id_map"]:

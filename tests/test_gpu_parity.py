@@ -58,12 +58,15 @@ def check_routing(w, inp, layer, c):
     sc = layer.scores.cpu().numpy()
     logits, scores = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
     assert logit_rel_err(lg, logits) < TOL_ROUTER
-    assert slice_rel_err(sc, scores) < TOL_ROUTER
+    # scores and gates inherit the logits' error through exp: a relative error eps on
+    # logits of size up to L moves them by about eps*L relative
+    tol_s = TOL_ROUTER * max(1.0, float(np.abs(logits).max()))
+    assert slice_rel_err(sc, scores) < tol_s
     idx_gpu = layer.topk_idx.cpu().numpy()
     idx_ora = O.select(c, lg, sc, inp.get("sel_bias"))
     assert np.array_equal(idx_gpu, idx_ora), np.argwhere(idx_gpu != idx_ora)[:5]
     g_ora = O.gates(c, logits, idx_gpu)
-    assert slice_rel_err(layer.gates.cpu().numpy(), g_ora) < TOL_ROUTER
+    assert slice_rel_err(layer.gates.cpu().numpy(), g_ora) < 2 * tol_s
     d = O.dispatch(c, idx_gpu, R=layer.R)
     n_used = int(d["offsets"][-1])
     assert np.array_equal(layer.counts.cpu().numpy(), d["counts"])
