@@ -52,7 +52,8 @@ typedef enum {
 } moe_status;
 
 /* Layer configuration (plain data, passed by pointer, read only during the call).
- *  T, H, E, k, F  sizes; H and F must be multiples of 128, 1 <= k <= E <= 256, k <= 32.
+ *  T, H, E, k, F  sizes; H and F must be multiples of 128, 1 <= k <= E <= 256, k <= 32,
+ *                 and E a multiple of 8 when E > 32.
  *  F_shared       size of the always-on shared expert (0: none); multiple of 128.
  *  score_fn       0: softmax over the E logits; 1: sigmoid of each logit.
  *  renorm         1: gates renormalised over the k selected experts.
@@ -104,7 +105,9 @@ moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
  *                                    key = logit + sel_bias (softmax) or score + sel_bias (sigmoid),
  *                                    exact ties to the lower expert index
  *  gates    [T,k] fp32 out           combine weights (renormalised, times gate_scale)
- *  counts   [E] int32 out            tokens per expert */
+ *  counts   [E] int32 out            tokens per expert
+ *  ws       workspace (needed when E > 32: the logits then run on the tensor cores from an exact
+ *           three-term bf16 split of W_r, FP32 accumulation) */
 moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float* W_r,
                            const float* logit_bias, const float* sel_bias, float* logits, float* scores,
                            int32_t* topk_idx, float* gates, int32_t* counts, void* ws, void* stream);

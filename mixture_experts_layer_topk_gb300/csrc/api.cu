@@ -44,6 +44,7 @@ moe_status check_cfg(const moe_config* c, bool gemm) {
     if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k) return MOE_ERR_INVALID_ARG;
   }
   if (c->E > 256 || c->k > 32 || c->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->E > 32 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;  // tensor-core router: fp32 rows of 32-byte multiples
   if (c->H % 128 != 0 || c->F % 128 != 0 || c->F_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k + (int64_t)c->E * (c->align - 1) >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->H >= (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
@@ -153,12 +154,15 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
   if (!tok_ok(cfg, X) || !W_r || !tok_ok(cfg, logits) || !tok_ok(cfg, scores) || !tok_ok(cfg, topk_idx) ||
       !tok_ok(cfg, gates) || !counts)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(W_r)) return MOE_ERR_INVALID_ARG;
-  (void)ws;
+  if (!aligned16(X) || !aligned16(W_r) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  if (!ws && cfg->E > 32) return MOE_ERR_WORKSPACE;
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
+  const WsLayout L = ws_layout(*cfg);
+  uint16_t* wsplit = ws ? ws_ptr<uint16_t>(ws, L.wsplit) : nullptr;
+  int* err = ws ? ws_ptr<int>(ws, L.err) : nullptr;
   return cuda_status(launch_router_topk(*cfg, X, W_r, logit_bias, sel_bias, logits, scores, topk_idx, gates, counts,
-                                        (cudaStream_t)stream, nsm));
+                                        wsplit, err, (cudaStream_t)stream, nsm));
 }
 
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
@@ -292,12 +296,22 @@ moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const f
   if (!tok_ok(cfg, X) || !W_r || !tok_ok(cfg, logits) || !tok_ok(cfg, topk_idx) || !tok_ok(cfg, gates) ||
       !tok_ok(cfg, dgates) || !dW_r || !tok_ok(cfg, dX_router))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(W_r) || !aligned16(dX_router)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W_r) || !aligned16(dX_router) || !aligned16(dW_r)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*cfg);
-  return cuda_status(launch_router_bwd(*cfg, X, W_r, logits, topk_idx, gates, dgates, dW_r, dlogit_bias, dX_router,
-                                       ws_ptr<float>(ws, L.dlogits), ws_ptr<float>(ws, L.rbwd_part), L.rbwd_splits,
-                                       (cudaStream_t)stream));
+  const int nsm = num_sms();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  RouterBwdScratch w;
+  w.dl = ws_ptr<float>(ws, L.dlogits);
+  w.part = ws_ptr<float>(ws, L.rbwd_part);
+  w.splits = L.rbwd_splits;
+  w.dl_rows = ws_ptr<uint16_t>(ws, L.dl_rows);
+  w.dl_cols = ws_ptr<uint16_t>(ws, L.dl_cols);
+  w.wb = ws_ptr<uint16_t>(ws, L.wb);
+  w.Tp = L.Tp;
+  w.Ep = L.Ep;
+  return cuda_status(launch_router_bwd(*cfg, X, W_r, logits, topk_idx, gates, dgates, dW_r, dlogit_bias, dX_router, w,
+                                       ws_ptr<int>(ws, L.err), nsm, (cudaStream_t)stream));
 }
 
 moe_status moe_permute_bwd(const moe_config* cfg, const moe_bf16* dXperm, const int32_t* row_id_map,

@@ -19,8 +19,14 @@ struct WsLayout {
   size_t chunk_counts;  // int32[nchunks * E]
   size_t chunk_base;    // int32[nchunks * E]
   size_t dlogits;       // float[T * E]
-  size_t rbwd_part;     // float[splits * E * H]: split-K partials of dW_r
+  size_t rbwd_part;     // E <= 32: float[splits * E * H] token-split partials of dW_r
   int rbwd_splits;
+  // E > 32 (router GEMMs on the tensor cores, exact three-term bf16 splits):
+  size_t wsplit;        // bf16[E * 3H]     W_r as hi | mid | lo along K (forward)
+  size_t wb;            // bf16[6Ep * H]    W_r row blocks hi, mid, hi, lo, hi, mid (dX_router)
+  size_t dl_rows;       // bf16[3Tp * Ep]   dlogits row blocks hi, mid, lo (dW_r)
+  size_t dl_cols;       // bf16[T * 6Ep]    dlogits column blocks hi, hi, mid, hi, lo, mid (dX_router)
+  int Tp, Ep;
   size_t total;
 };
 
@@ -57,7 +63,18 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + (size_t)c.T * c.E * sizeof(float));
   L.rbwd_splits = router_bwd_splits(c);
   L.rbwd_part = o;
-  o = align256(o + (size_t)L.rbwd_splits * c.E * c.H * sizeof(float));
+  if (c.E <= 32) o = align256(o + (size_t)L.rbwd_splits * c.E * c.H * sizeof(float));
+  L.Tp = (c.T + 63) / 64 * 64;
+  L.Ep = (c.E + 31) / 32 * 32;
+  const bool tc = c.E > 32;
+  L.wsplit = o;
+  if (tc) o = align256(o + (size_t)c.E * 3 * c.H * 2);
+  L.wb = o;
+  if (tc) o = align256(o + (size_t)6 * L.Ep * c.H * 2);
+  L.dl_rows = o;
+  if (tc) o = align256(o + (size_t)3 * L.Tp * L.Ep * 2);
+  L.dl_cols = o;
+  if (tc) o = align256(o + (size_t)c.T * 6 * L.Ep * 2);
   L.total = o;
   return L;
 }
@@ -205,6 +222,32 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// Bulk tensor store shared -> global (3D map), tracked by bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 
 // 32 lanes x 32 consecutive fp32 columns (one row per thread).

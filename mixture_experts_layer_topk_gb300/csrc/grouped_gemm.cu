@@ -34,9 +34,11 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int kThreads = 192;
+constexpr int kStagingBytes = 16384;
+constexpr int kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
 
 enum { MODE_FWD = 0, MODE_DGRAD = 1, MODE_WGRAD = 2 };
-enum { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+enum { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_F32 = 3 };
 
 struct GemmArgs {
   int E;
@@ -55,6 +57,9 @@ struct GemmArgs {
   const uint16_t* GU;       // EPI_DSWIGLU: saved pre-activations
   int64_t ldgu;
   int F;                    // SWIGLU / DSWIGLU: column offset of the "up" half
+  int n_valid;              // > 0: output columns at or beyond n_valid are not stored
+  int kwrap;                // K-major A (FWD/DGRAD): the K coordinate wraps modulo kwrap;
+                            // WGRAD: B's row coordinate wraps modulo kwrap (0: no wrap)
   int* err;
 };
 
@@ -119,17 +124,20 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
 template <int MODE, int EPI, int BN, int ST>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap mapD, const GemmArgs g) {
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
+  constexpr bool TMA_OUT = EPI != EPI_SWIGLU;  // outputs leave through the staging buffer and TMA stores
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * STAGE);
+  // two 8 KB halves, each one [128 rows x 32 bf16] box in the 64-byte swizzle layout
+  uint8_t* staging = smem + ST * STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* empty = full + ST;
   uint64_t* acc_full = empty + ST;
   uint64_t* acc_empty = acc_full + 2;
@@ -160,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
+    if (TMA_OUT) tma_prefetch_desc(&mapD);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
@@ -200,10 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MODE == MODE_WGRAD) {
             tma_load_2d(sa, &mapA, bar, tl.m0, tl.k0 + kc);
             tma_load_2d(sa + 8192, &mapA, bar, tl.m0 + 64, tl.k0 + kc);
+            const int kb_row = g.kwrap > 0 ? (tl.k0 + kc) % g.kwrap : tl.k0 + kc;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, tl.k0 + kc);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, kb_row);
           } else {
-            tma_load_2d(sa, &mapA, bar, kc, tl.m0);
+            tma_load_2d(sa, &mapA, bar, g.kwrap > 0 ? kc % g.kwrap : kc, tl.m0);
             if constexpr (MODE == MODE_FWD) {
               if constexpr (EPI == EPI_SWIGLU) {
                 tma_load_3d(sb, &mapB, bar, kc, tl.n0, tl.e);
@@ -280,24 +290,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;  // row within the tile = tensor-memory lane
+    const bool leader = warp == 2 && lane == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int half = 0;  // staging half used by the next box
+    // Writes this thread's 32 values into staging half h (64-byte swizzle: 16-byte
+    // unit j of row r sits at unit j ^ ((r >> 1) & 3)).
+    auto stage_row = [&](int h, const float* v) {
+      uint8_t* base = staging + h * 8192 + r * 64;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(base + ((j ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * j);
+    };
+    // fp32 variant: one [128 rows x 32 fp32] box filling the whole staging buffer in
+    // the 128-byte swizzle layout (16-byte unit j of row r sits at unit j ^ (r & 7)).
+    auto stage_row_f32 = [&](const float* v) {
+      uint8_t* base = staging + r * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(base + ((j ^ (r & 7)) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    };
+    // Hands staged boxes to TMA: all threads fence + barrier, the leader stores.
+    auto publish = [&](int nbox, const int* hx, const int* xs, int y, int z) {
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBarrier, 128);
+      if (leader) {
+        for (int b = 0; b < nbox; ++b) tma_store_3d(&mapD, staging + hx[b] * 8192, xs[b], y, z);
+        bulk_commit_group();
+      }
+    };
+    // Before overwriting a staging half: its previous store must have read it.
+    auto reserve = [&](bool both) {
+      if (leader) {
+        if (both)
+          bulk_wait_group_read<0>();
+        else
+          bulk_wait_group_read<1>();
+      }
+      named_bar_sync(kEpiBarrier, 128);
+    };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+      const int64_t row = tl.m0 + r;
+      if constexpr (EPI == EPI_DSWIGLU) {
+        // pull this row's saved pre-activations into L2 while the accumulator fills
+        if (g.dense_rows <= 0 || row < g.dense_rows) {
+          const uint16_t* gp = g.GU + row * g.ldgu + tl.n0;
+#pragma unroll
+          for (int i = 0; i < BN * 2; i += 128) {
+            prefetch_l2(reinterpret_cast<const uint8_t*>(gp) + i);
+            prefetch_l2(reinterpret_cast<const uint8_t*>(gp + g.F) + i);
+          }
+        }
+      }
       if (tl.kb == 0) {
         // an expert without rows: its weight gradient is zero
-        uint16_t* out = g.D + (int64_t)tl.e * g.d_estride + (int64_t)(tl.m0 + r) * g.ldd + tl.n0;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = 0; i < BN / 8; ++i) reinterpret_cast<uint4*>(out)[i] = z;
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        for (int c = 0; c < BN / 32; ++c) {
+          if constexpr (EPI == EPI_F32) {
+            reserve(true);
+            stage_row_f32(z);
+            const int hx[1] = {0}, xs[1] = {tl.n0 + 32 * c};
+            publish(1, hx, xs, tl.m0, tl.e);
+          } else {
+            reserve(false);
+            stage_row(half, z);
+            const int hx[1] = {half}, xs[1] = {tl.n0 + 32 * c};
+            publish(1, hx, xs, tl.m0, tl.e);
+            half ^= 1;
+          }
+        }
         continue;
       }
-      if (!mbar_wait(&acc_full[acc], acc_phase)) {
-        set_device_error(g.err, MOE_ERR_TIMEOUT, 6);
+      // one thread waits (bounded) and shares the outcome, so that all four warps
+      // take the same path through the named barriers below
+      if (leader) tmem_holder[1] = mbar_wait(&acc_full[acc], acc_phase) ? 1u : 0u;
+      named_bar_sync(kEpiBarrier, 128);
+      const bool acc_ready = tmem_holder[1] != 0u;
+      named_bar_sync(kEpiBarrier, 128);  // everyone has read the flag before it is reused
+      if (!acc_ready) {
+        if (leader) set_device_error(g.err, MOE_ERR_TIMEOUT, 6);
         break;
       }
+      mbar_wait(&acc_full[acc], acc_phase);  // already complete: acquires the accumulator for this thread
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const int64_t row = tl.m0 + r;
       const bool valid = g.dense_rows <= 0 || MODE == MODE_WGRAD || row < g.dense_rows;
       if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
@@ -320,17 +400,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             store32(g.D2 + row * g.ldd2 + col, av);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
       } else if constexpr (EPI == EPI_DSWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t dr[32];
           tmem_ld32(tbase + c * 32, dr);
           tmem_ld_wait();
+          if (c == BN / 32 - 1) {  // the accumulator is no longer needed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const int col = tl.n0 + c * 32;
+          float dg[32], du[32];
           if (valid) {
-            const int col = tl.n0 + c * 32;
             const uint4* gp = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + col);
             const uint4* up = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + g.F + col);
-            float dg[32], du[32];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float gf[8], uf[8];
@@ -345,31 +433,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 du[8 * v + i] = da * sl;
               }
             }
-            store32(g.D + row * g.ldd + col, dg);
-            store32(g.D + row * g.ldd + g.F + col, du);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;
           }
+          reserve(true);
+          stage_row(0, dg);
+          stage_row(1, du);
+          const int hx[2] = {0, 1}, xs[2] = {col, g.F + col};
+          publish(2, hx, xs, tl.m0, 0);
         }
       } else {
-        uint16_t* out = g.D + (int64_t)tl.e * g.d_estride + row * g.ldd + tl.n0;
+        int nch = BN / 32;
+        if (g.n_valid > 0) {
+          const int left = (g.n_valid - tl.n0 + 31) / 32;
+          nch = left < nch ? (left > 1 ? left : 1) : nch;
+        }
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < nch; ++c) {
           uint32_t vr[32];
           tmem_ld32(tbase + c * 32, vr);
           tmem_ld_wait();
-          if (valid) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
-            store32(out + c * 32, v);
+          if (c == nch - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
           }
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
+          const int hx[1] = {EPI == EPI_F32 ? 0 : half}, xs[1] = {tl.n0 + 32 * c};
+          if constexpr (EPI == EPI_F32) {
+            reserve(true);
+            stage_row_f32(v);
+          } else {
+            reserve(false);
+            stage_row(half, v);
+            half ^= 1;
+          }
+          publish(1, hx, xs, tl.m0, MODE == MODE_WGRAD ? tl.e : 0);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    // every store has finished before the CTA (and its shared memory) goes away
+    if (TMA_OUT && leader) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -385,7 +494,7 @@ template <int MODE, int EPI, int BN>
 struct Kern {
   static constexpr int ST = BN == 256 ? 4 : 6;
   static constexpr int STAGE = (BM + BN) * BK * 2;
-  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + (2 * ST + 5) * 8 + 16 + 3 * 260 * 4;
+  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (2 * ST + 5) * 8 + 16 + 3 * 260 * 4;
 };
 
 // ---------------------------------------------------------------- host side
@@ -403,34 +512,49 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle.  dims/strides innermost first (strides in elements).
+// bf16 tensor map.  dims/strides innermost first (strides in elements).
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_elems,
-              uint32_t box0, uint32_t box1) {
+              uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const uint64_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   cuuint64_t gd[3], gs[2];
   cuuint32_t bd[3] = {box0, box1, 1}, es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) gd[i] = dims[i];
-  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_elems[i] * 2;
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_elems[i] * esz;
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), gd, gs, bd, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// operand maps: 128-byte swizzle, the layout the MMA descriptors expect
 bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t b0, uint32_t b1) {
   const uint64_t dims[2] = {inner, outer}, st[1] = {inner};
-  return make_map(m, base, 2, dims, st, b0, b1);
+  return make_map(m, base, 2, dims, st, b0, b1, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer, uint32_t b0,
            uint32_t b1) {
   const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
-  return make_map(m, base, 3, dims, st, b0, b1);
+  return make_map(m, base, 3, dims, st, b0, b1, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// output map: [outer][mid][inner] bf16, boxes of 32 columns x 128 rows, 64-byte swizzle
+// (the staging layout the epilogue writes)
+bool map_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer) {
+  const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
+  return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// fp32 output map: boxes of 32 columns x 128 rows, 128-byte swizzle
+bool map_out_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer) {
+  const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
+  return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
 template <int MODE, int EPI, int BN>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int max_tiles, int nsm,
-                   cudaStream_t st) {
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const GemmArgs& g, int max_tiles,
+                   int nsm, cudaStream_t st) {
   using K = Kern<MODE, EPI, BN>;
   static bool attr = false;
   auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST>;
@@ -441,7 +565,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g
   }
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = max_tiles < nsm ? max_tiles : nsm;
-  kern<<<grid, kThreads, K::smem, st>>>(a, b, g);
+  kern<<<grid, kThreads, K::smem, st>>>(a, b, d, g);
   return cudaGetLastError();
 }
 
@@ -459,81 +583,140 @@ cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = GU; g.ldd = 2 * (int64_t)s.F; g.D2 = Aact; g.ldd2 = s.F; g.F = s.F; g.err = err;
-  return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+  return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, ma, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
 
 // A [rows, F], W2 [E, H, F]: Y [rows, H].
 cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
                            cudaStream_t st) {
   const int bn = pick_bn(s.H);
-  CUtensorMap ma, mb;
-  if (!map2d(&ma, Aact, s.F, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, bn)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, Aact, s.F, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, bn) ||
+      !map_out(&md, Y, s.H, s.rows, 1))
+    return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.K = s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = Y; g.ldd = s.H; g.err = err;
-  return bn == 256 ? launch<MODE_FWD, EPI_STORE, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
-                   : launch<MODE_FWD, EPI_STORE, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+  return bn == 256 ? launch<MODE_FWD, EPI_STORE, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_FWD, EPI_STORE, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
 
 // dY [rows, H], W2 [E, H, F], GU [rows, 2F]: dGU [rows, 2F].
 cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
                              uint16_t* dGU, int* err, cudaStream_t st) {
   const int bn = pick_bn(s.F);
-  CUtensorMap ma, mb;
-  if (!map2d(&ma, dYp, s.H, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, 64)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dYp, s.H, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, 64) ||
+      !map_out(&md, dGU, 2 * (uint64_t)s.F, s.rows, 1))
+    return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dGU; g.ldd = 2 * (int64_t)s.F; g.GU = GU; g.ldgu = 2 * (int64_t)s.F; g.F = s.F; g.err = err;
-  return bn == 256 ? launch<MODE_DGRAD, EPI_DSWIGLU, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
-                   : launch<MODE_DGRAD, EPI_DSWIGLU, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+  return bn == 256 ? launch<MODE_DGRAD, EPI_DSWIGLU, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_DGRAD, EPI_DSWIGLU, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
 
 // dGU [rows, 2F], W13 [E, 2F, H]: dX [rows, H].
 cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* W13, uint16_t* dX1, int* err,
                              cudaStream_t st) {
   const int bn = pick_bn(s.H);
-  CUtensorMap ma, mb;
-  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 64))
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 64) ||
+      !map_out(&md, dX1, s.H, s.rows, 1))
     return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.K = 2 * s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dX1; g.ldd = s.H; g.err = err;
-  return bn == 256 ? launch<MODE_DGRAD, EPI_STORE, 256>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st)
-                   : launch<MODE_DGRAD, EPI_STORE, 128>(ma, mb, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+  return bn == 256 ? launch<MODE_DGRAD, EPI_STORE, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
+                   : launch<MODE_DGRAD, EPI_STORE, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
 
 // dW2 [E, H, F] = dY^T A per expert.
 cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* Aact, uint16_t* dW2, int* err,
                              cudaStream_t st) {
   const int bn = pick_bn(s.F);
-  CUtensorMap ma, mb;
-  if (!map2d(&ma, dYp, s.H, s.rows, 64, 64) || !map2d(&mb, Aact, s.F, s.rows, 64, 64)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dYp, s.H, s.rows, 64, 64) || !map2d(&mb, Aact, s.F, s.rows, 64, 64) ||
+      !map_out(&md, dW2, s.F, s.H, s.dense_rows > 0 ? 1 : s.E))
+    return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.m_tiles = s.H / 128; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
-  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, g, tiles, s.nsm, st)
-                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, g, tiles, s.nsm, st);
+  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
+                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }
 
 // dW13 [E, 2F, H] = dGU^T X per expert.
 cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
                              cudaStream_t st) {
   const int bn = pick_bn(s.H);
-  CUtensorMap ma, mb;
-  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !map2d(&mb, X1, s.H, s.rows, 64, 64))
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !map2d(&mb, X1, s.H, s.rows, 64, 64) ||
+      !map_out(&md, dW13, s.H, 2 * (uint64_t)s.F, s.dense_rows > 0 ? 1 : s.E))
     return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.m_tiles = 2 * s.F / 128; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
-  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, g, tiles, s.nsm, st)
-                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, g, tiles, s.nsm, st);
+  return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
+                   : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
+}
+
+// ---------------------------------------------------------------- router GEMMs on tensor cores
+// FP32-grade products from bf16 operands: every FP32 operand is split exactly into
+// three bf16 terms (hi + mid + lo), each bf16 x bf16 product is exact in the FP32
+// accumulator, and the terms are laid out along K so one GEMM sums them.
+
+// logits[T,E] (fp32) = X[T,H] . Wsplit[E,3H]^T; A's K coordinate wraps every H columns.
+cudaError_t launch_router_logits_tc(int T, int H, int E, const uint16_t* X, const uint16_t* Wsplit, float* logits,
+                                   int* err, int nsm, cudaStream_t st) {
+  const int bn = E <= 128 ? 128 : 256;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, X, H, T, 64, 128) || !map3d(&mb, Wsplit, 3 * (uint64_t)H, E, 1, 64, bn) ||
+      !map_out_f32(&md, logits, E, T, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = 1; g.K = 3 * H; g.n_tiles = 1; g.dense_rows = T; g.kwrap = H; g.n_valid = E; g.err = err;
+  const int tiles = (T + 127) / 128;
+  return bn == 256 ? launch<MODE_FWD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
+                   : launch<MODE_FWD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
+}
+
+// dW_r[E,H] (fp32) = sum over the 3*Tp rows of dlsplit[3Tp,Ep] (hi rows, mid rows, lo rows,
+// each block zero beyond T) times X rows taken modulo Tp (rows >= T read as zero).
+cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint16_t* dlsplit, const uint16_t* X,
+                                 float* dWr, int* err, int nsm, cudaStream_t st) {
+  const int bn = H % 256 == 0 ? 256 : 128;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dlsplit, Ep, 3 * (uint64_t)Tp, 64, 64) || !map2d(&mb, X, H, T, 64, 64) ||
+      !map_out_f32(&md, dWr, H, E, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = 1; g.m_tiles = (E + 127) / 128; g.n_tiles = H / bn; g.dense_rows = 3 * Tp; g.kwrap = Tp; g.err = err;
+  const int tiles = g.m_tiles * g.n_tiles;
+  return bn == 256 ? launch<MODE_WGRAD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
+                   : launch<MODE_WGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
+}
+
+// dX_r[T,H] (fp32) = dlA[T,6Ep] . WB[6Ep,H] (the six significant products of the two splits).
+cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const uint16_t* WB, float* dXr, int* err,
+                                int nsm, cudaStream_t st) {
+  const int bn = H % 256 == 0 ? 256 : 128;
+  CUtensorMap ma, mb, md;
+  if (!map2d(&ma, dlA, 6 * (uint64_t)Ep, T, 64, 128) || !map3d(&mb, WB, H, 6 * (uint64_t)Ep, 1, 64, 64) ||
+      !map_out_f32(&md, dXr, H, T, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = 1; g.K = 6 * Ep; g.n_tiles = H / bn; g.dense_rows = T; g.err = err;
+  const int tiles = ((T + 127) / 128) * g.n_tiles;
+  return bn == 256 ? launch<MODE_DGRAD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
+                   : launch<MODE_DGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
 }
 
 }  // namespace moe

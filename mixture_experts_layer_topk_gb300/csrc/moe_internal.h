@@ -20,12 +20,23 @@ struct GemmShape {
   int nsm;
 };
 
+// Workspace pieces of the router backward.
+struct RouterBwdScratch {
+  float* dl;          // [T,E] fp32 dlogits
+  float* part;        // E <= 32: [splits,E,H] partial dW_r
+  int splits;
+  uint16_t* dl_rows;  // E > 32: [3*Tp, Ep] bf16 split of dl (row blocks hi, mid, lo)
+  uint16_t* dl_cols;  // E > 32: [T, 6*Ep] bf16 split of dl (column blocks hi, hi, mid, hi, lo, mid)
+  uint16_t* wb;       // E > 32: [6*Ep, H] bf16 split of W_r (row blocks hi, mid, hi, lo, hi, mid)
+  int Tp, Ep;
+};
+
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm);
+                               int32_t* counts, uint16_t* wsplit, int* err, cudaStream_t st, int nsm);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
-                              float* dlogit_bias, float* dX_router, float* dl, float* part, int splits,
+                              float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,
                               cudaStream_t st);
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
                            int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
@@ -51,5 +62,12 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
                              cudaStream_t st);
 cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
                              cudaStream_t st);
+
+cudaError_t launch_router_logits_tc(int T, int H, int E, const uint16_t* X, const uint16_t* Wsplit, float* logits,
+                                   int* err, int nsm, cudaStream_t st);
+cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint16_t* dlsplit, const uint16_t* X,
+                                 float* dWr, int* err, int nsm, cudaStream_t st);
+cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const uint16_t* WB, float* dXr, int* err,
+                                int nsm, cudaStream_t st);
 
 }  // namespace moe

@@ -52,6 +52,17 @@ __device__ __forceinline__ void warp_argmax(float& v, int& e) {
   }
 }
 
+// ---------------------------------------------------------------- exact bf16 splits
+// w = hi + mid + lo exactly: each term is the leading 8 significant bits of what is
+// left (truncation), and an fp32 has 24, so the third remainder fits in a bf16.
+__device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
+  hi = (uint16_t)(__float_as_uint(w) >> 16);
+  const float r1 = __fsub_rn(w, __uint_as_float((uint32_t)hi << 16));
+  mid = (uint16_t)(__float_as_uint(r1) >> 16);
+  const float r2 = __fsub_rn(r1, __uint_as_float((uint32_t)mid << 16));
+  lo = (uint16_t)(__float_as_uint(r2) >> 16);
+}
+
 // Scores, selection and gates of token t by one warp.  lrow: the token's E
 // logits (bias included) in shared memory.  hist: per-CTA expert histogram.
 template <int V>
@@ -379,6 +390,10 @@ struct RouteBwdArgs {
   int T, E, k;
   int score_fn, renorm;
   float gate_scale;
+  // optional exact bf16 splits of dl for the tensor-core router GEMMs
+  uint16_t* dl_rows;  // [3*Tp, Ep]: rows t, Tp+t, 2Tp+t hold hi, mid, lo
+  uint16_t* dl_cols;  // [T, 6*Ep]: column blocks hi, hi, mid, hi, lo, mid
+  int Tp, Ep;
 };
 
 // dlogits of one token per warp: the exact gradient of the gates with respect
@@ -450,6 +465,20 @@ __global__ void __launch_bounds__(256) k_router_dlogits(RouteBwdArgs a) {
       v = al * p * (dgm - dense_s);
     }
     if (e < E) a.dl[(size_t)t * E + e] = v;
+    if (a.dl_rows && e < a.Ep) {
+      uint16_t hi = 0, mid = 0, lo = 0;
+      if (e < E) split3(v, hi, mid, lo);
+      a.dl_rows[(size_t)t * a.Ep + e] = hi;
+      a.dl_rows[((size_t)a.Tp + t) * a.Ep + e] = mid;
+      a.dl_rows[((size_t)2 * a.Tp + t) * a.Ep + e] = lo;
+      uint16_t* c = a.dl_cols + (size_t)t * 6 * a.Ep + e;
+      c[0] = hi;
+      c[a.Ep] = hi;
+      c[2 * a.Ep] = mid;
+      c[3 * a.Ep] = hi;
+      c[4 * a.Ep] = lo;
+      c[5 * a.Ep] = mid;
+    }
   }
 }
 
@@ -590,6 +619,51 @@ __global__ void __launch_bounds__(256) k_reduce_splits(const float* __restrict__
   }
 }
 
+// W_r [E,H] fp32 -> fwd [E,3H] (hi | mid | lo along K) and/or bwd [6*Ep,H] (row blocks
+// hi, mid, hi, lo, hi, mid; rows E..Ep-1 of each block zero).
+__global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, int E, int H, int Ep,
+                                                  uint16_t* __restrict__ fwd, uint16_t* __restrict__ bwd) {
+  const int64_t n = (int64_t)Ep * H;
+  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int e = (int)(i / H), h = (int)(i % H);
+    uint16_t hi = 0, mid = 0, lo = 0;
+    if (e < E) split3(Wr[i], hi, mid, lo);
+    if (fwd && e < E) {
+      uint16_t* row = fwd + (size_t)e * 3 * H;
+      row[h] = hi;
+      row[H + h] = mid;
+      row[2 * H + h] = lo;
+    }
+    if (bwd) {
+      const uint16_t seg[6] = {hi, mid, hi, lo, hi, mid};
+#pragma unroll
+      for (int k = 0; k < 6; ++k) bwd[((size_t)k * Ep + e) * H + h] = seg[k];
+    }
+  }
+}
+
+// Routing of tokens whose raw logits X.W_r^T are already in `logits` (written by
+// the tensor-core GEMM): one warp per token adds logit_bias, then scores, selects
+// and gates exactly as the fused kernels do.
+template <int V>
+__global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
+  __shared__ float rows[8][32 * V];
+  __shared__ int hist[32 * V];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * V; i += 256) hist[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * 8 + warp;
+  if (t < a.T) {
+    for (int e = lane; e < a.E; e += 32)
+      rows[warp][e] = a.logits[(size_t)t * a.E + e] + (a.logit_bias ? a.logit_bias[e] : 0.f);
+    __syncwarp();
+    route_token<V>(a, t, rows[warp], hist);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += 256)
+    if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
+}
+
 struct Bf16In {
   uint16_t v;
   __device__ __forceinline__ explicit operator float() const { return __uint_as_float((uint32_t)v << 16); }
@@ -599,7 +673,7 @@ struct Bf16In {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm) {
+                               int32_t* counts, uint16_t* wsplit, int* err, cudaStream_t st, int nsm) {
   RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
               c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
               c.group_score};
@@ -609,21 +683,42 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
   if (c.E <= 8) return launch_small<8, 4>(a, st, nsm);
   if (c.E <= 16) return launch_small<16, 2>(a, st, nsm);
   if (c.E <= 32) return launch_small<32, 1>(a, st, nsm);
-  if (c.E <= 64) return launch_large<64, 4>(a, st);
-  if (c.E <= 128) return launch_large<128, 4>(a, st);
-  return launch_large<256, 4>(a, st);
+  // E > 32: logits on the tensor cores from the exact three-term split of W_r, then routing
+  {
+    int blocks = (int)(((int64_t)c.E * c.H + 255) / 256);
+    blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
+    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, c.E, wsplit, nullptr);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if ((e = launch_router_logits_tc(c.T, c.H, c.E, X, wsplit, logits, err, nsm, st)) != cudaSuccess) return e;
+  const int grid = (c.T + 7) / 8;
+  if (c.E <= 64)
+    k_route_rows<2><<<grid, 256, 0, st>>>(a);
+  else if (c.E <= 128)
+    k_route_rows<4><<<grid, 256, 0, st>>>(a);
+  else
+    k_route_rows<8><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
-                              float* dlogit_bias, float* dX_router, float* dl, float* part, int splits,
+                              float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,
                               cudaStream_t st) {
+  cudaError_t e;
   if (c.T == 0) {
-    cudaError_t e = cudaMemsetAsync(dW_r, 0, sizeof(float) * c.E * c.H, st);
+    e = cudaMemsetAsync(dW_r, 0, sizeof(float) * c.E * c.H, st);
     if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, sizeof(float) * c.E, st);
     return e;
   }
-  RouteBwdArgs a{logits, topk_idx, gates, dgates, dl, c.T, c.E, c.k, c.score_fn, c.renorm, c.gate_scale};
+  const bool tc = c.E > 32;  // large E: the three router-gradient products on the tensor cores
+  RouteBwdArgs a{logits, topk_idx, gates, dgates, w.dl, c.T, c.E, c.k, c.score_fn, c.renorm, c.gate_scale,
+                 tc ? w.dl_rows : nullptr, tc ? w.dl_cols : nullptr, w.Tp, w.Ep};
+  if (tc) {
+    // rows T..Tp-1 of each third of dl_rows must read as zero
+    e = cudaMemsetAsync(w.dl_rows, 0, sizeof(uint16_t) * 3 * (size_t)w.Tp * w.Ep, st);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = (c.T + 7) / 8;
   if (c.E <= 32)
     k_router_dlogits<1><<<grid, 256, 0, st>>>(a);
@@ -633,45 +728,43 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
     k_router_dlogits<4><<<grid, 256, 0, st>>>(a);
   else
     k_router_dlogits<8><<<grid, 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (dlogit_bias) {
-    k_colsum<<<c.E, 256, 0, st>>>(dl, c.T, c.E, dlogit_bias);
+    k_colsum<<<c.E, 256, 0, st>>>(w.dl, c.T, c.E, dlogit_bias);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // dW_r[E,H] = dl^T X : a reduction over the T tokens, split over `splits` token ranges
+  if (tc) {
+    int blocks = (int)(((int64_t)w.Ep * c.H + 255) / 256);
+    blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
+    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, w.Ep, nullptr, w.wb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_router_dwr_tc(c.T, w.Tp, c.H, c.E, w.Ep, w.dl_rows, X, dW_r, err, nsm, st)) != cudaSuccess)
+      return e;
+    return launch_router_dx_tc(c.T, c.H, w.Ep, w.dl_cols, w.wb, dX_router, err, nsm, st);
+  }
+  // small E: dW_r over token splits (fixed-order reduction), dX_r = dl W_r with K = E
   {
+    const int splits = w.splits;
     const int tps = (c.T + splits - 1) / splits;
-    float* dst = splits > 1 ? part : dW_r;
-    if (c.E <= 8) {
-      k_dwr_small<8><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
-    } else if (c.E <= 16) {
-      k_dwr_small<16><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
-    } else if (c.E <= 32) {
-      k_dwr_small<32><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(dl, X, c.T, c.H, c.E, tps, dst);
-    } else {
-      // M=E, N=H, K=T, A(m=e,k=t) = dl[t*E+e]; split-K with 8-aligned token ranges
-      const int kps = ((tps + 7) / 8) * 8;
-      dim3 grid2((c.H + 127) / 128, (c.E + 127) / 128, splits);
-      k_sgemm<true, Bf16In><<<grid2, 256, 0, st>>>(c.E, c.H, c.T, dl, c.E, reinterpret_cast<const Bf16In*>(X), c.H,
-                                                    dst, c.H, kps, (int64_t)c.E * c.H);
-    }
+    float* dst = splits > 1 ? w.part : dW_r;
+    if (c.E <= 8)
+      k_dwr_small<8><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(w.dl, X, c.T, c.H, c.E, tps, dst);
+    else if (c.E <= 16)
+      k_dwr_small<16><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(w.dl, X, c.T, c.H, c.E, tps, dst);
+    else
+      k_dwr_small<32><<<dim3((c.H + 511) / 512, splits), 256, 0, st>>>(w.dl, X, c.T, c.H, c.E, tps, dst);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (splits > 1) {
       const int64_t n = (int64_t)c.E * c.H;
       int blocks = (int)((n + 255) / 256);
       blocks = blocks < 2048 ? blocks : 2048;
-      k_reduce_splits<<<blocks, 256, 0, st>>>(part, splits, n, dW_r);
+      k_reduce_splits<<<blocks, 256, 0, st>>>(w.part, splits, n, dW_r);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
-  // dX_r[T,H] = dl W_r : M=T, N=H, K=E
-  {
-    dim3 grid3((c.H + 127) / 128, (c.T + 127) / 128);
-    k_sgemm<false, float><<<grid3, 256, 0, st>>>(c.T, c.H, c.E, dl, c.E, Wr, c.H, dX_router, c.H, c.E, 0);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  dim3 grid3((c.H + 127) / 128, (c.T + 127) / 128);
+  k_sgemm<false, float><<<grid3, 256, 0, st>>>(c.T, c.H, c.E, w.dl, c.E, Wr, c.H, dX_router, c.H, c.E, 0);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
