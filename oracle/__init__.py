@@ -32,7 +32,7 @@ class OraCfg(ctypes.Structure):
                 ("gate_scale", ctypes.c_double), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("group_score", ctypes.c_int32),
                 ("align", ctypes.c_int32), ("BM", ctypes.c_int32), ("mirror", ctypes.c_int32),
-                ("nthreads", ctypes.c_int32)]
+                ("nthreads", ctypes.c_int32), ("fp8", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -54,10 +54,11 @@ def _load():
 
 
 def cfg(w, mirror: bool = True, align: int = 128, BM: int = 128, nthreads: int = 0,
-        group_score: int = 0) -> OraCfg:
-    """Oracle configuration from a moe_synth.Workload."""
+        group_score: int = 0, fp8: bool | None = None) -> OraCfg:
+    """Oracle configuration from a moe_synth.Workload (fp8 defaults to the workload's flag)."""
+    f8 = getattr(w, "fp8", False) if fp8 is None else fp8
     return OraCfg(w.T, w.H, w.E, w.k, w.F, w.F_shared, w.score_fn, w.renorm, float(w.gate_scale),
-                  w.n_group, w.topk_group, group_score, align, BM, 1 if mirror else 0, nthreads)
+                  w.n_group, w.topk_group, group_score, align, BM, 1 if mirror else 0, nthreads, 1 if f8 else 0)
 
 
 def _p(a):
@@ -161,6 +162,41 @@ def router_wgrad(c: OraCfg, X, dlogits):
     return dWr, dlb
 
 
+def e4m3(x):
+    """FP8 E4M3 round-to-nearest-even of float64 values (|x| <= 448)."""
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.empty_like(x)
+    _load().ora_e4m3(_p(x), _p(out), ctypes.c_int64(x.size))
+    return out
+
+
+def qdq_blocks(x, blk=128):
+    """Quantize-dequantize consecutive blocks of `blk` values with power-of-two block scales."""
+    x = np.ascontiguousarray(x, np.float64).ravel()
+    out = np.empty_like(x)
+    _load().ora_qdq_blocks(_p(x), _p(out), ctypes.c_int64(x.size), ctypes.c_int(blk))
+    return out
+
+
+def qdq_weights(W):
+    """128x128 block quantize-dequantize of a stack of bf16 matrices (returned as bf16 bits)."""
+    W = np.ascontiguousarray(W, np.uint16)
+    rows, cols = W.shape[-2], W.shape[-1]
+    nmat = int(np.prod(W.shape[:-2])) if W.ndim > 2 else 1
+    out = np.empty_like(W)
+    _load().ora_qdq_weight_blocks(_p(W), ctypes.c_int64(nmat), ctypes.c_int(rows), ctypes.c_int(cols), _p(out))
+    return out
+
+
+def fp8_inputs(inp: dict) -> dict:
+    """The inputs with every expert weight replaced by its 128x128-block FP8 quantize-dequantize."""
+    out = dict(inp)
+    for k in ["W13", "W2", "W13_s", "W2_s"]:
+        if out.get(k) is not None:
+            out[k] = qdq_weights(out[k])
+    return out
+
+
 def round_bf16(x):
     x = np.ascontiguousarray(x, np.float64)
     out = np.empty_like(x)
@@ -175,6 +211,8 @@ def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int
     when given, the selection runs on them in float32 (identical-scores rule).
     """
     c = cfg(w, mirror=mirror, nthreads=nthreads)
+    if c.fp8:
+        inp = fp8_inputs(inp)
     logits, scores = router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
     if sel_scores is None:
         idx = select(c, logits, scores, inp.get("sel_bias"))

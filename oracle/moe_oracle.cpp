@@ -61,6 +61,7 @@ typedef struct {
   int32_t BM;          // rows per M tile, for tile_offsets
   int32_t mirror;      // 1: round to bf16 where the GPU stores bf16; 0: pure double
   int32_t nthreads;    // 0: all host cores
+  int32_t fp8;         // 1: every expert GEMM operand passes through FP8 E4M3 block quantization
 } ora_cfg;
 }
 
@@ -89,6 +90,58 @@ inline double silu(double z) { return z * sigm(z); }
 inline double dsilu(double z) {
   const double s = sigm(z);
   return s * (1.0 + z * (1.0 - s));
+}
+
+// ---------------------------------------------------------------- FP8 E4M3
+// E4M3 ("fn" flavour): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+// infinities, largest finite 448, smallest normal 2^-6, subnormal spacing 2^-9.
+// Round to nearest, ties to even.  Inputs here never exceed 448 in magnitude.
+double e4m3_rne(double v) {
+  if (v == 0.0) return 0.0;
+  const double a = std::fabs(v);
+  int ex;
+  std::frexp(a, &ex);                  // a = m * 2^ex, 0.5 <= m < 1, so floor(log2 a) = ex - 1
+  const int e = std::max(ex - 1, -6);  // below 2^-6 the spacing stays 2^-9
+  const double ulp = std::ldexp(1.0, e - 3);
+  const double q = std::nearbyint(a / ulp) * ulp;
+  return v < 0 ? -q : q;
+}
+
+// Block scale: the smallest power of two s = 2^e with 448*s >= amax (s = 1 for an
+// all-zero block).  Power-of-two scales are exact to apply and to undo.
+double block_scale(double amax) {
+  if (!(amax > 0.0)) return 1.0;
+  int ex;
+  std::frexp(amax / 448.0, &ex);
+  int e = ex;                                          // 2^(ex-1) <= amax/448 < 2^ex
+  while (e > -127 && 448.0 * std::ldexp(1.0, e - 1) >= amax) --e;  // exact comparisons
+  while (448.0 * std::ldexp(1.0, e) < amax) ++e;
+  return std::ldexp(1.0, e);
+}
+
+// Quantize-dequantize n consecutive values as blocks of `blk` elements.
+void qdq_blocks(const double* in, double* out, int n, int blk) {
+  for (int b0 = 0; b0 < n; b0 += blk) {
+    const int b1 = std::min(n, b0 + blk);
+    double amax = 0;
+    for (int i = b0; i < b1; ++i) amax = std::max(amax, std::fabs(in[i]));
+    const double s = block_scale(amax);
+    for (int i = b0; i < b1; ++i) out[i] = e4m3_rne(in[i] / s) * s;
+  }
+}
+
+// Column-wise blocks: rows [r0, r0+128) of each column of a [m x n] row-major array.
+void qdq_columns(double* a, int64_t m, int n) {
+  std::vector<double> col;
+  for (int64_t r0 = 0; r0 < m; r0 += 128) {
+    const int64_t r1 = std::min<int64_t>(m, r0 + 128);
+    for (int j = 0; j < n; ++j) {
+      double amax = 0;
+      for (int64_t r = r0; r < r1; ++r) amax = std::max(amax, std::fabs(a[r * n + j]));
+      const double s = block_scale(amax);
+      for (int64_t r = r0; r < r1; ++r) a[r * n + j] = e4m3_rne(a[r * n + j] / s) * s;
+    }
+  }
 }
 
 int nthreads_of(const ora_cfg& c) {
@@ -227,9 +280,18 @@ void token_dlogits(const ora_cfg& c, const double* l, const int32_t* sel, const 
 // One SwiGLU expert applied to one token.  w13: [2F,H] (gate rows then up rows),
 // w2: [H,F].  Outputs (all length as named): gr,ur (F) = stored pre-activations,
 // ar (F) = stored activation, yr (H) = stored expert output.
-void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* x,
+void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* x_in,
                 double* gr, double* ur, double* ar, double* yr) {
   const int H = c.H;
+  // FP8: the token row enters FC1 as 1x128 blocks along H, the activation enters
+  // FC2 as 1x128 blocks along F; the weights are passed already block-quantized.
+  std::vector<double> xq, aq;
+  const double* x = x_in;
+  if (c.fp8) {
+    xq.resize(H);
+    qdq_blocks(x_in, xq.data(), H, 128);
+    x = xq.data();
+  }
   for (int f = 0; f < F; ++f) {
     double g = 0, u = 0;
     const uint16_t* wg = w13 + (size_t)f * H;
@@ -242,10 +304,16 @@ void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
     ur[f] = maybe_r(c, u);
     ar[f] = maybe_r(c, silu(g) * u);  // the activation is formed from the unrounded g, u
   }
+  const double* a = ar;
+  if (c.fp8) {
+    aq.resize(F);
+    qdq_blocks(ar, aq.data(), F, 128);
+    a = aq.data();
+  }
   for (int h = 0; h < H; ++h) {
     double y = 0;
     const uint16_t* w = w2 + (size_t)h * F;
-    for (int f = 0; f < F; ++f) y += bf(w[f]) * ar[f];
+    for (int f = 0; f < F; ++f) y += bf(w[f]) * a[f];
     yr[h] = maybe_r(c, y);
   }
 }
@@ -253,9 +321,15 @@ void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
 // Backward of one expert for one token, given the upstream gradient dyp (H) of
 // its output.  Produces dG, dU (F, as stored) and dx (H, as stored).
 void expert_bwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* gr,
-                const double* ur, const double* dyp, double* dG, double* dU, double* dx) {
+                const double* ur, const double* dyp_in, double* dG, double* dU, double* dx) {
   const int H = c.H;
-  std::vector<double> dA(F, 0.0);
+  std::vector<double> dA(F, 0.0), dq;
+  const double* dyp = dyp_in;
+  if (c.fp8) {  // FC2 dgrad takes the output gradient as 1x128 blocks along H
+    dq.resize(H);
+    qdq_blocks(dyp_in, dq.data(), H, 128);
+    dyp = dq.data();
+  }
   for (int h = 0; h < H; ++h) {
     const uint16_t* w = w2 + (size_t)h * F;
     const double d = dyp[h];
@@ -266,10 +340,20 @@ void expert_bwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
     dU[f] = maybe_r(c, dA[f] * silu(gr[f]));
   }
   for (int h = 0; h < H; ++h) dx[h] = 0.0;
+  std::vector<double> gq;
+  if (c.fp8) {  // FC1 dgrad takes [dG | dU] as 1x128 blocks along 2F
+    gq.resize(2 * (size_t)F);
+    std::vector<double> cat(2 * (size_t)F);
+    for (int f = 0; f < F; ++f) {
+      cat[f] = dG[f];
+      cat[F + f] = dU[f];
+    }
+    qdq_blocks(cat.data(), gq.data(), 2 * F, 128);
+  }
   for (int f = 0; f < F; ++f) {
     const uint16_t* wg = w13 + (size_t)f * H;
     const uint16_t* wu = w13 + (size_t)(F + f) * H;
-    const double a = dG[f], b = dU[f];
+    const double a = c.fp8 ? gq[f] : dG[f], b = c.fp8 ? gq[F + f] : dU[f];
     for (int h = 0; h < H; ++h) dx[h] += bf(wg[h]) * a + bf(wu[h]) * b;
   }
   for (int h = 0; h < H; ++h) dx[h] = maybe_r(c, dx[h]);
@@ -483,6 +567,24 @@ void ora_expert_wgrad(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13,
       for (int h = 0; h < H; ++h) dyp[h] = maybe_r(c, gsel[c0 + i] * bf(dY[(size_t)t * H + h]));
       expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dyp, &dGs[(size_t)i * F], &dUs[(size_t)i * F], dxe.data());
     });
+    if (c.fp8) {
+      // wgrad operands: 128x1 blocks along the expert's tokens (in token order, 128 per block)
+      qdq_columns(dyps.data(), m, H);
+      qdq_columns(as.data(), m, F);
+      qdq_columns(xs.data(), m, H);
+      std::vector<double> cat((size_t)m * 2 * F);
+      for (int64_t i = 0; i < m; ++i)
+        for (int f = 0; f < F; ++f) {
+          cat[(size_t)i * 2 * F + f] = dGs[(size_t)i * F + f];
+          cat[(size_t)i * 2 * F + F + f] = dUs[(size_t)i * F + f];
+        }
+      qdq_columns(cat.data(), m, 2 * F);
+      for (int64_t i = 0; i < m; ++i)
+        for (int f = 0; f < F; ++f) {
+          dGs[(size_t)i * F + f] = cat[(size_t)i * 2 * F + f];
+          dUs[(size_t)i * F + f] = cat[(size_t)i * 2 * F + F + f];
+        }
+    }
     // dW2[h,f] += dyp[h] a[f]; dWg[f,h] += dG[f] x[h]; dWu[f,h] += dU[f] x[h]
     parallel_for(H, nthreads_of(c), [&](int64_t h) {
       double* row = dW2 + (size_t)h * F;
@@ -528,6 +630,39 @@ void ora_router_wgrad(const ora_cfg* cp, const uint16_t* X, const double* dlogit
     if (dlogit_bias) dlogit_bias[e] = sb;
   });
 }
+
+// 128x128 block quantization of nmat row-major [rows x cols] bf16 matrices; the
+// dequantized values (exact in bf16) are written back as bf16 bit patterns.
+void ora_qdq_weight_blocks(const uint16_t* W, int64_t nmat, int rows, int cols, uint16_t* out) {
+  unsigned hc = std::thread::hardware_concurrency();
+  parallel_for(nmat * ((rows + 127) / 128), hc ? (int)hc : 1, [&](int64_t job) {
+    const int64_t mi = job / ((rows + 127) / 128);
+    const int r0 = (int)(job % ((rows + 127) / 128)) * 128, r1 = std::min(rows, r0 + 128);
+    const uint16_t* w = W + mi * rows * (int64_t)cols;
+    uint16_t* o = out + mi * rows * (int64_t)cols;
+    for (int c0 = 0; c0 < cols; c0 += 128) {
+      const int c1 = std::min(cols, c0 + 128);
+      double amax = 0;
+      for (int r = r0; r < r1; ++r)
+        for (int cc = c0; cc < c1; ++cc) amax = std::max(amax, std::fabs(bf(w[(int64_t)r * cols + cc])));
+      const double sc = block_scale(amax);
+      for (int r = r0; r < r1; ++r)
+        for (int cc = c0; cc < c1; ++cc) {
+          const double q = e4m3_rne(bf(w[(int64_t)r * cols + cc]) / sc) * sc;
+          float f = (float)q;  // exact: 4 significant bits
+          uint32_t u;
+          std::memcpy(&u, &f, 4);
+          o[(int64_t)r * cols + cc] = (uint16_t)(u >> 16);
+        }
+    }
+  });
+}
+
+// E4M3 rounding and block quantization, exposed for their own tests.
+void ora_e4m3(const double* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_rne(in[i]);
+}
+void ora_qdq_blocks(const double* in, double* out, int64_t n, int blk) { qdq_blocks(in, out, (int)n, blk); }
 
 // bf16 rounding as used in mirror mode, exposed for its own test.
 void ora_round_bf16(const double* in, double* out, int64_t n) {

@@ -437,3 +437,117 @@ def test_autograd_matches_backward(w):
     for t, key in [(X, "dX"), (Wr, "dW_r"), (W13, "dW13"), (W2, "dW2"), (lb, "dlogit_bias")] + extra:
         ref = t.grad.numpy()
         assert np.allclose(out[key], ref, rtol=1e-10, atol=1e-12 * max(1.0, np.abs(ref).max())), key
+
+
+# ---------------------------------------------------------------- FP8 E4M3 (block-scaled)
+
+
+def torch_e4m3(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_rounding_matches_torch():
+    rng = np.random.default_rng(11)
+    v = np.concatenate([rng.uniform(-448, 448, 20000), rng.standard_normal(20000) * 1e-2,
+                        rng.standard_normal(5000) * 2.0 ** -8])
+    grid = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    grid = grid[np.isfinite(grid)]
+    mids = (np.sort(grid)[1:] + np.sort(grid)[:-1]) / 2  # exact ties between neighbours
+    v = np.concatenate([v, grid, mids[np.abs(mids) <= 448]]).astype(np.float32).astype(np.float64)
+    assert np.array_equal(O.e4m3(v), torch_e4m3(v))
+
+
+def torch_qdq_rows(x, blk=128):
+    """Independent block quantize-dequantize: torch's e4m3 cast with power-of-two scales."""
+    x = np.asarray(x, np.float64)
+    out = np.empty_like(x)
+    for b0 in range(0, x.shape[-1], blk):
+        blkv = x[..., b0:b0 + blk]
+        amax = np.abs(blkv).max(axis=-1, keepdims=True)
+        e = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / 448.0)), 0.0)
+        s = 2.0 ** e
+        out[..., b0:b0 + blk] = torch_e4m3(blkv / s) * s
+    return out
+
+
+def test_block_scales_power_of_two_and_tight():
+    rng = np.random.default_rng(12)
+    for scale in [1e-3, 1.0, 37.0, 5e3]:
+        x = rng.standard_normal(1024) * scale
+        q = O.qdq_blocks(x, 128)
+        assert np.array_equal(q, torch_qdq_rows(x[None])[0])
+        assert np.array_equal(O.qdq_blocks(q, 128), q)  # idempotent
+        for b in range(8):
+            blk = x[128 * b:128 * b + 128]
+            amax = np.abs(blk).max()
+            s = 2.0 ** np.ceil(np.log2(amax / 448))
+            assert 224 < amax / s <= 448
+    assert np.array_equal(O.qdq_blocks(np.zeros(256), 128), np.zeros(256))
+
+
+def test_weight_blocks_are_128x128():
+    rng = np.random.default_rng(13)
+    W = (rng.standard_normal((2, 256, 384)) * 0.02).astype(np.float32)
+    W[1, :128, 128:256] *= 50  # one block with a larger scale
+    bits = torch.from_numpy(W).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q = S.bf16_bits_to_f32(O.qdq_weights(bits)).astype(np.float64)
+    wf = S.bf16_bits_to_f32(bits).astype(np.float64)
+    for m in range(2):
+        for r0 in range(0, 256, 128):
+            for c0 in range(0, 384, 128):
+                blk = wf[m, r0:r0 + 128, c0:c0 + 128]
+                amax = np.abs(blk).max()
+                s = 2.0 ** np.ceil(np.log2(amax / 448))
+                assert np.array_equal(q[m, r0:r0 + 128, c0:c0 + 128], torch_e4m3(blk / s) * s)
+
+
+def test_fp8_e1_k1_is_dense_swiglu_on_quantized_operands():
+    """E=1, k=1 in FP8 mode: every GEMM operand block-quantized, numpy matmuls in double."""
+    w = small(T=200, H=256, E=1, k=1, F=256, fp8=True)
+    inp = inputs(w)
+
+    def ramp(bits, axis):
+        # alternate 64-entry runs of size 1 and 2^-12 along `axis`: power-of-two scales make
+        # E4M3 rounding scale-invariant except in the subnormal range, so a block of the wrong
+        # size (sharing a scale across a quiet and a loud run, or not) shows up there
+        v = torch.from_numpy(S.bf16_bits_to_f32(bits).copy())
+        n = v.shape[axis]
+        f = torch.tensor([2.0 ** (-12 * ((i // 64) % 2)) for i in range(n)], dtype=torch.float32)
+        v = v * (f if axis == v.dim() - 1 else f[:, None])
+        return v.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    inp["X"] = ramp(ramp(inp["X"], 1), 0)
+    inp["dY"] = ramp(ramp(inp["dY"], 1), 0)
+    out = O.full_layer(w, inp, mirror=False)
+    x = f32(inp["X"])
+    W13 = S.bf16_bits_to_f32(O.qdq_weights(inp["W13"]))[0].astype(np.float64)
+    W2 = S.bf16_bits_to_f32(O.qdq_weights(inp["W2"]))[0].astype(np.float64)
+    F = w.F
+    xq = torch_qdq_rows(x)
+    g, u = xq @ W13[:F].T, xq @ W13[F:].T
+    a = g * sps.expit(g) * u
+    y = torch_qdq_rows(a) @ W2.T
+    assert np.allclose(out["Y"], y, rtol=1e-12, atol=1e-13)
+    dy = f32(inp["dY"])
+    dA = torch_qdq_rows(dy) @ W2
+    sg = sps.expit(g)
+    dG, dU = dA * u * sg * (1 + g * (1 - sg)), dA * g * sg
+    dgu = torch_qdq_rows(np.concatenate([dG, dU], axis=1))
+    dx = dgu @ W13
+    assert np.allclose(out["dX"], dx, rtol=1e-11, atol=1e-12)
+    # wgrad operands: 128-token blocks per column
+    colq = lambda m: torch_qdq_rows(m.T.copy()).T
+    assert np.allclose(out["dW2"][0], colq(dy).T @ colq(a), rtol=1e-11, atol=1e-12)
+    assert np.allclose(out["dW13"][0], colq(np.concatenate([dG, dU], axis=1)).T @ colq(x), rtol=1e-11, atol=1e-12)
+
+
+def test_fp8_layer_close_to_bf16_layer():
+    w = small(T=256, H=256, E=4, k=2, F=256)
+    inp = inputs(w)
+    a = O.full_layer(w, inp, mirror=True)
+    b = O.full_layer(w.replace(fp8=True), inp, mirror=True)
+    assert np.array_equal(a["topk_idx"], b["topk_idx"])
+    # E4M3 keeps 3 mantissa bits: ~2-3% RMS noise per quantized operand, compounded over
+    # the two chained GEMMs of an expert; a dropped or wrong term would be O(1)
+    for key in ["Y", "dX", "dW13", "dW2"]:
+        err = np.sqrt(np.mean((a[key] - b[key]) ** 2) / np.mean(a[key] ** 2))
+        assert 1e-3 < err < 0.1, (key, err)
