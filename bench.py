@@ -157,20 +157,36 @@ def run_step(layer, X, dY, ev=None):
     M.moe_permute(c, X, layer.topk_idx, layer.counts, layer.offsets, layer.tile_offsets, layer.row_id_map,
                   layer.slot_src, layer.Xperm, layer.ws)
     rec(2)
-    M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
-                             layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
-                             layer.Yshared, layer.ws)
+    if layer.fp8:
+        # the step re-quantizes the weights (as after every optimizer update) inside the timed region
+        layer.quantize_weights()
+        M.moe_grouped_swiglu_mlp_fp8(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.W13q, layer.W13sc,
+                                     layer.W2q, layer.W2sc, layer.GU, layer.A, layer.Yperm,
+                                     X if c.F_shared else None, layer.W13q_s, layer.W13sc_s, layer.W2q_s,
+                                     layer.W2sc_s, layer.GU_s, layer.A_s, layer.Yshared, layer.fp8_ws, layer.ws)
+    else:
+        M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
+                                 layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
+                                 layer.Yshared, layer.ws)
     rec(3)
     M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, layer.gates, layer.Yshared, layer.Y)
     rec(4)
     M.moe_unpermute_combine_bwd(c, dY, layer.Yperm, layer.row_id_map, layer.gates, layer.offsets, layer.counts,
                                 layer.dYperm, layer.dgates)
     rec(5)
-    M.moe_grouped_swiglu_mlp_bwd(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, w.W13, w.W2,
-                                 layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm, layer.dW13, layer.dW2,
-                                 X if c.F_shared else None, dY if c.F_shared else None, w.W13_s, w.W2_s,
-                                 layer.GU_s, layer.A_s, layer.dGU_s, layer.dX_shared, layer.dW13_s, layer.dW2_s,
-                                 layer.ws)
+    sh = c.F_shared > 0
+    if layer.fp8:
+        M.moe_grouped_swiglu_mlp_bwd_fp8(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, layer.W13q,
+                                         layer.W13sc, layer.W2q, layer.W2sc, layer.GU, layer.A, layer.dYperm,
+                                         layer.dGU, layer.dXperm, layer.dW13, layer.dW2, X if sh else None,
+                                         dY if sh else None, layer.W13q_s, layer.W13sc_s, layer.W2q_s, layer.W2sc_s,
+                                         layer.GU_s, layer.A_s, layer.dGU_s, layer.dX_shared, layer.dW13_s,
+                                         layer.dW2_s, layer.fp8_ws, layer.ws)
+    else:
+        M.moe_grouped_swiglu_mlp_bwd(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, w.W13, w.W2,
+                                     layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm, layer.dW13, layer.dW2,
+                                     X if sh else None, dY if sh else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
+                                     layer.dGU_s, layer.dX_shared, layer.dW13_s, layer.dW2_s, layer.ws)
     rec(6)
     M.moe_router_topk_bwd(c, X, w.W_r, layer.logits, layer.scores, layer.topk_idx, layer.gates, layer.dgates,
                           layer.dW_r, layer.dlogit_bias if w.logit_bias is not None else None, layer.dX_router,
@@ -182,13 +198,20 @@ def run_step(layer, X, dY, ev=None):
 
 def launches_per_step(w):
     """Kernels of ours launched by run_step (memsets are not counted)."""
-    n = 1                         # router
-    n += 3                        # chunk histogram, scan, scatter
-    n += 2 + (2 if w.F_shared else 0)      # FC1 (+SwiGLU), FC2
-    n += 1 + 1                    # combine, combine backward
-    n += 4 + (4 if w.F_shared else 0)      # FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad
-    n += 1 + (1 if w.skew else 0) + 2      # dlogits, (bias column sums), dW_r, dX_router
-    n += 1                        # permute backward
+    sh = 1 if w.F_shared else 0
+    n = 1                                  # router
+    n += 4                                 # chunk histogram, scan, scatter, row copy
+    n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
+    n += 2                                 # combine, combine backward
+    n += 4 * (1 + sh)                      # FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad
+    n += 1 + (1 if w.skew else 0)          # dlogits, (bias column sums)
+    n += 3 if w.E > 32 else 1              # W_r split, dW_r, dX_router (E > 32) | dW_r, dX_router
+    n += 1 if w.E > 32 or w.T > 64 else 0  # fixed-order reduction of the dW_r partials
+    n += 1                                 # permute backward
+    if w.fp8:
+        n += 2 * (1 + sh)                  # weight quantization
+        n += 2 * (1 + sh)                  # forward activations (rows)
+        n += 6 * (1 + sh)                  # backward: 2 row-, 4 column-quantizations
     return n
 
 
@@ -257,7 +280,7 @@ def bench_ours(args, w):
     dev = torch.device("cuda", local)
     weights, X, dY = device_inputs(w, args.seed, dev)
     cfg = M.config_from(w)
-    layer = M.MoELayer(cfg, weights, device=dev)
+    layer = M.MoELayer(cfg, weights, device=dev, fp8=w.fp8)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -330,6 +353,10 @@ def bench_ours(args, w):
     gemm_ms = stage_ms["gemm_fwd"] + stage_ms["gemm_bwd"]
     gemm_tflops = gemm_flop / (gemm_ms / 1e3) / 1e12
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak_kind = f"{pk_kind} bf16 sustained"
+    if w.fp8:  # dense FP8 runs at twice the BF16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s)
+        peak_t *= 2.0
+        peak_kind = f"{pk_kind} bf16 sustained x 2 (FP8:BF16 nominal ratio)"
     traffic = traffic_record("k_grouped_gemm", w.name)
     hb = hbm_bytes(w)
     hbm = {}
@@ -340,17 +367,17 @@ def bench_ours(args, w):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if w.fp8 else "bf16", "data": "synthetic (seeded normal inputs)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared,
                    "router": ("softmax" if w.score_fn == 0 else "sigmoid") + (", renorm" if w.renorm else ""),
                    "l2": "inputs larger than L2 (expert weights %.2f GB re-read every step)" %
                          (w.E * 3 * w.F * w.H * 2 / 1e9),
                    "parallelism": "replicas" if ws_ > 1 else "single GPU"},
-        "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_bf16_peak": round(gemm_tflops / peak_t, 3),
+        "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_peak": round(gemm_tflops / peak_t, 3),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "roofline": {"kernel": "k_grouped_gemm (FC1+SwiGLU, FC2, FC2 dgrad+dSwiGLU, FC2 wgrad, FC1 dgrad, FC1 wgrad)",
                      "bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / peak_t, 3), "peak_source": f"{pk_kind} bf16 sustained",
+                     "frac": round(gemm_tflops / peak_t, 3), "peak_source": peak_kind,
                      "traffic": traffic},
         "hbm_stages": hbm,
         "clocks": clocks,

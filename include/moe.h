@@ -106,8 +106,7 @@ moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
  *                                    exact ties to the lower expert index
  *  gates    [T,k] fp32 out           combine weights (renormalised, times gate_scale)
  *  counts   [E] int32 out            tokens per expert
- *  ws       workspace (needed when E > 32: the logits then run on the tensor cores from an exact
- *           three-term bf16 split of W_r, FP32 accumulation) */
+ *  ws       workspace (unused by this call; may be NULL) */
 moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float* W_r,
                            const float* logit_bias, const float* sel_bias, float* logits, float* scores,
                            int32_t* topk_idx, float* gates, int32_t* counts, void* ws, void* stream);
@@ -178,7 +177,9 @@ moe_status moe_grouped_swiglu_mlp_bwd(const moe_config* cfg, const moe_bf16* Xpe
  * no gradient flows through the selection or sel_bias.
  *  logits, scores [T,E] fp32, topk_idx [T,k], gates, dgates [T,k] fp32 (device) in
  *  dW_r [E,H] fp32 out = dlogits^T X;  dlogit_bias [E] fp32 out (nullable) = column sums of dlogits;
- *  dX_router [T,H] fp32 out = dlogits W_r. */
+ *  dX_router [T,H] fp32 out = dlogits W_r.
+ * For E > 32 the dW_r and dX_router products run on the tensor cores from exact three-term
+ * bf16 splits of dlogits and W_r (FP32 accumulation), E must then be a multiple of 8. */
 moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const float* W_r, const float* logits,
                                const float* scores, const int32_t* topk_idx, const float* gates,
                                const float* dgates, float* dW_r, float* dlogit_bias, float* dX_router, void* ws,
@@ -188,6 +189,50 @@ moe_status moe_router_topk_bwd(const moe_config* cfg, const moe_bf16* X, const f
  * FP32 sum, one bf16 rounding.  dX_router [T,H] fp32 and dX_shared [T,H] bf16 are nullable. */
 moe_status moe_permute_bwd(const moe_config* cfg, const moe_bf16* dXperm, const int32_t* row_id_map,
                            const float* dX_router, const moe_bf16* dX_shared, moe_bf16* dX, void* stream);
+
+/* ---------------------------------------------------------------- FP8 E4M3 expert GEMMs
+ * ("Abstract" of the index page and "Method" of the summary page: FP8 low-precision
+ * training across the expert GEMMs, the router kept in higher precision.)  Every
+ * operand of the six expert GEMMs is quantized to E4M3 in blocks of 128 values that
+ * share one power-of-two scale (the smallest 2^e with 448*2^e >= the block's max |x|,
+ * stored as the UE8M0 byte e+127): activations in 1x128 blocks along each GEMM's K,
+ * weights in 128x128 blocks, weight-gradient operands in 128x1 blocks along the tokens.
+ * The GEMMs run on the block-scaled FP8 tensor cores with FP32 accumulation; stored
+ * tensors (GU, A, Yperm, dGU, dXperm, dW) stay bf16.  The router, gates, permute and
+ * combine calls are the bf16 ones above. */
+
+/* Bytes of the FP8 workspace (quantized activations and their scales). */
+moe_status moe_fp8_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Quantizes the expert weights: W13 [E,2F,H] -> W13q [E,2F,H] e4m3 + W13sc [E,2F/128,H/128]
+ * UE8M0; W2 [E,H,F] -> W2q + W2sc [E,H/128,F/128]; the shared expert's likewise
+ * (with E = 1) when F_shared > 0.  All pointers device, outputs caller-owned. */
+moe_status moe_quantize_weights_fp8(const moe_config* cfg, const moe_bf16* W13, const moe_bf16* W2,
+                                    const moe_bf16* W13_s, const moe_bf16* W2_s, uint8_t* W13q, uint8_t* W13sc,
+                                    uint8_t* W2q, uint8_t* W2sc, uint8_t* W13q_s, uint8_t* W13sc_s, uint8_t* W2q_s,
+                                    uint8_t* W2sc_s, void* stream);
+
+/* moe_grouped_swiglu_mlp with FP8 E4M3 GEMMs: quantized weights from
+ * moe_quantize_weights_fp8; activations are quantized on the fly into fp8_ws. */
+moe_status moe_grouped_swiglu_mlp_fp8(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                      const int32_t* tile_offsets, const uint8_t* W13q, const uint8_t* W13sc,
+                                      const uint8_t* W2q, const uint8_t* W2sc, moe_bf16* GU, moe_bf16* A,
+                                      moe_bf16* Yperm, const moe_bf16* X, const uint8_t* W13q_s,
+                                      const uint8_t* W13sc_s, const uint8_t* W2q_s, const uint8_t* W2sc_s,
+                                      moe_bf16* GU_s, moe_bf16* A_s, moe_bf16* Yshared, void* fp8_ws, void* ws,
+                                      void* stream);
+
+/* moe_grouped_swiglu_mlp_bwd with FP8 E4M3 GEMMs (same outputs, bf16). */
+moe_status moe_grouped_swiglu_mlp_bwd_fp8(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                          const int32_t* tile_offsets, const int32_t* counts, const uint8_t* W13q,
+                                          const uint8_t* W13sc, const uint8_t* W2q, const uint8_t* W2sc,
+                                          const moe_bf16* GU, const moe_bf16* A, const moe_bf16* dYperm,
+                                          moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* dW13, moe_bf16* dW2,
+                                          const moe_bf16* X, const moe_bf16* dY, const uint8_t* W13q_s,
+                                          const uint8_t* W13sc_s, const uint8_t* W2q_s, const uint8_t* W2sc_s,
+                                          const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                          moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* fp8_ws,
+                                          void* ws, void* stream);
 
 /* Dispatch without a workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart of this call; it exists because moe_permute

@@ -31,7 +31,8 @@ __all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
 EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_workspace_init",
             "moe_read_device_error", "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp",
             "moe_unpermute_combine", "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd",
-            "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc"]
+            "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc", "moe_fp8_workspace_size",
+            "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -75,6 +76,10 @@ def load(build: bool = True):
                 "moe_router_topk_bwd": [cfgp] + [vp] * 12,
                 "moe_permute_bwd": [cfgp] + [vp] * 6,
                 "moe_permute_noalloc": [cfgp] + [vp] * 9,
+                "moe_fp8_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t)],
+                "moe_quantize_weights_fp8": [cfgp] + [vp] * 13,
+                "moe_grouped_swiglu_mlp_fp8": [cfgp] + [vp] * 20,
+                "moe_grouped_swiglu_mlp_bwd_fp8": [cfgp] + [vp] * 29,
             }
             for name, args in sigs.items():
                 f = getattr(lib, name)
@@ -201,6 +206,38 @@ def moe_grouped_swiglu_mlp_bwd(cfg, Xperm, offsets, tile_offsets, counts, W13, W
     _call("moe_grouped_swiglu_mlp_bwd", cfg, *map(_ptr, ts), _stream(stream))
 
 
+def moe_fp8_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t()
+    _call("moe_fp8_workspace_size", cfg, ctypes.byref(n))
+    return n.value
+
+
+def moe_quantize_weights_fp8(cfg, W13, W2, W13_s, W2_s, W13q, W13sc, W2q, W2sc, W13q_s=None, W13sc_s=None,
+                             W2q_s=None, W2sc_s=None, stream=None):
+    ts = (W13, W2, W13_s, W2_s, W13q, W13sc, W2q, W2sc, W13q_s, W13sc_s, W2q_s, W2sc_s)
+    _dev(*ts)
+    _call("moe_quantize_weights_fp8", cfg, *map(_ptr, ts), _stream(stream))
+
+
+def moe_grouped_swiglu_mlp_fp8(cfg, Xperm, offsets, tile_offsets, W13q, W13sc, W2q, W2sc, GU, A, Yperm, X=None,
+                               W13q_s=None, W13sc_s=None, W2q_s=None, W2sc_s=None, GU_s=None, A_s=None, Yshared=None,
+                               fp8_ws=None, ws=None, stream=None):
+    ts = (Xperm, offsets, tile_offsets, W13q, W13sc, W2q, W2sc, GU, A, Yperm, X, W13q_s, W13sc_s, W2q_s, W2sc_s,
+          GU_s, A_s, Yshared, fp8_ws, ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_fp8", cfg, *map(_ptr, ts), _stream(stream))
+
+
+def moe_grouped_swiglu_mlp_bwd_fp8(cfg, Xperm, offsets, tile_offsets, counts, W13q, W13sc, W2q, W2sc, GU, A, dYperm,
+                                   dGU, dXperm, dW13, dW2, X=None, dY=None, W13q_s=None, W13sc_s=None, W2q_s=None,
+                                   W2sc_s=None, GU_s=None, A_s=None, dGU_s=None, dX_shared=None, dW13_s=None,
+                                   dW2_s=None, fp8_ws=None, ws=None, stream=None):
+    ts = (Xperm, offsets, tile_offsets, counts, W13q, W13sc, W2q, W2sc, GU, A, dYperm, dGU, dXperm, dW13, dW2, X, dY,
+          W13q_s, W13sc_s, W2q_s, W2sc_s, GU_s, A_s, dGU_s, dX_shared, dW13_s, dW2_s, fp8_ws, ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_bwd_fp8", cfg, *map(_ptr, ts), _stream(stream))
+
+
 def moe_router_topk_bwd(cfg, X, W_r, logits, scores, topk_idx, gates, dgates, dW_r, dlogit_bias, dX_router, ws,
                         stream=None):
     ts = (X, W_r, logits, scores, topk_idx, gates, dgates, dW_r, dlogit_bias, dX_router, ws)
@@ -232,9 +269,10 @@ class MoELayer:
     both can be captured in a CUDA graph.
     """
 
-    def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda"):
+    def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda", fp8: bool = False):
         self.cfg = cfg
         self.w = weights
+        self.fp8 = fp8
         T, H, E, k, F, Fs = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F, cfg.F_shared
         self.R = R = moe_max_rows(cfg)
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
@@ -259,6 +297,23 @@ class MoELayer:
             self.GU_s = self.A_s = self.Yshared = self.dGU_s = self.dX_shared = self.dW13_s = self.dW2_s = None
         self.X = None
         self.dY = None
+        if fp8:
+            u8 = torch.uint8
+            q = lambda *s: torch.empty(*s, dtype=u8, device=device)
+            self.W13q, self.W13sc = q(E, 2 * F, H), q(E, 2 * F // 128, H // 128)
+            self.W2q, self.W2sc = q(E, H, F), q(E, H // 128, F // 128)
+            if Fs:
+                self.W13q_s, self.W13sc_s = q(2 * Fs, H), q(2 * Fs // 128, H // 128)
+                self.W2q_s, self.W2sc_s = q(H, Fs), q(H // 128, Fs // 128)
+            else:
+                self.W13q_s = self.W13sc_s = self.W2q_s = self.W2sc_s = None
+            self.fp8_ws = q(moe_fp8_workspace_size(cfg))
+
+    def quantize_weights(self):
+        """FP8 mode: E4M3 copies of the expert weights (128x128 power-of-two block scales)."""
+        w = self.w
+        moe_quantize_weights_fp8(self.cfg, w.W13, w.W2, w.W13_s, w.W2_s, self.W13q, self.W13sc, self.W2q, self.W2sc,
+                                 self.W13q_s, self.W13sc_s, self.W2q_s, self.W2sc_s)
 
     def forward(self, X: torch.Tensor) -> torch.Tensor:
         c, w = self.cfg, self.w
@@ -267,9 +322,16 @@ class MoELayer:
                         self.counts, self.ws)
         moe_permute(c, X, self.topk_idx, self.counts, self.offsets, self.tile_offsets, self.row_id_map,
                     self.slot_src, self.Xperm, self.ws)
-        moe_grouped_swiglu_mlp(c, self.Xperm, self.offsets, self.tile_offsets, w.W13, w.W2, self.GU, self.A,
-                               self.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, self.GU_s, self.A_s,
-                               self.Yshared, self.ws)
+        if self.fp8:
+            self.quantize_weights()
+            moe_grouped_swiglu_mlp_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.W13q, self.W13sc,
+                                       self.W2q, self.W2sc, self.GU, self.A, self.Yperm, X if c.F_shared else None,
+                                       self.W13q_s, self.W13sc_s, self.W2q_s, self.W2sc_s, self.GU_s, self.A_s,
+                                       self.Yshared, self.fp8_ws, self.ws)
+        else:
+            moe_grouped_swiglu_mlp(c, self.Xperm, self.offsets, self.tile_offsets, w.W13, w.W2, self.GU, self.A,
+                                   self.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, self.GU_s, self.A_s,
+                                   self.Yshared, self.ws)
         moe_unpermute_combine(c, self.Yperm, self.row_id_map, self.gates, self.Yshared, self.Y)
         return self.Y
 
@@ -278,10 +340,19 @@ class MoELayer:
         self.dY = dY
         moe_unpermute_combine_bwd(c, dY, self.Yperm, self.row_id_map, self.gates, self.offsets, self.counts,
                                   self.dYperm, self.dgates)
-        moe_grouped_swiglu_mlp_bwd(c, self.Xperm, self.offsets, self.tile_offsets, self.counts, w.W13, w.W2, self.GU,
-                                   self.A, self.dYperm, self.dGU, self.dXperm, self.dW13, self.dW2,
-                                   self.X if c.F_shared else None, dY if c.F_shared else None, w.W13_s, w.W2_s,
-                                   self.GU_s, self.A_s, self.dGU_s, self.dX_shared, self.dW13_s, self.dW2_s, self.ws)
+        sh = c.F_shared > 0
+        if self.fp8:
+            moe_grouped_swiglu_mlp_bwd_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.counts, self.W13q,
+                                           self.W13sc, self.W2q, self.W2sc, self.GU, self.A, self.dYperm, self.dGU,
+                                           self.dXperm, self.dW13, self.dW2, self.X if sh else None,
+                                           dY if sh else None, self.W13q_s, self.W13sc_s, self.W2q_s, self.W2sc_s,
+                                           self.GU_s, self.A_s, self.dGU_s, self.dX_shared, self.dW13_s, self.dW2_s,
+                                           self.fp8_ws, self.ws)
+        else:
+            moe_grouped_swiglu_mlp_bwd(c, self.Xperm, self.offsets, self.tile_offsets, self.counts, w.W13, w.W2,
+                                       self.GU, self.A, self.dYperm, self.dGU, self.dXperm, self.dW13, self.dW2,
+                                       self.X if sh else None, dY if sh else None, w.W13_s, w.W2_s, self.GU_s,
+                                       self.A_s, self.dGU_s, self.dX_shared, self.dW13_s, self.dW2_s, self.ws)
         moe_router_topk_bwd(c, self.X, w.W_r, self.logits, self.scores, self.topk_idx, self.gates, self.dgates,
                             self.dW_r, self.dlogit_bias if w.logit_bias is not None else None, self.dX_router, self.ws)
         moe_permute_bwd(c, self.dXperm, self.row_id_map, self.dX_router, self.dX_shared, self.dX)

@@ -44,7 +44,7 @@ moe_status check_cfg(const moe_config* c, bool gemm) {
     if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k) return MOE_ERR_INVALID_ARG;
   }
   if (c->E > 256 || c->k > 32 || c->n_group > 32) return MOE_ERR_UNSUPPORTED;
-  if (c->E > 32 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;  // tensor-core router: fp32 rows of 32-byte multiples
+  if (c->E > 32 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;  // tensor-core router backward: 32-byte fp32 rows
   if (c->H % 128 != 0 || c->F % 128 != 0 || c->F_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k + (int64_t)c->E * (c->align - 1) >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->H >= (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
@@ -85,6 +85,47 @@ GemmShape shared_shape(const moe_config& c) {
   s.offsets = s.tile_offsets = s.counts = nullptr;
   s.nsm = num_sms();
   return s;
+}
+
+// FP8 workspace: per operand the E4M3 values and their UE8M0 block scales.
+// Routed operands have R rows, the shared expert's T rows.
+struct Fp8Buf {
+  uint8_t* q;
+  uint8_t* sc;
+};
+struct Fp8Set {  // one expert family (routed or shared)
+  Fp8Buf x, a, dy, dgu;      // row blocks (1x128 along K)
+  Fp8Buf dyc, ac, dguc, xc;  // token blocks (128x1)
+};
+struct Fp8Layout {
+  Fp8Set routed, shared;
+  size_t total;
+};
+
+Fp8Layout fp8_layout(const moe_config& c, void* base) {
+  Fp8Layout L{};
+  char* b = static_cast<char*>(base);
+  size_t o = 0;
+  auto take = [&](size_t n) {
+    char* p = b ? b + o : nullptr;
+    o = align256(o + n);
+    return reinterpret_cast<uint8_t*>(p);
+  };
+  auto rows_set = [&](Fp8Set& S, int64_t rows, int64_t H, int64_t F) {
+    const int64_t rb = (rows + 127) / 128;
+    S.x = {take(rows * H), take(rows * (H / 128))};
+    S.a = {take(rows * F), take(rows * (F / 128))};
+    S.dy = {take(rows * H), take(rows * (H / 128))};
+    S.dgu = {take(rows * 2 * F), take(rows * (2 * F / 128))};
+    S.dyc = {take(rows * H), take(rb * H)};
+    S.ac = {take(rows * F), take(rb * F)};
+    S.dguc = {take(rows * 2 * F), take(rb * 2 * F)};
+    S.xc = {take(rows * H), take(rb * H)};
+  };
+  rows_set(L.routed, max_rows(c), c.H, c.F);
+  if (c.F_shared > 0) rows_set(L.shared, c.T, c.H, c.F_shared);
+  L.total = o;
+  return L;
 }
 
 #define MOE_TRY(expr)                               \
@@ -155,14 +196,11 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
       !tok_ok(cfg, gates) || !counts)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(W_r) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
-  if (!ws && cfg->E > 32) return MOE_ERR_WORKSPACE;
+  (void)ws;
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  const WsLayout L = ws_layout(*cfg);
-  uint16_t* wsplit = ws ? ws_ptr<uint16_t>(ws, L.wsplit) : nullptr;
-  int* err = ws ? ws_ptr<int>(ws, L.err) : nullptr;
   return cuda_status(launch_router_topk(*cfg, X, W_r, logit_bias, sel_bias, logits, scores, topk_idx, gates, counts,
-                                        wsplit, err, (cudaStream_t)stream, nsm));
+                                        (cudaStream_t)stream, nsm));
 }
 
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
@@ -282,6 +320,142 @@ moe_status moe_grouped_swiglu_mlp_bwd(const moe_config* cfg, const moe_bf16* Xpe
     MOE_TRY(launch_fc2_wgrad(ss, dY, A_s, dW2_s, err, st));
     MOE_TRY(launch_fc1_dgrad(ss, dGU_s, W13_s, dX_shared, err, st));
     MOE_TRY(launch_fc1_wgrad(ss, dGU_s, X, dW13_s, err, st));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_fp8_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = fp8_layout(*cfg, nullptr).total;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_weights_fp8(const moe_config* cfg, const moe_bf16* W13, const moe_bf16* W2,
+                                    const moe_bf16* W13_s, const moe_bf16* W2_s, uint8_t* W13q, uint8_t* W13sc,
+                                    uint8_t* W2q, uint8_t* W2sc, uint8_t* W13q_s, uint8_t* W13sc_s, uint8_t* W2q_s,
+                                    uint8_t* W2sc_s, void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!W13 || !W2 || !W13q || !W13sc || !W2q || !W2sc) return MOE_ERR_INVALID_ARG;
+  const void* al[] = {W13, W2, W13q, W2q};
+  for (const void* p : al)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const moe_config& c = *cfg;
+  MOE_TRY(launch_quant_weights(W13, c.E, 2 * c.F, c.H, W13q, W13sc, st));
+  MOE_TRY(launch_quant_weights(W2, c.E, c.H, c.F, W2q, W2sc, st));
+  if (c.F_shared > 0) {
+    if (!W13_s || !W2_s || !W13q_s || !W13sc_s || !W2q_s || !W2sc_s) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(launch_quant_weights(W13_s, 1, 2 * c.F_shared, c.H, W13q_s, W13sc_s, st));
+    MOE_TRY(launch_quant_weights(W2_s, 1, c.H, c.F_shared, W2q_s, W2sc_s, st));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_grouped_swiglu_mlp_fp8(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                      const int32_t* tile_offsets, const uint8_t* W13q, const uint8_t* W13sc,
+                                      const uint8_t* W2q, const uint8_t* W2sc, moe_bf16* GU, moe_bf16* A,
+                                      moe_bf16* Yperm, const moe_bf16* X, const uint8_t* W13q_s,
+                                      const uint8_t* W13sc_s, const uint8_t* W2q_s, const uint8_t* W2sc_s,
+                                      moe_bf16* GU_s, moe_bf16* A_s, moe_bf16* Yshared, void* fp8_ws, void* ws,
+                                      void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!Xperm || !offsets || !tile_offsets || !W13q || !W13sc || !W2q || !W2sc || !GU || !A || !Yperm)
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {Xperm, W13q, W2q, GU, A, Yperm};
+  for (const void* p : al)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0 &&
+      (!tok_ok(cfg, X) || !W13q_s || !W13sc_s || !W2q_s || !W2sc_s || !tok_ok(cfg, GU_s) || !tok_ok(cfg, A_s) ||
+       !tok_ok(cfg, Yshared)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || !fp8_ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const moe_config& c = *cfg;
+  int* err = err_word(ws, c);
+  const Fp8Layout L = fp8_layout(c, fp8_ws);
+  const GemmShape rs = routed_shape(c, offsets, tile_offsets, nullptr);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  const int32_t* rv = offsets + c.E;  // rows in use, read on the device
+  const Fp8Set& R = L.routed;
+  MOE_TRY(launch_quant_rows(Xperm, rs.rows, c.H, rv, R.x.q, R.x.sc, rs.nsm, st));
+  MOE_TRY(launch_fc1_fwd_fp8(rs, {R.x.q, R.x.sc}, {W13q, W13sc}, GU, A, err, st));
+  MOE_TRY(launch_quant_rows(A, rs.rows, c.F, rv, R.a.q, R.a.sc, rs.nsm, st));
+  MOE_TRY(launch_fc2_fwd_fp8(rs, {R.a.q, R.a.sc}, {W2q, W2sc}, Yperm, err, st));
+  if (c.F_shared > 0 && c.T > 0) {
+    const GemmShape ss = shared_shape(c);
+    const Fp8Set& Sh = L.shared;
+    MOE_TRY(launch_quant_rows(X, c.T, c.H, nullptr, Sh.x.q, Sh.x.sc, rs.nsm, st));
+    MOE_TRY(launch_fc1_fwd_fp8(ss, {Sh.x.q, Sh.x.sc}, {W13q_s, W13sc_s}, GU_s, A_s, err, st));
+    MOE_TRY(launch_quant_rows(A_s, c.T, c.F_shared, nullptr, Sh.a.q, Sh.a.sc, rs.nsm, st));
+    MOE_TRY(launch_fc2_fwd_fp8(ss, {Sh.a.q, Sh.a.sc}, {W2q_s, W2sc_s}, Yshared, err, st));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_grouped_swiglu_mlp_bwd_fp8(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                          const int32_t* tile_offsets, const int32_t* counts, const uint8_t* W13q,
+                                          const uint8_t* W13sc, const uint8_t* W2q, const uint8_t* W2sc,
+                                          const moe_bf16* GU, const moe_bf16* A, const moe_bf16* dYperm,
+                                          moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* dW13, moe_bf16* dW2,
+                                          const moe_bf16* X, const moe_bf16* dY, const uint8_t* W13q_s,
+                                          const uint8_t* W13sc_s, const uint8_t* W2q_s, const uint8_t* W2sc_s,
+                                          const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                          moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* fp8_ws,
+                                          void* ws, void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!Xperm || !offsets || !tile_offsets || !counts || !W13q || !W13sc || !W2q || !W2sc || !GU || !A || !dYperm ||
+      !dGU || !dXperm || !dW13 || !dW2)
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {Xperm, W13q, W2q, GU, A, dYperm, dGU, dXperm, dW13, dW2};
+  for (const void* p : al)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0 &&
+      (!tok_ok(cfg, X) || !tok_ok(cfg, dY) || !W13q_s || !W13sc_s || !W2q_s || !W2sc_s || !tok_ok(cfg, GU_s) ||
+       !tok_ok(cfg, A_s) || !tok_ok(cfg, dGU_s) || !tok_ok(cfg, dX_shared) || !dW13_s || !dW2_s))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || !fp8_ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const moe_config& c = *cfg;
+  int* err = err_word(ws, c);
+  const Fp8Layout L = fp8_layout(c, fp8_ws);
+  const GemmShape rs = routed_shape(c, offsets, tile_offsets, counts);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  const int32_t* rv = offsets + c.E;
+  const Fp8Set& R = L.routed;
+  MOE_TRY(launch_quant_rows(dYperm, rs.rows, c.H, rv, R.dy.q, R.dy.sc, rs.nsm, st));
+  MOE_TRY(launch_fc2_dgrad_fp8(rs, {R.dy.q, R.dy.sc}, {W2q, W2sc}, GU, dGU, err, st));
+  MOE_TRY(launch_quant_cols(dYperm, rs.rows, c.H, rv, R.dyc.q, R.dyc.sc, st));
+  MOE_TRY(launch_quant_cols(A, rs.rows, c.F, rv, R.ac.q, R.ac.sc, st));
+  MOE_TRY(launch_fc2_wgrad_fp8(rs, {R.dyc.q, R.dyc.sc}, {R.ac.q, R.ac.sc}, dW2, err, st));
+  MOE_TRY(launch_quant_rows(dGU, rs.rows, 2 * c.F, rv, R.dgu.q, R.dgu.sc, rs.nsm, st));
+  MOE_TRY(launch_fc1_dgrad_fp8(rs, {R.dgu.q, R.dgu.sc}, {W13q, W13sc}, dXperm, err, st));
+  MOE_TRY(launch_quant_cols(dGU, rs.rows, 2 * c.F, rv, R.dguc.q, R.dguc.sc, st));
+  MOE_TRY(launch_quant_cols(Xperm, rs.rows, c.H, rv, R.xc.q, R.xc.sc, st));
+  MOE_TRY(launch_fc1_wgrad_fp8(rs, {R.dguc.q, R.dguc.sc}, {R.xc.q, R.xc.sc}, dW13, err, st));
+  if (c.F_shared > 0) {
+    if (c.T == 0) {
+      MOE_TRY(cudaMemsetAsync(dW13_s, 0, sizeof(moe_bf16) * 2 * c.F_shared * c.H, st));
+      MOE_TRY(cudaMemsetAsync(dW2_s, 0, sizeof(moe_bf16) * c.F_shared * c.H, st));
+      return MOE_OK;
+    }
+    const GemmShape ss = shared_shape(c);
+    const Fp8Set& Sh = L.shared;
+    const int Fs = c.F_shared;
+    MOE_TRY(launch_quant_rows(dY, c.T, c.H, nullptr, Sh.dy.q, Sh.dy.sc, rs.nsm, st));
+    MOE_TRY(launch_fc2_dgrad_fp8(ss, {Sh.dy.q, Sh.dy.sc}, {W2q_s, W2sc_s}, GU_s, dGU_s, err, st));
+    MOE_TRY(launch_quant_cols(dY, c.T, c.H, nullptr, Sh.dyc.q, Sh.dyc.sc, st));
+    MOE_TRY(launch_quant_cols(A_s, c.T, Fs, nullptr, Sh.ac.q, Sh.ac.sc, st));
+    MOE_TRY(launch_fc2_wgrad_fp8(ss, {Sh.dyc.q, Sh.dyc.sc}, {Sh.ac.q, Sh.ac.sc}, dW2_s, err, st));
+    MOE_TRY(launch_quant_rows(dGU_s, c.T, 2 * Fs, nullptr, Sh.dgu.q, Sh.dgu.sc, rs.nsm, st));
+    MOE_TRY(launch_fc1_dgrad_fp8(ss, {Sh.dgu.q, Sh.dgu.sc}, {W13q_s, W13sc_s}, dX_shared, err, st));
+    MOE_TRY(launch_quant_cols(dGU_s, c.T, 2 * Fs, nullptr, Sh.dguc.q, Sh.dguc.sc, st));
+    MOE_TRY(launch_quant_cols(X, c.T, c.H, nullptr, Sh.xc.q, Sh.xc.sc, st));
+    MOE_TRY(launch_fc1_wgrad_fp8(ss, {Sh.dguc.q, Sh.dguc.sc}, {Sh.xc.q, Sh.xc.sc}, dW13_s, err, st));
   }
   return MOE_OK;
 }

@@ -22,7 +22,6 @@ struct WsLayout {
   size_t rbwd_part;     // E <= 32: float[splits * E * H] token-split partials of dW_r
   int rbwd_splits;
   // E > 32 (router GEMMs on the tensor cores, exact three-term bf16 splits):
-  size_t wsplit;        // bf16[E * 3H]     W_r as hi | mid | lo along K (forward)
   size_t wb;            // bf16[6Ep * H]    W_r row blocks hi, mid, hi, lo, hi, mid (dX_router)
   size_t dl_rows;       // bf16[3Tp * Ep]   dlogits row blocks hi, mid, lo (dW_r)
   size_t dl_cols;       // bf16[T * 6Ep]    dlogits column blocks hi, hi, mid, hi, lo, mid (dX_router)
@@ -42,10 +41,11 @@ inline int router_bwd_splits(const moe_config& c) {
     const int s = (c.T + 63) / 64;
     return s < 64 ? s : 64;
   }
-  const int tiles = ((c.H + 127) / 128) * ((c.E + 127) / 128);
+  // tensor-core dW_r: output tiles of 128 x 256 over [E, H]; rows 3*Tp split in 64-row multiples
+  const int tiles = ((c.H + 255) / 256) * ((c.E + 127) / 128);
   int s = (304 + tiles - 1) / tiles;
-  s = s < 16 ? s : 16;
-  const int kmax = (c.T + 7) / 8;
+  s = s < 32 ? s : 32;
+  const int kmax = (3 * ((c.T + 63) / 64 * 64)) / 64;
   return s < kmax ? s : kmax;
 }
 
@@ -63,12 +63,10 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + (size_t)c.T * c.E * sizeof(float));
   L.rbwd_splits = router_bwd_splits(c);
   L.rbwd_part = o;
-  if (c.E <= 32) o = align256(o + (size_t)L.rbwd_splits * c.E * c.H * sizeof(float));
+  o = align256(o + (size_t)L.rbwd_splits * c.E * c.H * sizeof(float));
   L.Tp = (c.T + 63) / 64 * 64;
   L.Ep = (c.E + 31) / 32 * 32;
   const bool tc = c.E > 32;
-  L.wsplit = o;
-  if (tc) o = align256(o + (size_t)c.E * 3 * c.H * 2);
   L.wb = o;
   if (tc) o = align256(o + (size_t)6 * L.Ep * c.H * 2);
   L.dl_rows = o;
@@ -218,6 +216,24 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A * B^T, kind::mxf8f6f4 with per-row UE8M0 block scales read from tensor
+// memory (one scale per row per 32-wide K step).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// One 32-bit column into this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -274,6 +290,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B and UE8M0 scales:
+//  bits 4-5 B scale-factor id (0), 7-9 A format (0 = E4M3), 10-12 B format (0 = E4M3),
+//  15/16 A/B major (1 = MN), 17-22 N >> 3, 23 scale type (1 = UE8M0), 24-28 M >> 4,
+//  29-30 A scale-factor id (0).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_mn, int b_mn) {
+  return ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.

@@ -32,8 +32,17 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 192;
+constexpr int BM = 128;
+// every stage holds 128 bytes of K per row: 64 bf16 or 128 FP8 elements
+template <bool FP8>
+struct Geo {
+  static constexpr int EB = FP8 ? 1 : 2;          // element bytes
+  static constexpr int BKE = 128 / EB;            // K elements per stage
+  static constexpr int MN_INNER = 128 / EB;       // elements of one 128-byte MN-major row
+  static constexpr int MN_BOX = 128 * BKE;        // bytes of one MN-major box (MN_INNER x BKE)
+  static constexpr int KSTEP = FP8 ? 32 : 16;     // K of one MMA instruction
+  static constexpr int THREADS = FP8 ? 320 : 192; // + 4 scale-factor warps for FP8
+};
 constexpr int kStagingBytes = 16384;
 constexpr int kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
 
@@ -58,8 +67,15 @@ struct GemmArgs {
   int64_t ldgu;
   int F;                    // SWIGLU / DSWIGLU: column offset of the "up" half
   int n_valid;              // > 0: output columns at or beyond n_valid are not stored
+  int ksplit_rows;          // WGRAD dense: > 0 splits the rows into chunks of this many ("experts")
   int kwrap;                // K-major A (FWD/DGRAD): the K coordinate wraps modulo kwrap;
                             // WGRAD: B's row coordinate wraps modulo kwrap (0: no wrap)
+  // FP8 block scales (UE8M0 bytes): A and B, addressed per mode (see the SF warps)
+  const uint8_t* sfa;
+  int64_t sfa_ld;
+  const uint8_t* sfb;
+  int sfb_r, sfb_c;
+  int64_t sfb_ld;
   int* err;
 };
 
@@ -67,7 +83,7 @@ struct Tile {
   int e, m0, n0, k0, kb;
 };
 
-template <int MODE, int EPI, int BN>
+template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                             const int* s_cnt) {
   Tile r;
@@ -104,7 +120,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.e = e;
     r.m0 = (local % g.m_tiles) * BM;
     r.n0 = (local / g.m_tiles) * BN;
-    if (g.dense_rows > 0) {
+    if (g.dense_rows > 0 && g.ksplit_rows > 0) {
+      r.k0 = e * g.ksplit_rows;
+      const int rows = g.dense_rows - r.k0 < g.ksplit_rows ? g.dense_rows - r.k0 : g.ksplit_rows;
+      r.kb = rows > 0 ? (rows + BK - 1) / BK : 0;
+    } else if (g.dense_rows > 0) {
       r.k0 = 0;
       r.kb = (g.dense_rows + BK - 1) / BK;
     } else {
@@ -121,15 +141,20 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
 }
 
-template <int MODE, int EPI, int BN, int ST>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int EPI, int BN, int ST, bool FP8>
+__global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapD, const GemmArgs g) {
-  constexpr int A_BYTES = BM * BK * 2;
-  constexpr int B_BYTES = BN * BK * 2;
+  using G = Geo<FP8>;
+  constexpr int BK = G::BKE;
+  constexpr int kThreads = G::THREADS;
+  constexpr int A_BYTES = BM * 128;
+  constexpr int B_BYTES = BN * 128;
   constexpr int STAGE = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
+  constexpr uint32_t TMEM_COLS = FP8 ? 512 : 2 * BN;  // FP8: accumulators + per-stage scale columns
+  constexpr uint32_t SFC = 2 * BN;                    // first scale-factor column (FP8): 8 per stage
+  constexpr uint32_t IDESC = FP8 ? idesc_mxf8(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD)
+                                 : idesc_bf16(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
   constexpr bool TMA_OUT = EPI != EPI_SWIGLU;  // outputs leave through the staging buffer and TMA stores
 
   extern __shared__ uint8_t smem_raw[];
@@ -139,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* staging = smem + ST * STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* empty = full + ST;
-  uint64_t* acc_full = empty + ST;
+  uint64_t* sf_full = empty + ST;  // FP8: this stage's scale factors are in tensor memory
+  uint64_t* acc_full = sf_full + ST;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -159,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -184,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mt = g.dense_rows > 0 ? (g.dense_rows + BM - 1) / BM : s_tile[g.E];
     total = mt * g.n_tiles;
   } else {
-    total = (g.dense_rows > 0 ? 1 : g.E) * g.m_tiles * g.n_tiles;
+    total = (g.dense_rows > 0 && g.ksplit_rows <= 0 ? 1 : g.E) * g.m_tiles * g.n_tiles;
   }
 
   if (warp == 0) {
@@ -194,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, used = 0, last_par = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+        const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
         for (int kb = 0; kb < tl.kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
@@ -207,11 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar, STAGE);
           const int kc = kb * BK;
           if constexpr (MODE == MODE_WGRAD) {
-            tma_load_2d(sa, &mapA, bar, tl.m0, tl.k0 + kc);
-            tma_load_2d(sa + 8192, &mapA, bar, tl.m0 + 64, tl.k0 + kc);
+#pragma unroll
+            for (int j = 0; j < BM / G::MN_INNER; ++j)
+              tma_load_2d(sa + j * G::MN_BOX, &mapA, bar, tl.m0 + G::MN_INNER * j, tl.k0 + kc);
             const int kb_row = g.kwrap > 0 ? (tl.k0 + kc) % g.kwrap : tl.k0 + kc;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, kb_row);
+            for (int j = 0; j < BN / G::MN_INNER; ++j)
+              tma_load_2d(sb + j * G::MN_BOX, &mapB, bar, tl.n0 + G::MN_INNER * j, kb_row);
           } else {
             tma_load_2d(sa, &mapA, bar, g.kwrap > 0 ? kc % g.kwrap : kc, tl.m0);
             if constexpr (MODE == MODE_FWD) {
@@ -223,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 8192, &mapB, bar, tl.n0 + 64 * j, kc, tl.e);
+              for (int j = 0; j < BN / G::MN_INNER; ++j)
+                tma_load_3d(sb + j * G::MN_BOX, &mapB, bar, tl.n0 + G::MN_INNER * j, kc, tl.e);
             }
           }
           used |= 1u << stage;
@@ -246,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+        const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
         if (tl.kb == 0) continue;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
           set_device_error(g.err, MOE_ERR_TIMEOUT, 3);
@@ -255,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
         for (int kb = 0; kb < tl.kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
+          if (!mbar_wait(&full[stage], phase) || (FP8 && !mbar_wait(&sf_full[stage], phase))) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 4);
             ok = false;
             break;
@@ -263,13 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(tiles + stage * STAGE);
           const uint32_t sb = sa + A_BYTES;
+          // K-major operands step 32 bytes per instruction inside the 128-byte swizzle row;
+          // MN-major operands step KSTEP rows of 128 bytes, with MN atoms MN_BOX bytes apart
+          constexpr uint32_t MN_STEP = G::KSTEP * 128;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+          for (int kk = 0; kk < BK / G::KSTEP; ++kk) {
+            const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * MN_STEP, G::MN_BOX, 1024)
                                                    : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = MODE == MODE_FWD ? smem_desc_sw128(sb + kk * 32, 16, 1024)
-                                                 : smem_desc_sw128(sb + kk * 2048, 8192, 1024);
-            umma_f16(d, ad, bd, IDESC, (kb | kk) != 0);
+                                                 : smem_desc_sw128(sb + kk * MN_STEP, G::MN_BOX, 1024);
+            if constexpr (FP8)
+              umma_mxf8(d, ad, bd, IDESC, tmem + SFC + 8 * stage, tmem + SFC + 8 * stage + 4, (kb | kk) != 0);
+            else
+              umma_f16(d, ad, bd, IDESC, (kb | kk) != 0);
           }
           umma_commit(&empty[stage]);
           if (++stage == ST) {
@@ -286,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) set_device_error(g.err, MOE_ERR_TIMEOUT, 5);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;  // row within the tile = tensor-memory lane
@@ -331,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(kEpiBarrier, 128);
     };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE, EPI, BN>(t, g, s_seg, s_tile, s_cnt);
+      const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
       const int64_t row = tl.m0 + r;
       if constexpr (EPI == EPI_DSWIGLU) {
         // pull this row's saved pre-activations into L2 while the accumulator fills
@@ -392,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) {
               gv[i] = __uint_as_float(gr[i]);
               uv[i] = __uint_as_float(ur[i]);
-              av[i] = gv[i] / (1.0f + __expf(-gv[i])) * uv[i];
+              // silu(g) * u with the fast reciprocal (outputs are bf16; exp(-g) = inf gives 0)
+              av[i] = __fdividef(gv[i], 1.0f + __expf(-gv[i])) * uv[i];
             }
             const int col = tl.n0 + c * 32;
             store32(g.D + row * g.ldd + col, gv);
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float da = __uint_as_float(dr[8 * v + i]);
-                const float s = 1.0f / (1.0f + __expf(-gf[i]));
+                const float s = __fdividef(1.0f, 1.0f + __expf(-gf[i]));  // sigmoid, fast reciprocal
                 const float sl = gf[i] * s;
                 dg[8 * v + i] = da * uf[i] * (s * (1.0f + gf[i] * (1.0f - s)));
                 du[8 * v + i] = da * sl;
@@ -479,6 +516,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every store has finished before the CTA (and its shared memory) goes away
     if (TMA_OUT && leader) bulk_wait_group<0>();
+  } else if constexpr (FP8) {
+    // ------------------------------------------------------------ scale-factor warps (FP8)
+    // Each warp owns one 32-lane quarter of tensor memory: for every stage it writes the
+    // UE8M0 scale of each of its 32 tile rows of A and of B (the byte repeated 4 times,
+    // so every scale-factor id reads the same value) into the stage's A and B columns.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+      for (int kb = 0; kb < tl.kb; ++kb) {
+        const bool w_ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1) : false, 0);
+        if (!w_ok) {
+          if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 7);
+          ok = false;
+          break;
+        }
+        uint32_t a = 127, b = 127;
+        if constexpr (MODE == MODE_WGRAD) {
+          const int64_t blk = tl.k0 / 128 + kb;  // 128-row block of the token dimension
+          a = g.sfa[blk * g.sfa_ld + tl.m0 + r];
+          b = g.sfb[blk * g.sfb_ld + tl.n0 + r];
+        } else {
+          const int64_t row = tl.m0 + r;
+          if (g.dense_rows <= 0 || row < g.dense_rows) a = g.sfa[row * g.sfa_ld + kb];
+          if constexpr (MODE == MODE_FWD) {  // weights [E][N rows][K]: block (n/128, kb)
+            const int nrow = EPI == EPI_SWIGLU ? (r < BN / 2 ? tl.n0 + r : g.F + tl.n0 + r - BN / 2) : tl.n0 + r;
+            b = g.sfb[((int64_t)tl.e * g.sfb_r + nrow / 128) * g.sfb_c + kb];
+          } else {  // weights [E][K rows][N]: block (kb, n/128)
+            b = g.sfb[((int64_t)tl.e * g.sfb_r + kb) * g.sfb_c + (tl.n0 + r) / 128];
+          }
+        }
+        // scale-factor columns start on 4-column (128-bit) boundaries: A at SFC + 8*stage, B 4 after
+        const uint32_t sf_addr = tmem + ((uint32_t)(q * 32) << 16) + SFC + 8 * stage;
+        tmem_st1(sf_addr, a * 0x01010101u);
+        tmem_st1(sf_addr + 4, b * 0x01010101u);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[stage]);
+        if (++stage == ST) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -490,11 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int EPI, int BN>
+template <int MODE, int EPI, int BN, bool FP8>
 struct Kern {
   static constexpr int ST = BN == 256 ? 4 : 6;
-  static constexpr int STAGE = (BM + BN) * BK * 2;
-  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (2 * ST + 5) * 8 + 16 + 3 * 260 * 4;
+  static constexpr int STAGE = (BM + BN) * 128;
+  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (3 * ST + 5) * 8 + 16 + 3 * 260 * 4;
 };
 
 // ---------------------------------------------------------------- host side
@@ -518,7 +603,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, 
               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const uint64_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
+  const uint64_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
   cuuint64_t gd[3], gs[2];
   cuuint32_t bd[3] = {box0, box1, 1}, es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) gd[i] = dims[i];
@@ -546,18 +631,29 @@ bool map_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uin
   return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// FP8 operand maps (bytes), 128-byte swizzle
+bool map2d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t b0, uint32_t b1) {
+  const uint64_t dims[2] = {inner, outer}, st[1] = {inner};
+  return make_map(m, base, 2, dims, st, b0, b1, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+bool map3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer, uint32_t b0,
+              uint32_t b1) {
+  const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
+  return make_map(m, base, 3, dims, st, b0, b1, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 // fp32 output map: boxes of 32 columns x 128 rows, 128-byte swizzle
 bool map_out_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer) {
   const uint64_t dims[3] = {inner, mid, outer}, st[2] = {inner, inner * mid};
   return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
-template <int MODE, int EPI, int BN>
+template <int MODE, int EPI, int BN, bool FP8 = false>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const GemmArgs& g, int max_tiles,
                    int nsm, cudaStream_t st) {
-  using K = Kern<MODE, EPI, BN>;
+  using K = Kern<MODE, EPI, BN, FP8>;
   static bool attr = false;
-  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST>;
+  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8>;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
     if (e != cudaSuccess) return e;
@@ -565,7 +661,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
   }
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = max_tiles < nsm ? max_tiles : nsm;
-  kern<<<grid, kThreads, K::smem, st>>>(a, b, d, g);
+  kern<<<grid, Geo<FP8>::THREADS, K::smem, st>>>(a, b, d, g);
   return cudaGetLastError();
 }
 
@@ -668,38 +764,115 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
                    : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }
 
+// ---------------------------------------------------------------- FP8 expert GEMMs
+// E4M3 operands with UE8M0 block scales; 128 x 128 x 128 tiles on kind::mxf8f6f4.
+
+cudaError_t launch_fc1_fwd_fp8(const GemmShape& s, const Fp8Op& X1, const Fp8Op& W13, uint16_t* GU, uint16_t* Aact,
+                               int* err, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map2d_u8(&ma, X1.q, s.H, s.rows, 128, 128) || !map3d_u8(&mb, W13.q, s.H, 2 * (uint64_t)s.F, s.E, 128, 64))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.H; g.n_tiles = s.F / 64; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = GU; g.ldd = 2 * (int64_t)s.F; g.D2 = Aact; g.ldd2 = s.F; g.F = s.F; g.err = err;
+  g.sfa = X1.sc; g.sfa_ld = s.H / 128; g.sfb = W13.sc; g.sfb_r = 2 * s.F / 128; g.sfb_c = s.H / 128;
+  return launch<MODE_FWD, EPI_SWIGLU, 128, true>(ma, mb, ma, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+cudaError_t launch_fc2_fwd_fp8(const GemmShape& s, const Fp8Op& A1, const Fp8Op& W2, uint16_t* Y, int* err,
+                               cudaStream_t st) {
+  CUtensorMap ma, mb, md;
+  if (!map2d_u8(&ma, A1.q, s.F, s.rows, 128, 128) || !map3d_u8(&mb, W2.q, s.F, s.H, s.E, 128, 128) ||
+      !map_out(&md, Y, s.H, s.rows, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.F; g.n_tiles = s.H / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = Y; g.ldd = s.H; g.err = err;
+  g.sfa = A1.sc; g.sfa_ld = s.F / 128; g.sfb = W2.sc; g.sfb_r = s.H / 128; g.sfb_c = s.F / 128;
+  return launch<MODE_FWD, EPI_STORE, 128, true>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+cudaError_t launch_fc2_dgrad_fp8(const GemmShape& s, const Fp8Op& dY1, const Fp8Op& W2, const uint16_t* GU,
+                                 uint16_t* dGU, int* err, cudaStream_t st) {
+  CUtensorMap ma, mb, md;
+  if (!map2d_u8(&ma, dY1.q, s.H, s.rows, 128, 128) || !map3d_u8(&mb, W2.q, s.F, s.H, s.E, 128, 128) ||
+      !map_out(&md, dGU, 2 * (uint64_t)s.F, s.rows, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dGU; g.ldd = 2 * (int64_t)s.F; g.GU = GU; g.ldgu = 2 * (int64_t)s.F; g.F = s.F; g.err = err;
+  g.sfa = dY1.sc; g.sfa_ld = s.H / 128; g.sfb = W2.sc; g.sfb_r = s.H / 128; g.sfb_c = s.F / 128;
+  return launch<MODE_DGRAD, EPI_DSWIGLU, 128, true>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+cudaError_t launch_fc1_dgrad_fp8(const GemmShape& s, const Fp8Op& dGU1, const Fp8Op& W13, uint16_t* dX1, int* err,
+                                 cudaStream_t st) {
+  CUtensorMap ma, mb, md;
+  if (!map2d_u8(&ma, dGU1.q, 2 * (uint64_t)s.F, s.rows, 128, 128) ||
+      !map3d_u8(&mb, W13.q, s.H, 2 * (uint64_t)s.F, s.E, 128, 128) || !map_out(&md, dX1, s.H, s.rows, 1))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.K = 2 * s.F; g.n_tiles = s.H / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dX1; g.ldd = s.H; g.err = err;
+  g.sfa = dGU1.sc; g.sfa_ld = 2 * s.F / 128; g.sfb = W13.sc; g.sfb_r = 2 * s.F / 128; g.sfb_c = s.H / 128;
+  return launch<MODE_DGRAD, EPI_STORE, 128, true>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
+}
+
+// Column-quantized operands: q [rows, cols], scales [rows/128, cols].
+cudaError_t launch_fc2_wgrad_fp8(const GemmShape& s, const Fp8Op& dYc, const Fp8Op& Ac, uint16_t* dW2, int* err,
+                                 cudaStream_t st) {
+  CUtensorMap ma, mb, md;
+  if (!map2d_u8(&ma, dYc.q, s.H, s.rows, 128, 128) || !map2d_u8(&mb, Ac.q, s.F, s.rows, 128, 128) ||
+      !map_out(&md, dW2, s.F, s.H, s.dense_rows > 0 ? 1 : s.E))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.m_tiles = s.H / 128; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
+  g.sfa = dYc.sc; g.sfa_ld = s.H; g.sfb = Ac.sc; g.sfb_ld = s.F;
+  const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  return launch<MODE_WGRAD, EPI_STORE, 128, true>(ma, mb, md, g, tiles, s.nsm, st);
+}
+
+cudaError_t launch_fc1_wgrad_fp8(const GemmShape& s, const Fp8Op& dGUc, const Fp8Op& Xc, uint16_t* dW13, int* err,
+                                 cudaStream_t st) {
+  CUtensorMap ma, mb, md;
+  if (!map2d_u8(&ma, dGUc.q, 2 * (uint64_t)s.F, s.rows, 128, 128) || !map2d_u8(&mb, Xc.q, s.H, s.rows, 128, 128) ||
+      !map_out(&md, dW13, s.H, 2 * (uint64_t)s.F, s.dense_rows > 0 ? 1 : s.E))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = s.E; g.m_tiles = 2 * s.F / 128; g.n_tiles = s.H / 128; g.dense_rows = s.dense_rows;
+  g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
+  g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
+  g.sfa = dGUc.sc; g.sfa_ld = 2 * s.F; g.sfb = Xc.sc; g.sfb_ld = s.H;
+  const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  return launch<MODE_WGRAD, EPI_STORE, 128, true>(ma, mb, md, g, tiles, s.nsm, st);
+}
+
 // ---------------------------------------------------------------- router GEMMs on tensor cores
 // FP32-grade products from bf16 operands: every FP32 operand is split exactly into
 // three bf16 terms (hi + mid + lo), each bf16 x bf16 product is exact in the FP32
 // accumulator, and the terms are laid out along K so one GEMM sums them.
 
-// logits[T,E] (fp32) = X[T,H] . Wsplit[E,3H]^T; A's K coordinate wraps every H columns.
-cudaError_t launch_router_logits_tc(int T, int H, int E, const uint16_t* X, const uint16_t* Wsplit, float* logits,
-                                   int* err, int nsm, cudaStream_t st) {
-  const int bn = E <= 128 ? 128 : 256;
-  CUtensorMap ma, mb, md;
-  if (!map2d(&ma, X, H, T, 64, 128) || !map3d(&mb, Wsplit, 3 * (uint64_t)H, E, 1, 64, bn) ||
-      !map_out_f32(&md, logits, E, T, 1))
-    return cudaErrorInvalidValue;
-  GemmArgs g{};
-  g.E = 1; g.K = 3 * H; g.n_tiles = 1; g.dense_rows = T; g.kwrap = H; g.n_valid = E; g.err = err;
-  const int tiles = (T + 127) / 128;
-  return bn == 256 ? launch<MODE_FWD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
-                   : launch<MODE_FWD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
-}
-
 // dW_r[E,H] (fp32) = sum over the 3*Tp rows of dlsplit[3Tp,Ep] (hi rows, mid rows, lo rows,
 // each block zero beyond T) times X rows taken modulo Tp (rows >= T read as zero).
 cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint16_t* dlsplit, const uint16_t* X,
-                                 float* dWr, int* err, int nsm, cudaStream_t st) {
+                                 float* dWr, int splits, int* err, int nsm, cudaStream_t st) {
   const int bn = H % 256 == 0 ? 256 : 128;
   CUtensorMap ma, mb, md;
   if (!map2d(&ma, dlsplit, Ep, 3 * (uint64_t)Tp, 64, 64) || !map2d(&mb, X, H, T, 64, 64) ||
-      !map_out_f32(&md, dWr, H, E, 1))
+      !map_out_f32(&md, dWr, H, E, splits))
     return cudaErrorInvalidValue;
   GemmArgs g{};
-  g.E = 1; g.m_tiles = (E + 127) / 128; g.n_tiles = H / bn; g.dense_rows = 3 * Tp; g.kwrap = Tp; g.err = err;
-  const int tiles = g.m_tiles * g.n_tiles;
+  g.E = splits; g.m_tiles = (E + 127) / 128; g.n_tiles = H / bn; g.dense_rows = 3 * Tp; g.kwrap = Tp; g.err = err;
+  // split s covers rows [s*ksplit_rows, ...) of the 3*Tp and writes the s-th [E,H] partial
+  g.ksplit_rows = (3 * Tp / splits + 63) / 64 * 64;
+  g.d_estride = (int64_t)E * H;
+  const int tiles = splits * g.m_tiles * g.n_tiles;
   return bn == 256 ? launch<MODE_WGRAD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
                    : launch<MODE_WGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
 }

@@ -20,10 +20,16 @@ struct GemmShape {
   int nsm;
 };
 
+// An FP8 E4M3 operand: values and their UE8M0 block scales.
+struct Fp8Op {
+  const uint8_t* q;
+  const uint8_t* sc;
+};
+
 // Workspace pieces of the router backward.
 struct RouterBwdScratch {
   float* dl;          // [T,E] fp32 dlogits
-  float* part;        // E <= 32: [splits,E,H] partial dW_r
+  float* part;        // [splits,E,H] partial dW_r (token splits)
   int splits;
   uint16_t* dl_rows;  // E > 32: [3*Tp, Ep] bf16 split of dl (row blocks hi, mid, lo)
   uint16_t* dl_cols;  // E > 32: [T, 6*Ep] bf16 split of dl (column blocks hi, hi, mid, hi, lo, mid)
@@ -33,7 +39,7 @@ struct RouterBwdScratch {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, uint16_t* wsplit, int* err, cudaStream_t st, int nsm);
+                               int32_t* counts, cudaStream_t st, int nsm);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
                               float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,
@@ -63,10 +69,27 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
 cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
                              cudaStream_t st);
 
-cudaError_t launch_router_logits_tc(int T, int H, int E, const uint16_t* X, const uint16_t* Wsplit, float* logits,
-                                   int* err, int nsm, cudaStream_t st);
+cudaError_t launch_fc1_fwd_fp8(const GemmShape& s, const Fp8Op& X1, const Fp8Op& W13, uint16_t* GU, uint16_t* Aact,
+                               int* err, cudaStream_t st);
+cudaError_t launch_fc2_fwd_fp8(const GemmShape& s, const Fp8Op& A1, const Fp8Op& W2, uint16_t* Y, int* err,
+                               cudaStream_t st);
+cudaError_t launch_fc2_dgrad_fp8(const GemmShape& s, const Fp8Op& dY1, const Fp8Op& W2, const uint16_t* GU,
+                                 uint16_t* dGU, int* err, cudaStream_t st);
+cudaError_t launch_fc1_dgrad_fp8(const GemmShape& s, const Fp8Op& dGU1, const Fp8Op& W13, uint16_t* dX1, int* err,
+                                 cudaStream_t st);
+cudaError_t launch_fc2_wgrad_fp8(const GemmShape& s, const Fp8Op& dYc, const Fp8Op& Ac, uint16_t* dW2, int* err,
+                                 cudaStream_t st);
+cudaError_t launch_fc1_wgrad_fp8(const GemmShape& s, const Fp8Op& dGUc, const Fp8Op& Xc, uint16_t* dW13, int* err,
+                                 cudaStream_t st);
+cudaError_t launch_quant_rows(const uint16_t* X, int64_t rows, int K, const int32_t* rows_valid, uint8_t* q,
+                              uint8_t* sc, int nsm, cudaStream_t st);
+cudaError_t launch_quant_cols(const uint16_t* X, int64_t rows, int N, const int32_t* rows_valid, uint8_t* q,
+                              uint8_t* sc, cudaStream_t st);
+cudaError_t launch_quant_weights(const uint16_t* W, int64_t nmat, int rows, int cols, uint8_t* q, uint8_t* sc,
+                                 cudaStream_t st);
+
 cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint16_t* dlsplit, const uint16_t* X,
-                                 float* dWr, int* err, int nsm, cudaStream_t st);
+                                 float* dWr, int splits, int* err, int nsm, cudaStream_t st);
 cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const uint16_t* WB, float* dXr, int* err,
                                 int nsm, cudaStream_t st);
 

@@ -642,28 +642,6 @@ __global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, 
   }
 }
 
-// Routing of tokens whose raw logits X.W_r^T are already in `logits` (written by
-// the tensor-core GEMM): one warp per token adds logit_bias, then scores, selects
-// and gates exactly as the fused kernels do.
-template <int V>
-__global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
-  __shared__ float rows[8][32 * V];
-  __shared__ int hist[32 * V];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 32 * V; i += 256) hist[i] = 0;
-  __syncthreads();
-  const int t = blockIdx.x * 8 + warp;
-  if (t < a.T) {
-    for (int e = lane; e < a.E; e += 32)
-      rows[warp][e] = a.logits[(size_t)t * a.E + e] + (a.logit_bias ? a.logit_bias[e] : 0.f);
-    __syncwarp();
-    route_token<V>(a, t, rows[warp], hist);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < a.E; e += 256)
-    if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
-}
-
 struct Bf16In {
   uint16_t v;
   __device__ __forceinline__ explicit operator float() const { return __uint_as_float((uint32_t)v << 16); }
@@ -673,7 +651,7 @@ struct Bf16In {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, uint16_t* wsplit, int* err, cudaStream_t st, int nsm) {
+                               int32_t* counts, cudaStream_t st, int nsm) {
   RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
               c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
               c.group_score};
@@ -683,22 +661,13 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
   if (c.E <= 8) return launch_small<8, 4>(a, st, nsm);
   if (c.E <= 16) return launch_small<16, 2>(a, st, nsm);
   if (c.E <= 32) return launch_small<32, 1>(a, st, nsm);
-  // E > 32: logits on the tensor cores from the exact three-term split of W_r, then routing
-  {
-    int blocks = (int)(((int64_t)c.E * c.H + 255) / 256);
-    blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
-    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, c.E, wsplit, nullptr);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if ((e = launch_router_logits_tc(c.T, c.H, c.E, X, wsplit, logits, err, nsm, st)) != cudaSuccess) return e;
-  const int grid = (c.T + 7) / 8;
-  if (c.E <= 64)
-    k_route_rows<2><<<grid, 256, 0, st>>>(a);
-  else if (c.E <= 128)
-    k_route_rows<4><<<grid, 256, 0, st>>>(a);
-  else
-    k_route_rows<8><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  // E > 32: FP32 register-tiled GEMM on the CUDA cores.  (The tensor cores' FP32
+  // accumulation drifts by about half an ulp per MMA step, ~5e-5 relative over K=3H
+  // split terms, which the 1e-5 logit bound does not allow; the backward products,
+  // held to bf16-class bounds, do run on the tensor cores.)
+  if (c.E <= 64) return launch_large<64, 4>(a, st);
+  if (c.E <= 128) return launch_large<128, 4>(a, st);
+  return launch_large<256, 4>(a, st);
 }
 
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
@@ -738,8 +707,19 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
     blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
     k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, w.Ep, nullptr, w.wb);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_router_dwr_tc(c.T, w.Tp, c.H, c.E, w.Ep, w.dl_rows, X, dW_r, err, nsm, st)) != cudaSuccess)
+    // dW_r = a reduction over 3*Tp rows into only ceil(E/128)*H/256 output tiles: split
+    // the rows over w.splits partials, then sum them in a fixed order
+    const int splits = w.splits;
+    if ((e = launch_router_dwr_tc(c.T, w.Tp, c.H, c.E, w.Ep, w.dl_rows, X, splits > 1 ? w.part : dW_r, splits, err,
+                                  nsm, st)) != cudaSuccess)
       return e;
+    if (splits > 1) {
+      const int64_t n = (int64_t)c.E * c.H;
+      int blocks = (int)((n + 255) / 256);
+      blocks = blocks < 2048 ? blocks : 2048;
+      k_reduce_splits<<<blocks, 256, 0, st>>>(w.part, splits, n, dW_r);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     return launch_router_dx_tc(c.T, c.H, w.Ep, w.dl_cols, w.wb, dX_router, err, nsm, st);
   }
   // small E: dW_r over token splits (fixed-order reduction), dX_r = dl W_r with K = E

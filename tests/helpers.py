@@ -63,4 +63,4 @@ def make_layer(w: S.Workload, inp: dict, device="cuda"):
         W_r=to_dev(inp["W_r"]), W13=to_dev(inp["W13"]), W2=to_dev(inp["W2"]),
         logit_bias=to_dev(inp.get("logit_bias")), sel_bias=to_dev(inp.get("sel_bias")),
         W13_s=to_dev(inp.get("W13_s")), W2_s=to_dev(inp.get("W2_s")))
-    return M.MoELayer(cfg, weights, device=device)
+    return M.MoELayer(cfg, weights, device=device, fp8=getattr(w, "fp8", False))

@@ -200,3 +200,102 @@ def test_empty_tokens():
     assert layer.device_error() == 0
     assert (layer.offsets.cpu() == 0).all()
     assert (layer.dW13.float().abs().sum() == 0).item() and (layer.dW2.float().abs().sum() == 0).item()
+
+
+# ---------------------------------------------------------------- FP8 E4M3 expert GEMMs
+
+TOL_FP8 = 6e-2
+
+FP8_CASES = {
+    "ragged-fp8": S.Workload("ragged-fp8", T=1000, H=256, E=8, k=2, F=384, fp8=True),
+    "dsv3-mini-fp8": S.Workload("dsv3-mini-fp8", T=520, H=256, E=64, k=6, F=256, F_shared=256, score_fn=1,
+                                gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True, fp8=True),
+}
+
+
+@pytest.mark.parametrize("name", list(FP8_CASES))
+def test_layer_parity_fp8(name):
+    w = FP8_CASES[name]
+    inp = S.host_inputs(w)
+    layer = run_layer(w, inp)
+    c = O.cfg(w, mirror=True)
+    logits, idx, g, d = check_routing(w, inp, layer, c)
+    inp8 = O.fp8_inputs(inp)
+    tk = O.tokens(c, inp8, idx, logits, g)
+    assert slice_rel_err(host_f64(layer.Y), tk["Y"]) < TOL_FP8
+    assert slice_rel_err(layer.dgates.cpu().numpy(), tk["dgates"]) < TOL_FP8
+    assert slice_rel_err(host_f64(layer.dX), tk["dX"]) < TOL_FP8
+    for e in range(w.E):
+        dW13, dW2 = O.expert_wgrad(c, inp8, idx, g, e)
+        assert slice_rel_err(host_f64(layer.dW13[e]), dW13, 2) < TOL_FP8, e
+        assert slice_rel_err(host_f64(layer.dW2[e]), dW2, 2) < TOL_FP8, e
+    if w.F_shared:
+        dW13s, dW2s = O.expert_wgrad(c, inp8, idx, g, -1)
+        assert slice_rel_err(host_f64(layer.dW13_s), dW13s, 2) < TOL_FP8
+        assert slice_rel_err(host_f64(layer.dW2_s), dW2s, 2) < TOL_FP8
+
+
+def _pow2_scale(amax):
+    """Smallest power of two s with 448*s >= amax (1 where amax == 0), float64 tensor."""
+    a = amax.double()
+    e = torch.ceil(torch.log2(torch.where(a > 0, a, torch.ones_like(a)) / 448.0))
+    e = e - ((448.0 * torch.pow(2.0, e - 1) >= a) & (a > 0)).double()
+    e = e + (448.0 * torch.pow(2.0, e) < a).double()
+    return torch.where(a > 0, torch.pow(2.0, e), torch.ones_like(a))
+
+
+def _q(x, s):
+    return (x.double() / s).float().to(torch.float8_e4m3fn).double() * s
+
+
+def _qrows(x):  # [R, K]: 1x128 blocks along K
+    R, K = x.shape
+    xb = x.double().view(R, K // 128, 128)
+    s = _pow2_scale(xb.abs().amax(-1, keepdim=True))
+    return _q(xb, s).view(R, K)
+
+
+def _qcols(x):  # [R, N]: 128x1 blocks along R (R a multiple of 128 here)
+    return _qrows(x.t().contiguous()).t()
+
+
+def _qw(W):  # [E, N, K]: 128x128 blocks
+    E, N, K = W.shape
+    wb = W.double().view(E, N // 128, 128, K // 128, 128)
+    s = _pow2_scale(wb.abs().amax(dim=(2, 4), keepdim=True))
+    return _q(wb, s).view(E, N, K)
+
+
+def test_fp8_gemm_modes_match_torch():
+    """The six FP8 GEMMs against double-precision matmuls of the same E4M3 operands
+    (quantized here with torch's float8_e4m3fn cast and power-of-two block scales)."""
+    w = FP8_CASES["ragged-fp8"]
+    inp = S.host_inputs(w)
+    L = run_layer(w, inp)
+    F = w.F
+    off, cnt = L.offsets.cpu().numpy(), L.counts.cpu().numpy()
+    W13q, W2q = _qw(L.w.W13), _qw(L.w.W2)
+    errs = {}
+    for e in range(w.E):
+        r0, r1 = int(off[e]), int(off[e]) + int(cnt[e])
+        seg = slice(int(off[e]), int(off[e + 1]))  # the whole 128-aligned segment
+        if r1 == r0:
+            continue
+        xq = _qrows(L.Xperm[r0:r1])
+        gu = xq @ W13q[e].t()
+        errs[f"fc1_fwd[{e}]"] = slice_rel_err(host_f64(L.GU[r0:r1]), gu.cpu().numpy())
+        yq = _qrows(L.A[r0:r1]) @ W2q[e].t()
+        errs[f"fc2_fwd[{e}]"] = slice_rel_err(host_f64(L.Yperm[r0:r1]), yq.cpu().numpy())
+        dA = _qrows(L.dYperm[r0:r1]) @ W2q[e]
+        g, u = L.GU[r0:r1, :F].double(), L.GU[r0:r1, F:].double()
+        sg = torch.sigmoid(g)
+        dgu = torch.cat([dA * u * sg * (1 + g * (1 - sg)), dA * g * sg], 1)
+        errs[f"fc2_dgrad[{e}]"] = slice_rel_err(host_f64(L.dGU[r0:r1]), dgu.cpu().numpy())
+        dx = _qrows(L.dGU[r0:r1]) @ W13q[e]
+        errs[f"fc1_dgrad[{e}]"] = slice_rel_err(host_f64(L.dXperm[r0:r1]), dx.cpu().numpy())
+        dW2 = _qcols(L.dYperm[seg]).t() @ _qcols(L.A[seg])
+        errs[f"fc2_wgrad[{e}]"] = slice_rel_err(host_f64(L.dW2[e]), dW2.cpu().numpy(), 2)
+        dW13 = _qcols(L.dGU[seg]).t() @ _qcols(L.Xperm[seg])
+        errs[f"fc1_wgrad[{e}]"] = slice_rel_err(host_f64(L.dW13[e]), dW13.cpu().numpy(), 2)
+    bad = {k: v for k, v in errs.items() if not v < 1e-2}
+    assert not bad, bad
