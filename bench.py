@@ -50,6 +50,19 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity on one process).
+
+    The benchmark reports the slowest rank's time: every rank runs its own replica of
+    the layer on its own GPU, and the job is done when the last one finishes."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 # ---------------------------------------------------------------- inputs
 
 
@@ -227,8 +240,19 @@ def hbm_bytes(w):
     }
 
 
+def kernel_digest(files=("grouped_gemm.cu", "common.cuh")):
+    """Digest of the sources that define the grouped GEMM kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mixture_experts_layer_topk_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel, workload):
-    """DRAM traffic per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    """DRAM bytes per step of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -236,10 +260,7 @@ def traffic_record(kernel, workload):
         with open(p) as fh:
             d = json.load(fh)
         rec = d.get(f"{kernel}:{workload}")
-        if not rec:
-            return None
-        from mixture_experts_layer_topk_gb300 import build as B
-        if rec.get("source_digest") != B._digest():
+        if not rec or rec.get("source_digest") != kernel_digest():
             return None
         return rec.get("bytes_per_step")
     except Exception:
@@ -337,11 +358,7 @@ def bench_ours(args, w):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
-    t_local = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if ws_ > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t_local[0]), float(t_local[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device=dev)
     if rank != 0:
         return None
 

@@ -15,9 +15,14 @@
 // One CTA per SM, 6 warps: warp 0 issues TMA loads into a ring of shared
 // memory stages, warp 1 allocates tensor memory and issues tcgen05.mma from
 // one thread, warps 2-5 drain the double-buffered accumulator (tcgen05.ld),
-// apply the epilogue and store bf16.  Tiles are 128 x BN x 64 (bf16, 128-byte
-// swizzle).  Every wait is bounded; a wait that runs out records
-// MOE_ERR_TIMEOUT in the device error word and the CTA unwinds.
+// apply the epilogue and stage bf16 outputs for TMA bulk stores.  bf16 tiles
+// that are 256 wide run on CTA pairs (a cluster of two): one tcgen05.mma
+// cta_group::2 computes a 256 x 256 x 16 step from both CTAs' shared memory,
+// each CTA holding 128 rows of A and half of B, and each CTA's tensor memory
+// holding its 128 rows of the accumulator.  Narrower bf16 tiles and the FP8
+// tiles (128 x 128 x 128, block-scaled) run one CTA per tile.  Every wait is
+// bounded; a wait that runs out records MOE_ERR_TIMEOUT in the device error
+// word and the CTA unwinds.
 //
 // The three operand layouts:
 //   FWD   D[m,n] = sum_k A[m,k] B[n,k]  A K-major (rows of a permuted buffer), B K-major (weights)
@@ -81,6 +86,7 @@ struct GemmArgs {
 
 struct Tile {
   int e, m0, n0, k0, kb;
+  bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
 };
 
 template <int MODE, int EPI, int BN, int BK>
@@ -114,6 +120,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.n0 = n * (EPI == EPI_SWIGLU ? BN / 2 : BN);
     r.k0 = 0;
     r.kb = g.K / BK;
+    r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
     const int e = t / per, local = t % per;
@@ -131,6 +138,64 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
       r.k0 = s_seg[e];
       r.kb = (s_cnt[e] + BK - 1) / BK;
     }
+    r.valid = true;
+  }
+  return r;
+}
+
+// CTA pairs: tile t is a 256-row pair of M tiles (2*mp and 2*mp+1 of one expert);
+// CTA `rank` owns M tile 2*mp + rank, which may not exist when an expert has an odd
+// number of M tiles (its A rows then point past the tensor and read as zeros).
+template <int MODE, int EPI, int BN, int BK>
+__device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
+                                                 const int* s_ptile, const int* s_cnt, int rank, int64_t oob_row) {
+  Tile r;
+  if constexpr (MODE != MODE_WGRAD) {
+    int e = 0, n, mp, mt;
+    if (g.dense_rows > 0) {
+      mt = (g.dense_rows + BM - 1) / BM;
+      const int pm = (mt + 1) / 2;
+      n = t / pm;
+      mp = t % pm;
+    } else {
+      int lo = 0, hi = g.E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_ptile[mid] * g.n_tiles <= t)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      e = lo;
+      const int local = t - s_ptile[e] * g.n_tiles;
+      const int pm = s_ptile[e + 1] - s_ptile[e];
+      n = local / pm;
+      mp = local % pm;
+      mt = s_tile[e + 1] - s_tile[e];
+    }
+    const int m = 2 * mp + rank;
+    r.valid = m < mt;
+    r.m0 = g.dense_rows > 0 ? m * BM : (r.valid ? s_seg[e] + m * BM : (int)oob_row);
+    r.e = e;
+    r.n0 = n * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+    r.k0 = 0;
+    r.kb = g.K / BK;
+  } else {
+    const int mpairs = (g.m_tiles + 1) / 2;
+    const int per = mpairs * g.n_tiles;
+    const int e = t / per, local = t % per;
+    const int m = 2 * (local % mpairs) + rank;
+    r.e = e;
+    r.valid = m < g.m_tiles;
+    r.m0 = m * BM;  // past M when invalid: the MN-major A box reads zeros
+    r.n0 = (local / mpairs) * BN;
+    if (g.dense_rows > 0) {
+      r.k0 = 0;
+      r.kb = (g.dense_rows + BK - 1) / BK;
+    } else {
+      r.k0 = s_seg[e];
+      r.kb = (s_cnt[e] + BK - 1) / BK;
+    }
   }
   return r;
 }
@@ -141,7 +206,7 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
 }
 
-template <int MODE, int EPI, int BN, int ST, bool FP8>
+template <int MODE, int EPI, int BN, int ST, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapD, const GemmArgs g) {
@@ -149,12 +214,14 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
   constexpr int BK = G::BKE;
   constexpr int kThreads = G::THREADS;
   constexpr int A_BYTES = BM * 128;
-  constexpr int B_BYTES = BN * 128;
+  constexpr int BNL = PAIR ? BN / 2 : BN;  // B rows (N) held by this CTA
+  constexpr int B_BYTES = BNL * 128;
   constexpr int STAGE = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = FP8 ? 512 : 2 * BN;  // FP8: accumulators + per-stage scale columns
   constexpr uint32_t SFC = 2 * BN;                    // first scale-factor column (FP8): 8 per stage
   constexpr uint32_t IDESC = FP8 ? idesc_mxf8(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD)
-                                 : idesc_bf16(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
+                                 : idesc_bf16(PAIR ? 2 * BM : BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
+  static_assert(!(PAIR && FP8), "CTA pairs are built for the bf16 path only");
   constexpr bool TMA_OUT = EPI != EPI_SWIGLU;  // outputs leave through the staging buffer and TMA stores
 
   extern __shared__ uint8_t smem_raw[];
@@ -172,15 +239,32 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
   int* s_seg = reinterpret_cast<int*>(tmem_holder + 4);
   int* s_tile = s_seg + 260;
   int* s_cnt = s_tile + 260;
+  int* s_ptile = s_cnt + 260;  // CTA pairs: prefix of ceil(M tiles / 2) per expert
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
   if (g.dense_rows <= 0) {
     for (int i = threadIdx.x; i <= g.E; i += kThreads) {
       s_seg[i] = g.seg_off[i];
       if (MODE != MODE_WGRAD) s_tile[i] = g.tile_off[i];
       if (MODE == MODE_WGRAD && i < g.E) s_cnt[i] = g.counts[i];
     }
+    if (PAIR && MODE != MODE_WGRAD) {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        s_ptile[0] = 0;
+        for (int e = 0; e < g.E; ++e) s_ptile[e + 1] = s_ptile[e] + (s_tile[e + 1] - s_tile[e] + 1) / 2;
+      }
+    }
   }
+  // rows of the A tensor map: a coordinate at or past it reads zeros
+  const int64_t oob_row = 1LL << 30;
+  auto decode = [&](int t) {
+    if constexpr (PAIR)
+      return decode_pair_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_ptile, s_cnt, rank, oob_row);
+    else
+      return decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+  };
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
@@ -189,7 +273,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], PAIR ? 8 : 4);  // pairs: both CTAs' epilogue warps release
     }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -198,21 +282,35 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     if (TMA_OUT) tma_prefetch_desc(&mapD);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // one warp of each CTA of the pair allocates together
+      tmem_alloc_pair(tmem_holder, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
   int total;
   if constexpr (MODE != MODE_WGRAD) {
-    const int mt = g.dense_rows > 0 ? (g.dense_rows + BM - 1) / BM : s_tile[g.E];
-    total = mt * g.n_tiles;
+    if constexpr (PAIR) {
+      const int mt = g.dense_rows > 0 ? (g.dense_rows + BM - 1) / BM : 0;
+      total = (g.dense_rows > 0 ? (mt + 1) / 2 : s_ptile[g.E]) * g.n_tiles;
+    } else {
+      const int mt = g.dense_rows > 0 ? (g.dense_rows + BM - 1) / BM : s_tile[g.E];
+      total = mt * g.n_tiles;
+    }
   } else {
-    total = (g.dense_rows > 0 && g.ksplit_rows <= 0 ? 1 : g.E) * g.m_tiles * g.n_tiles;
+    const int mtl = PAIR ? (g.m_tiles + 1) / 2 : g.m_tiles;
+    total = (g.dense_rows > 0 && g.ksplit_rows <= 0 ? 1 : g.E) * mtl * g.n_tiles;
   }
+  const int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -220,8 +318,8 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, used = 0, last_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+      for (int t = t_first; t < total && ok; t += t_step) {
+        const Tile tl = decode(t);
         for (int kb = 0; kb < tl.kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
@@ -231,8 +329,30 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           uint8_t* sa = tiles + stage * STAGE;
           uint8_t* sb = sa + A_BYTES;
           uint64_t* bar = &full[stage];
-          mbar_arrive_expect_tx(bar, STAGE);
           const int kc = kb * BK;
+          if constexpr (PAIR) {
+            // both CTAs' copies land on the leader's barrier, which expects both
+            if (rank == 0) mbar_arrive_expect_tx(bar, 2 * STAGE);
+            const uint32_t cbar = mapa_shared(smem_u32(bar), 0);
+            if constexpr (MODE == MODE_WGRAD) {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * 8192, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
+#pragma unroll
+              for (int j = 0; j < BNL / 64; ++j)
+                tma_load_2d_pair(sb + j * 8192, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, tl.k0 + kc);
+            } else {
+              tma_load_2d_pair(sa, &mapA, cbar, kc, tl.m0);
+              if constexpr (MODE == MODE_FWD) {
+                const int brow = EPI == EPI_SWIGLU ? (rank ? g.F + tl.n0 : tl.n0) : tl.n0 + rank * BNL;
+                tma_load_3d_pair(sb, &mapB, cbar, kc, brow, tl.e);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BNL / 64; ++j)
+                  tma_load_3d_pair(sb + j * 8192, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, kc, tl.e);
+              }
+            }
+          } else {
+          mbar_arrive_expect_tx(bar, STAGE);
           if constexpr (MODE == MODE_WGRAD) {
 #pragma unroll
             for (int j = 0; j < BM / G::MN_INNER; ++j)
@@ -256,6 +376,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
                 tma_load_3d(sb + j * G::MN_BOX, &mapB, bar, tl.n0 + G::MN_INNER * j, kc, tl.e);
             }
           }
+          }
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == ST) {
@@ -264,19 +385,22 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           }
         }
       }
-      // nothing may still be landing in shared memory when the CTA exits
-      for (int s = 0; s < ST; ++s)
-        if (used >> s & 1)
-          if (!mbar_wait(&full[s], last_par >> s & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
+      // nothing may still be landing in shared memory when the CTA exits (for pairs the
+      // leader's barriers count both CTAs' copies, and the closing cluster barrier
+      // keeps the peer alive until the leader has seen them land)
+      if (!PAIR || rank == 0)
+        for (int s = 0; s < ST; ++s)
+          if (used >> s & 1)
+            if (!mbar_wait(&full[s], last_par >> s & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (the leader CTA of a pair)
+    if (lane == 0 && (!PAIR || rank == 0)) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+      for (int t = t_first; t < total && ok; t += t_step) {
+        const Tile tl = decode(t);
         if (tl.kb == 0) continue;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
           set_device_error(g.err, MOE_ERR_TIMEOUT, 3);
@@ -302,24 +426,35 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
                                                    : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = MODE == MODE_FWD ? smem_desc_sw128(sb + kk * 32, 16, 1024)
                                                  : smem_desc_sw128(sb + kk * MN_STEP, G::MN_BOX, 1024);
-            if constexpr (FP8)
+            if constexpr (PAIR)
+              umma_f16_pair(d, ad, bd, IDESC, (kb | kk) != 0);
+            else if constexpr (FP8)
               umma_mxf8(d, ad, bd, IDESC, tmem + SFC + 8 * stage, tmem + SFC + 8 * stage + 4, (kb | kk) != 0);
             else
               umma_f16(d, ad, bd, IDESC, (kb | kk) != 0);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR)
+            umma_commit_pair(&empty[stage]);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == ST) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&acc_full[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair(&acc_full[acc]);
+        else
+          umma_commit(&acc_full[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       // every issued MMA has finished before tensor memory is released
-      umma_commit(done_bar);
+      if constexpr (PAIR)
+        umma_commit_pair(done_bar);
+      else
+        umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) set_device_error(g.err, MOE_ERR_TIMEOUT, 5);
     }
   } else if (warp < 6) {
@@ -347,11 +482,12 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         *reinterpret_cast<float4*>(base + ((j ^ (r & 7)) << 4)) =
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     };
-    // Hands staged boxes to TMA: all threads fence + barrier, the leader stores.
-    auto publish = [&](int nbox, const int* hx, const int* xs, int y, int z) {
+    // Hands staged boxes to TMA: all threads fence + barrier, the leader stores
+    // (nothing is stored for the missing half of a CTA pair's tile).
+    auto publish = [&](int nbox, const int* hx, const int* xs, int y, int z, bool store) {
       fence_proxy_async_smem();
       named_bar_sync(kEpiBarrier, 128);
-      if (leader) {
+      if (leader && store) {
         for (int b = 0; b < nbox; ++b) tma_store_3d(&mapD, staging + hx[b] * 8192, xs[b], y, z);
         bulk_commit_group();
       }
@@ -366,12 +502,24 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
       }
       named_bar_sync(kEpiBarrier, 128);
     };
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+    // The accumulator goes back to the MMA issuer: the leader CTA's barrier, which
+    // in a pair also counts the peer's epilogue warps.
+    auto release = [&](int b) {
+      if constexpr (PAIR) {
+        if (rank == 0)
+          mbar_arrive(&acc_empty[b]);
+        else
+          mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
+      } else {
+        mbar_arrive(&acc_empty[b]);
+      }
+    };
+    for (int t = t_first; t < total; t += t_step) {
+      const Tile tl = decode(t);
       const int64_t row = tl.m0 + r;
       if constexpr (EPI == EPI_DSWIGLU) {
         // pull this row's saved pre-activations into L2 while the accumulator fills
-        if (g.dense_rows <= 0 || row < g.dense_rows) {
+        if (tl.valid && (g.dense_rows <= 0 || row < g.dense_rows)) {
           const uint16_t* gp = g.GU + row * g.ldgu + tl.n0;
 #pragma unroll
           for (int i = 0; i < BN * 2; i += 128) {
@@ -390,12 +538,12 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
             reserve(true);
             stage_row_f32(z);
             const int hx[1] = {0}, xs[1] = {tl.n0 + 32 * c};
-            publish(1, hx, xs, tl.m0, tl.e);
+            publish(1, hx, xs, tl.m0, tl.e, tl.valid);
           } else {
             reserve(false);
             stage_row(half, z);
             const int hx[1] = {half}, xs[1] = {tl.n0 + 32 * c};
-            publish(1, hx, xs, tl.m0, tl.e);
+            publish(1, hx, xs, tl.m0, tl.e, tl.valid);
             half ^= 1;
           }
         }
@@ -414,7 +562,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
       mbar_wait(&acc_full[acc], acc_phase);  // already complete: acquires the accumulator for this thread
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const bool valid = g.dense_rows <= 0 || MODE == MODE_WGRAD || row < g.dense_rows;
+      const bool valid = tl.valid && (g.dense_rows <= 0 || MODE == MODE_WGRAD || row < g.dense_rows);
       if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -439,7 +587,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (lane == 0) release(acc);
       } else if constexpr (EPI == EPI_DSWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -449,7 +597,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           if (c == BN / 32 - 1) {  // the accumulator is no longer needed
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) release(acc);
           }
           const int col = tl.n0 + c * 32;
           float dg[32], du[32];
@@ -478,7 +626,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           stage_row(0, dg);
           stage_row(1, du);
           const int hx[2] = {0, 1}, xs[2] = {col, g.F + col};
-          publish(2, hx, xs, tl.m0, 0);
+          publish(2, hx, xs, tl.m0, 0, tl.valid);
         }
       } else {
         int nch = BN / 32;
@@ -494,7 +642,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           if (c == nch - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) release(acc);
           }
           float v[32];
 #pragma unroll
@@ -508,7 +656,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
             stage_row(half, v);
             half ^= 1;
           }
-          publish(1, hx, xs, tl.m0, MODE == MODE_WGRAD ? tl.e : 0);
+          publish(1, hx, xs, tl.m0, MODE == MODE_WGRAD ? tl.e : 0, tl.valid);
         }
       }
       acc ^= 1;
@@ -518,16 +666,17 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     if (TMA_OUT && leader) bulk_wait_group<0>();
   } else if constexpr (FP8) {
     // ------------------------------------------------------------ scale-factor warps (FP8)
-    // Each warp owns one 32-lane quarter of tensor memory: for every stage it writes the
-    // UE8M0 scale of each of its 32 tile rows of A and of B (the byte repeated 4 times,
-    // so every scale-factor id reads the same value) into the stage's A and B columns.
+    // The block-scaled MMA reads the scales of a 128-row operand as 32 lanes x 4 columns:
+    // row m at lane m % 32, column m / 32, one byte per 32-wide K step (the byte chosen
+    // by the scale-factor id).  Every lane quarter holds the same copy, so each of the four
+    // warps writes it into its own 32 lanes.  Our blocks span 128 of K, so all four bytes
+    // of a word carry the same UE8M0 scale.  A uses columns SFC+8s..+3, B SFC+8s+4..+7.
     const int q = warp & 3;
-    const int r = q * 32 + lane;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE, EPI, BN, BK>(t, g, s_seg, s_tile, s_cnt);
+    for (int t = t_first; t < total && ok; t += t_step) {
+      const Tile tl = decode(t);
       for (int kb = 0; kb < tl.kb; ++kb) {
         const bool w_ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1) : false, 0);
         if (!w_ok) {
@@ -535,25 +684,32 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           ok = false;
           break;
         }
-        uint32_t a = 127, b = 127;
-        if constexpr (MODE == MODE_WGRAD) {
-          const int64_t blk = tl.k0 / 128 + kb;  // 128-row block of the token dimension
-          a = g.sfa[blk * g.sfa_ld + tl.m0 + r];
-          b = g.sfb[blk * g.sfb_ld + tl.n0 + r];
-        } else {
-          const int64_t row = tl.m0 + r;
-          if (g.dense_rows <= 0 || row < g.dense_rows) a = g.sfa[row * g.sfa_ld + kb];
-          if constexpr (MODE == MODE_FWD) {  // weights [E][N rows][K]: block (n/128, kb)
-            const int nrow = EPI == EPI_SWIGLU ? (r < BN / 2 ? tl.n0 + r : g.F + tl.n0 + r - BN / 2) : tl.n0 + r;
-            b = g.sfb[((int64_t)tl.e * g.sfb_r + nrow / 128) * g.sfb_c + kb];
-          } else {  // weights [E][K rows][N]: block (kb, n/128)
-            b = g.sfb[((int64_t)tl.e * g.sfb_r + kb) * g.sfb_c + (tl.n0 + r) / 128];
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;  // tile row of this word
+          uint32_t a = 127, b = 127;
+          if constexpr (MODE == MODE_WGRAD) {
+            const int64_t blk = tl.k0 / 128 + kb;  // 128-row block of the token dimension
+            a = g.sfa[blk * g.sfa_ld + tl.m0 + r];
+            b = g.sfb[blk * g.sfb_ld + tl.n0 + r];
+          } else {
+            const int64_t row = tl.m0 + r;
+            if (g.dense_rows <= 0 || row < g.dense_rows) a = g.sfa[row * g.sfa_ld + kb];
+            if constexpr (MODE == MODE_FWD) {  // weights [E][N rows][K]: block (n/128, kb)
+              const int nrow =
+                  EPI == EPI_SWIGLU ? (r < BN / 2 ? tl.n0 + r : g.F + tl.n0 + r - BN / 2) : tl.n0 + r;
+              b = g.sfb[((int64_t)tl.e * g.sfb_r + nrow / 128) * g.sfb_c + kb];
+            } else {  // weights [E][K rows][N]: block (kb, n/128)
+              b = g.sfb[((int64_t)tl.e * g.sfb_r + kb) * g.sfb_c + (tl.n0 + r) / 128];
+            }
           }
+          wa[j] = a * 0x01010101u;
+          wb[j] = b * 0x01010101u;
         }
-        // scale-factor columns start on 4-column (128-bit) boundaries: A at SFC + 8*stage, B 4 after
         const uint32_t sf_addr = tmem + ((uint32_t)(q * 32) << 16) + SFC + 8 * stage;
-        tmem_st1(sf_addr, a * 0x01010101u);
-        tmem_st1(sf_addr + 4, b * 0x01010101u);
+        tmem_st4(sf_addr, wa[0], wa[1], wa[2], wa[3]);
+        tmem_st4(sf_addr + 4, wb[0], wb[1], wb[2], wb[3]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -568,18 +724,23 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-template <int MODE, int EPI, int BN, bool FP8>
+template <int MODE, int EPI, int BN, bool FP8, bool PAIR = false>
 struct Kern {
-  static constexpr int ST = BN == 256 ? 4 : 6;
-  static constexpr int STAGE = (BM + BN) * 128;
-  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (3 * ST + 5) * 8 + 16 + 3 * 260 * 4;
+  static constexpr int BNL = PAIR ? BN / 2 : BN;
+  static constexpr int STAGE = (BM + BNL) * 128;
+  static constexpr int ST = STAGE <= 32768 ? 6 : 4;
+  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (3 * ST + 5) * 8 + 16 + 4 * 260 * 4;
 };
 
 // ---------------------------------------------------------------- host side
@@ -648,24 +809,52 @@ bool map_out_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid,
   return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
-template <int MODE, int EPI, int BN, bool FP8 = false>
+template <int MODE, int EPI, int BN, bool FP8 = false, bool PAIR = false>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const GemmArgs& g, int max_tiles,
                    int nsm, cudaStream_t st) {
-  using K = Kern<MODE, EPI, BN, FP8>;
+  using K = Kern<MODE, EPI, BN, FP8, PAIR>;
   static bool attr = false;
-  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8>;
+  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8, PAIR>;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   if (max_tiles <= 0) return cudaSuccess;
-  const int grid = max_tiles < nsm ? max_tiles : nsm;
-  kern<<<grid, Geo<FP8>::THREADS, K::smem, st>>>(a, b, d, g);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    // max_tiles counts 256-row pair tiles here; two CTAs (one cluster) per pair tile
+    const int pairs = max_tiles < nsm / 2 ? max_tiles : nsm / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(Geo<FP8>::THREADS);
+    cfg.dynamicSmemBytes = K::smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, b, d, g);
+  } else {
+    const int grid = max_tiles < nsm ? max_tiles : nsm;
+    kern<<<grid, Geo<FP8>::THREADS, K::smem, st>>>(a, b, d, g);
+    return cudaGetLastError();
+  }
 }
 
 inline int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
+
+// 256-wide bf16 tiles run on CTA pairs (cta_group::2): each CTA stages only half of
+// B, halving its shared-memory operand traffic per MMA.
+constexpr bool use_pairs() { return true; }
+
+// pair tiles of a ragged launch: sum over experts of ceil(m tiles / 2) <= max_mtiles / 2 + E
+inline int pair_tiles(const GemmShape& s, int n_tiles) {
+  const int mt = s.dense_rows > 0 ? (s.dense_rows + 127) / 128 : s.max_mtiles;
+  return (s.dense_rows > 0 ? (mt + 1) / 2 : mt / 2 + s.E) * n_tiles;
+}
 
 }  // namespace
 
@@ -679,6 +868,7 @@ cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = GU; g.ldd = 2 * (int64_t)s.F; g.D2 = Aact; g.ldd2 = s.F; g.F = s.F; g.err = err;
+  if (use_pairs()) return launch<MODE_FWD, EPI_SWIGLU, 256, false, true>(ma, mb, ma, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, ma, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
 
@@ -686,14 +876,16 @@ cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_
 cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
                            cudaStream_t st) {
   const int bn = pick_bn(s.H);
+  const bool pairs = bn == 256 && use_pairs();
   CUtensorMap ma, mb, md;
-  if (!map2d(&ma, Aact, s.F, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, bn) ||
+  if (!map2d(&ma, Aact, s.F, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, pairs ? bn / 2 : bn) ||
       !map_out(&md, Y, s.H, s.rows, 1))
     return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.K = s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = Y; g.ldd = s.H; g.err = err;
+  if (pairs) return launch<MODE_FWD, EPI_STORE, 256, false, true>(ma, mb, md, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return bn == 256 ? launch<MODE_FWD, EPI_STORE, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
                    : launch<MODE_FWD, EPI_STORE, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
@@ -710,6 +902,8 @@ cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dGU; g.ldd = 2 * (int64_t)s.F; g.GU = GU; g.ldgu = 2 * (int64_t)s.F; g.F = s.F; g.err = err;
+  if (bn == 256 && use_pairs())
+    return launch<MODE_DGRAD, EPI_DSWIGLU, 256, false, true>(ma, mb, md, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return bn == 256 ? launch<MODE_DGRAD, EPI_DSWIGLU, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
                    : launch<MODE_DGRAD, EPI_DSWIGLU, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
@@ -726,6 +920,8 @@ cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint
   g.E = s.E; g.K = 2 * s.F; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dX1; g.ldd = s.H; g.err = err;
+  if (bn == 256 && use_pairs())
+    return launch<MODE_DGRAD, EPI_STORE, 256, false, true>(ma, mb, md, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return bn == 256 ? launch<MODE_DGRAD, EPI_STORE, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)
                    : launch<MODE_DGRAD, EPI_STORE, 128>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
@@ -743,6 +939,9 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  if (bn == 256 && use_pairs())
+    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(
+        ma, mb, md, g, (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles, s.nsm, st);
   return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
                    : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }
@@ -760,6 +959,9 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
+  if (bn == 256 && use_pairs())
+    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(
+        ma, mb, md, g, (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles, s.nsm, st);
   return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
                    : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }

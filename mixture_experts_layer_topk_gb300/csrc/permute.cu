@@ -86,21 +86,27 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
   }
 }
 
-// Chunk CTAs (blockIdx < nch): rank assignments and write the maps.
-// Padding CTAs (blockIdx >= nch): zero expert (blockIdx - nch)'s padding rows.
+// Chunk CTAs (blockIdx < nch): rank assignments and write the maps.  The chunk's
+// assignments (token-major) are split into 8 contiguous runs, one per warp; a
+// per-warp histogram and a scan over the warps give each run its starting slot per
+// expert, then each warp ranks its run with match_any, so token order is kept.
+// Padding CTAs (blockIdx >= nch): kPadSplit CTAs per expert zero its padding rows.
+constexpr int kPadSplit = 8;
 __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx,
                                                  const int32_t* __restrict__ chunk_base,
                                                  const int32_t* __restrict__ counts,
                                                  const int32_t* __restrict__ offsets, int T, int H, int E, int k,
                                                  int nch, int32_t* __restrict__ row_id_map,
                                                  int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm) {
-  __shared__ int cursor[256];
-  __shared__ int slot_of[kChunk * 32];
+  __shared__ int cursor[8][256];
   const int nvec = H / 8;
   if ((int)blockIdx.x >= nch) {
-    const int e = blockIdx.x - nch;
-    const int r1 = offsets[e + 1];
-    const int r0 = min(max(offsets[e] + counts[e], offsets[e]), r1);
+    const int p = blockIdx.x - nch;
+    const int e = p / kPadSplit, part = p % kPadSplit;
+    const int r1e = offsets[e + 1];
+    const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
+    const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
+    const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
     for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
@@ -110,34 +116,46 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
   const int c = blockIdx.x;
   const int t0 = c * kChunk, t1 = min(T, t0 + kChunk);
   const int n_items = (t1 - t0) * k;
-  for (int e = threadIdx.x; e < E; e += 256) cursor[e] = chunk_base[(size_t)c * E + e];
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0) {
-    const unsigned lt = (1u << lane) - 1u;
-    for (int b = 0; b < n_items; b += 32) {
-      const int i = b + lane;
-      int e = i < n_items ? topk_idx[(size_t)t0 * k + i] : -1 - lane;
-      const bool ok = i < n_items && (unsigned)e < (unsigned)E;
-      if (i < n_items && !ok) {
-        row_id_map[(size_t)t0 * k + i] = -1;  // an id outside [0,E): no slot
-        slot_of[i] = -1;
-        e = -1 - lane;
-      }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & lt);
-      int base = 0;
-      if (ok) base = cursor[e];
-      __syncwarp();
-      if (ok) {
-        const int slot = base + rank;
-        slot_of[i] = slot;
-        row_id_map[(size_t)t0 * k + i] = slot;
-        slot_src[slot] = t0 * k + i;
-        if (rank == 0) cursor[e] = base + __popc(peers);
-      }
-      __syncwarp();
+  const int run = (n_items + 7) / 8;
+  const int i0 = warp * run, i1 = min(n_items, i0 + run);
+  for (int i = threadIdx.x; i < 8 * 256; i += 256) (&cursor[0][0])[i] = 0;
+  __syncthreads();
+  for (int i = i0 + lane; i < i1; i += 32) {
+    const int e = topk_idx[(size_t)t0 * k + i];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cursor[warp][e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 256) {
+    int base = chunk_base[(size_t)c * E + e];
+    for (int w = 0; w < 8; ++w) {
+      const int n = cursor[w][e];
+      cursor[w][e] = base;
+      base += n;
     }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    int e = i < i1 ? topk_idx[(size_t)t0 * k + i] : -1 - lane;
+    const bool ok = i < i1 && (unsigned)e < (unsigned)E;
+    if (i < i1 && !ok) {
+      row_id_map[(size_t)t0 * k + i] = -1;  // an id outside [0,E): no slot
+      e = -1 - lane;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    int base = 0;
+    if (ok) base = cursor[warp][e];
+    __syncwarp();
+    if (ok) {
+      const int slot = base + rank;
+      row_id_map[(size_t)t0 * k + i] = slot;
+      slot_src[slot] = t0 * k + i;
+      if (rank == 0) cursor[warp][e] = base + __popc(peers);
+    }
+    __syncwarp();
   }
 }
 
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ Yp
 }
 
 // dYperm[slot] = bf16(g dY[t]); dgates[t,j] = <dY[t], Yperm[slot]>.
-// CTAs past the token range zero the padding rows of one expert each.
+// CTAs past the token range zero the padding rows, kPadSplit CTAs per expert.
 __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict__ dY,
                                                      const uint16_t* __restrict__ Yperm,
                                                      const int32_t* __restrict__ row_id_map,
@@ -206,9 +224,12 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict_
                                                      float* __restrict__ dgates, int T, int H, int k, int tok_blocks) {
   const int nvec = H / 8;
   if ((int)blockIdx.x >= tok_blocks) {
-    const int e = blockIdx.x - tok_blocks;
-    const int r1 = offsets[e + 1];
-    const int r0 = min(max(offsets[e] + counts[e], offsets[e]), r1);
+    const int p = blockIdx.x - tok_blocks;
+    const int e = p / kPadSplit, part = p % kPadSplit;
+    const int r1e = offsets[e + 1];
+    const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
+    const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
+    const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
       reinterpret_cast<uint4*>(dYperm)[i] = z;
@@ -295,8 +316,8 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   }
   k_scan<<<1, 1024, 0, st>>>(counts, chunk_counts, nch, c.E, c.align, offsets, tile_offsets, chunk_base, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_scatter<<<nch + c.E, 256, 0, st>>>(X, topk_idx, chunk_base, counts, offsets, c.T, c.H, c.E, c.k, nch,
-                                       row_id_map, slot_src, Xperm);
+  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(X, topk_idx, chunk_base, counts, offsets, c.T, c.H, c.E, c.k,
+                                                   nch, row_id_map, slot_src, Xperm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (c.T > 0) {
     const int64_t vec = (int64_t)c.T * (c.H / 8);
@@ -319,7 +340,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const uint16_t* dY, const ui
                                const int32_t* row_id_map, const float* gates, const int32_t* offsets,
                                const int32_t* counts, uint16_t* dYperm, float* dgates, cudaStream_t st) {
   const int tb = (c.T + 7) / 8;
-  k_combine_bwd<<<tb + c.E, 256, 0, st>>>(dY, Yperm, row_id_map, gates, offsets, counts, dYperm, dgates, c.T, c.H,
+  k_combine_bwd<<<tb + c.E * kPadSplit, 256, 0, st>>>(dY, Yperm, row_id_map, gates, offsets, counts, dYperm, dgates, c.T, c.H,
                                            c.k, tb);
   return cudaGetLastError();
 }

@@ -292,32 +292,58 @@ __global__ void __launch_bounds__(256) k_router_large(RouteArgs a) {
   for (int m = 0; m < TM; ++m)
 #pragma unroll
     for (int n = 0; n < 8; ++n) acc[m][n] = 0.f;
-  for (int k0 = 0; k0 < H; k0 += C::BK) {
-    // X tile: BT rows x 16 columns of bf16 = 2 vectors of 8 per row
-    for (int i = tid; i < C::BT * 2; i += 256) {
+  // Global loads of the next K tile are issued into registers before the current
+  // tile is consumed from shared memory (one tile of lookahead).
+  constexpr int XV = (C::BT * 2 + 255) / 256;   // 16-byte X vectors per thread
+  constexpr int WV = (EP * 4 + 255) / 256;      // float4 W vectors per thread
+  uint4 xr[XV];
+  float4 wr[WV];
+  auto load_tile = [&](int k0) {
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + 256 * v;
       const int tt = i >> 1, half = i & 1;
-      float x[8];
-      if (t0 + tt < a.T) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + tt) * H + k0) + half);
-        unpack8(v, x);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) Xs[(half * 8 + q) * C::BT + tt] = x[q];
+      xr[v] = make_uint4(0, 0, 0, 0);
+      if (i < C::BT * 2 && t0 + tt < a.T)
+        xr[v] = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + tt) * H + k0) + half);
     }
-    // W tile: EP rows x 16 fp32 columns = 4 float4 per row
-    for (int i = tid; i < EP * 4; i += 256) {
+#pragma unroll
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + 256 * v;
       const int e = i % EP, q4 = i / EP;
-      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) w = __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)e * H + k0) + q4);
-      Ws[(4 * q4 + 0) * EP + e] = w.x;
-      Ws[(4 * q4 + 1) * EP + e] = w.y;
-      Ws[(4 * q4 + 2) * EP + e] = w.z;
-      Ws[(4 * q4 + 3) * EP + e] = w.w;
+      wr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < EP * 4 && e < E) wr[v] = __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)e * H + k0) + q4);
     }
+  };
+  auto store_tile = [&]() {
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + 256 * v;
+      if (i < C::BT * 2) {
+        const int tt = i >> 1, half = i & 1;
+        float x[8];
+        unpack8(xr[v], x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) Xs[(half * 8 + q) * C::BT + tt] = x[q];
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + 256 * v;
+      if (i < EP * 4) {
+        const int e = i % EP, q4 = i / EP;
+        Ws[(4 * q4 + 0) * EP + e] = wr[v].x;
+        Ws[(4 * q4 + 1) * EP + e] = wr[v].y;
+        Ws[(4 * q4 + 2) * EP + e] = wr[v].z;
+        Ws[(4 * q4 + 3) * EP + e] = wr[v].w;
+      }
+    }
+  };
+  load_tile(0);
+  for (int k0 = 0; k0 < H; k0 += C::BK) {
+    store_tile();
     __syncthreads();
+    if (k0 + C::BK < H) load_tile(k0 + C::BK);
 #pragma unroll
     for (int kk = 0; kk < C::BK; ++kk) {
       float xa[TM];
