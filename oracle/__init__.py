@@ -50,6 +50,7 @@ def _load():
         if _lib is None:
             _lib = ctypes.CDLL(build())
             _lib.ora_dispatch.restype = ctypes.c_int
+            _lib.ora_dispatch_capacity.restype = ctypes.c_int
     return _lib
 
 
@@ -104,8 +105,11 @@ def gates(c: OraCfg, logits, topk_idx):
     return g
 
 
-def dispatch(c: OraCfg, topk_idx, R: int | None = None):
-    """counts [E], offsets [E+1], tile_offsets [E+1], row_id_map [T,k], slot_src [R]."""
+def dispatch(c: OraCfg, topk_idx, R: int | None = None, capacity: int | None = None):
+    """counts [E], offsets [E+1], tile_offsets [E+1], row_id_map [T,k], slot_src [R].
+
+    capacity: keep only each expert's first `capacity` assignments in token order
+    (dropped ones get row_id_map -1; counts are then the kept counts)."""
     if R is None:
         R = c.T * c.k + c.E * (c.align - 1)
     counts = np.empty(c.E, np.int32)
@@ -113,15 +117,20 @@ def dispatch(c: OraCfg, topk_idx, R: int | None = None):
     tiles = np.empty(c.E + 1, np.int32)
     rim = np.empty((c.T, c.k), np.int32)
     src = np.full(R, -2, np.int32)
-    rc = _load().ora_dispatch(ctypes.byref(c), _p(np.ascontiguousarray(topk_idx, np.int32)), _p(counts),
-                              _p(offsets), _p(tiles), _p(rim), _p(src), ctypes.c_int64(R))
+    cap = 2 ** 31 - 1 if capacity is None else int(capacity)
+    rc = _load().ora_dispatch_capacity(ctypes.byref(c), _p(np.ascontiguousarray(topk_idx, np.int32)),
+                                       ctypes.c_int32(cap), _p(counts), _p(offsets), _p(tiles), _p(rim), _p(src),
+                                       ctypes.c_int64(R))
     if rc != 0:
         raise ValueError("permuted rows exceed R")
     return dict(counts=counts, offsets=offsets, tile_offsets=tiles, row_id_map=rim, slot_src=src)
 
 
-def tokens(c: OraCfg, inp: dict, topk_idx, logits, gates_, tok_list=None, want_bwd=True):
-    """Per-token forward/backward: Y [n,H], dX [n,H], dgates [n,k], dlogits [n,E] (float64)."""
+def tokens(c: OraCfg, inp: dict, topk_idx, logits, gates_, tok_list=None, want_bwd=True, kept=None):
+    """Per-token forward/backward: Y [n,H], dX [n,H], dgates [n,k], dlogits [n,E] (float64).
+
+    kept: optional [T,k] mask; an assignment with kept == 0 (dropped by capacity)
+    adds nothing to Y and gets no gradient."""
     if tok_list is None:
         tok_list = np.arange(c.T, dtype=np.int64)
     tok_list = np.ascontiguousarray(tok_list, np.int64)
@@ -130,26 +139,29 @@ def tokens(c: OraCfg, inp: dict, topk_idx, logits, gates_, tok_list=None, want_b
     dX = np.empty((n, c.H), np.float64) if want_bwd else None
     dg = np.empty((n, c.k), np.float64) if want_bwd else None
     dl = np.empty((n, c.E), np.float64) if want_bwd else None
-    _load().ora_tokens(ctypes.byref(c), _p(_u16(inp["X"])), _p(_u16(inp["W13"])), _p(_u16(inp["W2"])),
+    kp = None if kept is None else np.ascontiguousarray(kept, np.int32)
+    _load().ora_tokens_kept(ctypes.byref(c), _p(_u16(inp["X"])), _p(_u16(inp["W13"])), _p(_u16(inp["W2"])),
                        _p(_u16(inp.get("W13_s"))), _p(_u16(inp.get("W2_s"))), _p(_f32(inp["W_r"])),
                        _p(np.ascontiguousarray(topk_idx, np.int32)),
                        _p(np.ascontiguousarray(logits, np.float64)),
                        _p(np.ascontiguousarray(gates_, np.float64)),
                        _p(_u16(inp["dY"])) if want_bwd else None, ctypes.c_int64(n), _p(tok_list),
-                       _p(Y), _p(dX), _p(dg), _p(dl))
+                       _p(Y), _p(dX), _p(dg), _p(dl), _p(kp))
     return dict(Y=Y, dX=dX, dgates=dg, dlogits=dl)
 
 
-def expert_wgrad(c: OraCfg, inp: dict, topk_idx, gates_, expert: int):
-    """dW13 [2F,H] and dW2 [H,F] (float64) of one expert; expert=-1 is the shared expert."""
+def expert_wgrad(c: OraCfg, inp: dict, topk_idx, gates_, expert: int, kept=None):
+    """dW13 [2F,H] and dW2 [H,F] (float64) of one expert; expert=-1 is the shared expert.
+    kept: optional [T,k] mask of the assignments that were not dropped."""
     F = c.F_shared if expert < 0 else c.F
     dW13 = np.empty((2 * F, c.H), np.float64)
     dW2 = np.empty((c.H, F), np.float64)
-    _load().ora_expert_wgrad(ctypes.byref(c), _p(_u16(inp["X"])), _p(_u16(inp["W13"])), _p(_u16(inp["W2"])),
-                             _p(_u16(inp.get("W13_s"))), _p(_u16(inp.get("W2_s"))),
-                             _p(np.ascontiguousarray(topk_idx, np.int32)),
-                             _p(np.ascontiguousarray(gates_, np.float64)), _p(_u16(inp["dY"])),
-                             ctypes.c_int32(expert), _p(dW13), _p(dW2))
+    kp = None if kept is None else np.ascontiguousarray(kept, np.int32)
+    _load().ora_expert_wgrad_kept(ctypes.byref(c), _p(_u16(inp["X"])), _p(_u16(inp["W13"])), _p(_u16(inp["W2"])),
+                                  _p(_u16(inp.get("W13_s"))), _p(_u16(inp.get("W2_s"))),
+                                  _p(np.ascontiguousarray(topk_idx, np.int32)),
+                                  _p(np.ascontiguousarray(gates_, np.float64)), _p(_u16(inp["dY"])),
+                                  ctypes.c_int32(expert), _p(dW13), _p(dW2), _p(kp))
     return dW13, dW2
 
 
@@ -204,7 +216,7 @@ def round_bf16(x):
     return out
 
 
-def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int = 0):
+def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int = 0, capacity=None):
     """Whole-layer forward and backward for every token and every expert (small cases).
 
     sel_scores: optional (logits_f32, scores_f32) from another implementation;
@@ -219,12 +231,13 @@ def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int
     else:
         idx = select(c, sel_scores[0], sel_scores[1], inp.get("sel_bias"))
     g = gates(c, logits, idx)
-    d = dispatch(c, idx)
-    tk = tokens(c, inp, idx, logits, g)
+    d = dispatch(c, idx, capacity=capacity)
+    kept = None if capacity is None else (d["row_id_map"] >= 0).astype(np.int32)
+    tk = tokens(c, inp, idx, logits, g, kept=kept)
     dW13 = np.empty((c.E, 2 * c.F, c.H))
     dW2 = np.empty((c.E, c.H, c.F))
     for e in range(c.E):
-        dW13[e], dW2[e] = expert_wgrad(c, inp, idx, g, e)
+        dW13[e], dW2[e] = expert_wgrad(c, inp, idx, g, e, kept=kept)
     dWr, dlb = router_wgrad(c, inp["X"], tk["dlogits"])
     out = dict(logits=logits, scores=scores, topk_idx=idx, gates=g, Y=tk["Y"], dX=tk["dX"],
                dgates=tk["dgates"], dlogits=tk["dlogits"], dW13=dW13, dW2=dW2, dW_r=dWr,

@@ -426,12 +426,25 @@ void ora_gates(const ora_cfg* cp, const double* logits, const int32_t* topk_idx,
 
 // Dispatch maps by a stable counting sort.  slot_src has R entries; entries at
 // or beyond offsets[E] are left untouched.  Padding slots get -1.
+int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, int32_t* counts,
+                          int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src, int64_t R);
+
 int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                  int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src, int64_t R) {
+  return ora_dispatch_capacity(cp, topk_idx, INT32_MAX, counts, offsets, tile_offsets, row_id_map, slot_src, R);
+}
+
+// Capacity-controlled dropping (position policy): expert e keeps its first `capacity`
+// assignments in token order; a dropped assignment gets row_id_map = -1 and no row.
+// counts are the kept counts.
+int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, int32_t* counts,
+                          int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
+                          int64_t R) {
   const ora_cfg c = *cp;
   const int E = c.E, k = c.k;
   for (int e = 0; e < E; ++e) counts[e] = 0;
   for (int64_t i = 0; i < (int64_t)c.T * k; ++i) counts[topk_idx[i]]++;
+  for (int e = 0; e < E; ++e) counts[e] = std::min(counts[e], capacity);
   offsets[0] = 0;
   tile_offsets[0] = 0;
   for (int e = 0; e < E; ++e) {
@@ -444,6 +457,10 @@ int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, in
   for (int t = 0; t < c.T; ++t)
     for (int j = 0; j < k; ++j) {
       const int e = topk_idx[(size_t)t * k + j];
+      if (cursor[e] - offsets[e] >= counts[e]) {  // over capacity: dropped
+        row_id_map[(size_t)t * k + j] = -1;
+        continue;
+      }
       const int32_t slot = cursor[e]++;
       row_id_map[(size_t)t * k + j] = slot;
       slot_src[slot] = t * k + j;
@@ -460,10 +477,27 @@ int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, in
 //   dX[i]     = sum_j d expert / dx + d shared / dx + dlogits W_r           (H)
 // logits are the double router logits of all T tokens; gates the double gates.
 // Any output may be null; dX/dgates/dlogits need dY.
+void ora_tokens_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                     const uint16_t* W13s, const uint16_t* W2s, const float* Wr, const int32_t* topk_idx,
+                     const double* logits, const double* gates, const uint16_t* dY, int64_t ntok,
+                     const int64_t* tok_list, double* Y, double* dX, double* dgates_out, double* dlogits_out,
+                     const int32_t* kept);
+
 void ora_tokens(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
                 const uint16_t* W13s, const uint16_t* W2s, const float* Wr, const int32_t* topk_idx,
                 const double* logits, const double* gates, const uint16_t* dY, int64_t ntok,
                 const int64_t* tok_list, double* Y, double* dX, double* dgates_out, double* dlogits_out) {
+  ora_tokens_kept(cp, X, W13, W2, W13s, W2s, Wr, topk_idx, logits, gates, dY, ntok, tok_list, Y, dX, dgates_out,
+                  dlogits_out, nullptr);
+}
+
+// Same, where kept[t*k+j] == 0 marks an assignment dropped by capacity: it adds
+// nothing to Y and receives no gradient (its dgate is 0).
+void ora_tokens_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                     const uint16_t* W13s, const uint16_t* W2s, const float* Wr, const int32_t* topk_idx,
+                     const double* logits, const double* gates, const uint16_t* dY, int64_t ntok,
+                     const int64_t* tok_list, double* Y, double* dX, double* dgates_out, double* dlogits_out,
+                     const int32_t* kept) {
   const ora_cfg c = *cp;
   const int H = c.H, F = c.F, Fs = c.F_shared, E = c.E, k = c.k;
   const bool bwd = dY && (dX || dgates_out || dlogits_out);
@@ -479,6 +513,7 @@ void ora_tokens(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const
     const int32_t* sel = topk_idx + (size_t)t * k;
     const double* gt = gates + (size_t)t * k;
     for (int j = 0; j < k; ++j) {
+      if (kept && !kept[(size_t)t * k + j]) continue;
       const int e = sel[j];
       const uint16_t* w13 = W13 + (size_t)e * 2 * F * H;
       const uint16_t* w2 = W2 + (size_t)e * H * F;
@@ -522,9 +557,20 @@ void ora_tokens(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const
 
 // Weight gradients of one expert (expert = -1: the shared expert, which sees
 // every token with gate 1).  dW13: [2F,H] (gate rows then up rows), dW2: [H,F].
+void ora_expert_wgrad_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                           const uint16_t* W13s, const uint16_t* W2s, const int32_t* topk_idx, const double* gates,
+                           const uint16_t* dY, int32_t expert, double* dW13, double* dW2, const int32_t* c_kept);
+
 void ora_expert_wgrad(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
                       const uint16_t* W13s, const uint16_t* W2s, const int32_t* topk_idx,
                       const double* gates, const uint16_t* dY, int32_t expert, double* dW13, double* dW2) {
+  ora_expert_wgrad_kept(cp, X, W13, W2, W13s, W2s, topk_idx, gates, dY, expert, dW13, dW2, nullptr);
+}
+
+// Weight gradients counting only kept assignments (c_kept may be null: all kept).
+void ora_expert_wgrad_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                           const uint16_t* W13s, const uint16_t* W2s, const int32_t* topk_idx, const double* gates,
+                           const uint16_t* dY, int32_t expert, double* dW13, double* dW2, const int32_t* c_kept) {
   const ora_cfg c = *cp;
   const int H = c.H, k = c.k;
   const int F = expert < 0 ? c.F_shared : c.F;
@@ -540,7 +586,7 @@ void ora_expert_wgrad(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13,
       continue;
     }
     for (int j = 0; j < k; ++j)
-      if (topk_idx[t * k + j] == expert) {
+      if (topk_idx[t * k + j] == expert && (!c_kept || c_kept[t * k + j])) {
         toks.push_back(t);
         gsel.push_back(gates[t * k + j]);
       }

@@ -551,3 +551,93 @@ def test_fp8_layer_close_to_bf16_layer():
     for key in ["Y", "dX", "dW13", "dW2"]:
         err = np.sqrt(np.mean((a[key] - b[key]) ** 2) / np.mean(a[key] ** 2))
         assert 1e-3 < err < 0.1, (key, err)
+
+
+# ---------------------------------------------------------------- capacity-controlled dropping
+
+
+def test_capacity_dispatch_keeps_first_tokens():
+    rng = np.random.default_rng(21)
+    T, E, k = 200, 8, 2
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=[.4, .2, .1, .1, .05, .05, .05, .05])
+                    for _ in range(T)]).astype(np.int32)
+    w = small(T=T, E=E, k=k)
+    c = O.cfg(w, align=128)
+    full = O.dispatch(c, idx)
+    same = O.dispatch(c, idx, capacity=int(full["counts"].max()))
+    for key in full:
+        assert np.array_equal(full[key], same[key]), key
+    cap = 30
+    d = O.dispatch(c, idx, capacity=cap)
+    assert (d["counts"] == np.minimum(np.bincount(idx.ravel(), minlength=E), cap)).all()
+    rim = d["row_id_map"]
+    for e in range(E):
+        pos = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]  # token order
+        for n, (t, j) in enumerate(pos):
+            if n < cap:
+                assert rim[t, j] == d["offsets"][e] + n
+            else:
+                assert rim[t, j] == -1
+
+
+def test_capacity_identical_experts_sum_kept_gates():
+    w = small(T=60, H=16, E=4, k=2, F=8, score_fn=1, gate_scale=2.0)
+    inp = inputs(w)
+    inp["W13"] = np.repeat(inp["W13"][:1], 4, axis=0)
+    inp["W2"] = np.repeat(inp["W2"][:1], 4, axis=0)
+    out = O.full_layer(w, inp, mirror=False, capacity=20)
+    kept = out["row_id_map"] >= 0
+    assert (~kept).any()
+    mlp = dense_swiglu(f32(inp["X"]), f32(inp["W13"][0]), f32(inp["W2"][0]))
+    want = (out["gates"] * kept).sum(1, keepdims=True) * mlp
+    assert np.allclose(out["Y"], want, rtol=1e-12, atol=1e-14)
+    assert (out["dgates"][~kept] == 0).all()
+
+
+def test_capacity_finite_differences():
+    w = small("fd-cap", T=12, H=8, E=4, k=2, F=6, score_fn=0)
+    rng = np.random.default_rng(5)
+    inp = inputs(w)
+    probes = [tuple(rng.integers(0, s) for s in inp["W_r"].shape) for _ in range(6)]
+    probes += [("X",) + tuple(rng.integers(0, s) for s in inp["X"].shape) for _ in range(4)]
+    for p in probes:
+        if p[0] == "X":
+            inp["X"][p[1:]] = 0
+        else:
+            inp["W_r"][p] = 0
+    cap = 4
+    out = O.full_layer(w, inp, mirror=False, capacity=cap)
+    assert (out["row_id_map"] < 0).any()
+    c = O.cfg(w, mirror=False)
+
+    def loss(i2):
+        lg, sc = O.router(c, i2["X"], i2["W_r"])
+        idx = O.select(c, lg, sc)
+        if not np.array_equal(idx, out["topk_idx"]):
+            return None
+        g = O.gates(c, lg, idx)
+        d = O.dispatch(c, idx, capacity=cap)
+        Y = O.tokens(c, i2, idx, lg, g, want_bwd=False, kept=(d["row_id_map"] >= 0).astype(np.int32))["Y"]
+        return float((Y * f32(i2["dY"])).sum())
+
+    checked = 0
+    for p in probes:
+        vals = []
+        for sgn in (1, -1):
+            i2 = dict(inp)
+            if p[0] == "X":
+                a = inp["X"].copy()
+                a[p[1:]] = int(np.array([sgn * FD_STEP], np.float32).view(np.uint32)[0] >> 16)
+                i2["X"] = a
+            else:
+                a = inp["W_r"].copy()
+                a[p] = sgn * FD_STEP
+                i2["W_r"] = a
+            vals.append(loss(i2))
+        if None in vals:
+            continue
+        fd = (vals[0] - vals[1]) / (2 * FD_STEP)
+        an = out["dX"][p[1:]] if p[0] == "X" else out["dW_r"][p]
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (p, fd, an)
+        checked += 1
+    assert checked >= 6
