@@ -51,6 +51,7 @@ def _load():
             _lib = ctypes.CDLL(build())
             _lib.ora_dispatch.restype = ctypes.c_int
             _lib.ora_dispatch_capacity.restype = ctypes.c_int
+            _lib.ora_dispatch_priority.restype = ctypes.c_int
     return _lib
 
 
@@ -105,11 +106,13 @@ def gates(c: OraCfg, logits, topk_idx):
     return g
 
 
-def dispatch(c: OraCfg, topk_idx, R: int | None = None, capacity: int | None = None):
+def dispatch(c: OraCfg, topk_idx, R: int | None = None, capacity: int | None = None, priority=None):
     """counts [E], offsets [E+1], tile_offsets [E+1], row_id_map [T,k], slot_src [R].
 
-    capacity: keep only each expert's first `capacity` assignments in token order
-    (dropped ones get row_id_map -1; counts are then the kept counts)."""
+    capacity: each expert keeps at most `capacity` assignments, dropped ones get
+    row_id_map -1 and counts are the kept counts.  Without `priority` the first ones
+    in token order are kept; with priority [T,k] the ones of largest priority (equal
+    priorities to the earlier assignment), their rows still in token order."""
     if R is None:
         R = c.T * c.k + c.E * (c.align - 1)
     counts = np.empty(c.E, np.int32)
@@ -118,9 +121,10 @@ def dispatch(c: OraCfg, topk_idx, R: int | None = None, capacity: int | None = N
     rim = np.empty((c.T, c.k), np.int32)
     src = np.full(R, -2, np.int32)
     cap = 2 ** 31 - 1 if capacity is None else int(capacity)
-    rc = _load().ora_dispatch_capacity(ctypes.byref(c), _p(np.ascontiguousarray(topk_idx, np.int32)),
-                                       ctypes.c_int32(cap), _p(counts), _p(offsets), _p(tiles), _p(rim), _p(src),
-                                       ctypes.c_int64(R))
+    pr = None if priority is None else np.ascontiguousarray(priority, np.float64)
+    rc = _load().ora_dispatch_priority(ctypes.byref(c), _p(np.ascontiguousarray(topk_idx, np.int32)),
+                                       ctypes.c_int32(cap), _p(pr), _p(counts), _p(offsets), _p(tiles), _p(rim),
+                                       _p(src), ctypes.c_int64(R))
     if rc != 0:
         raise ValueError("permuted rows exceed R")
     return dict(counts=counts, offsets=offsets, tile_offsets=tiles, row_id_map=rim, slot_src=src)
@@ -216,7 +220,8 @@ def round_bf16(x):
     return out
 
 
-def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int = 0, capacity=None):
+def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int = 0, capacity=None,
+               drop_by_gate: bool = False):
     """Whole-layer forward and backward for every token and every expert (small cases).
 
     sel_scores: optional (logits_f32, scores_f32) from another implementation;
@@ -231,7 +236,7 @@ def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int
     else:
         idx = select(c, sel_scores[0], sel_scores[1], inp.get("sel_bias"))
     g = gates(c, logits, idx)
-    d = dispatch(c, idx, capacity=capacity)
+    d = dispatch(c, idx, capacity=capacity, priority=g if drop_by_gate else None)
     kept = None if capacity is None else (d["row_id_map"] >= 0).astype(np.int32)
     tk = tokens(c, inp, idx, logits, g, kept=kept)
     dW13 = np.empty((c.E, 2 * c.F, c.H))

@@ -426,25 +426,49 @@ void ora_gates(const ora_cfg* cp, const double* logits, const int32_t* topk_idx,
 
 // Dispatch maps by a stable counting sort.  slot_src has R entries; entries at
 // or beyond offsets[E] are left untouched.  Padding slots get -1.
-int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, int32_t* counts,
-                          int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src, int64_t R);
+int ora_dispatch_priority(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, const double* priority,
+                          int32_t* counts, int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map,
+                          int32_t* slot_src, int64_t R);
 
 int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                  int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src, int64_t R) {
-  return ora_dispatch_capacity(cp, topk_idx, INT32_MAX, counts, offsets, tile_offsets, row_id_map, slot_src, R);
+  return ora_dispatch_priority(cp, topk_idx, INT32_MAX, nullptr, counts, offsets, tile_offsets, row_id_map, slot_src,
+                               R);
 }
 
-// Capacity-controlled dropping (position policy): expert e keeps its first `capacity`
+// Capacity-controlled dropping, position policy: expert e keeps its first `capacity`
 // assignments in token order; a dropped assignment gets row_id_map = -1 and no row.
 // counts are the kept counts.
 int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, int32_t* counts,
                           int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
                           int64_t R) {
+  return ora_dispatch_priority(cp, topk_idx, capacity, nullptr, counts, offsets, tile_offsets, row_id_map, slot_src,
+                               R);
+}
+
+// Capacity-controlled dropping, priority policy (priority [T,k], e.g. the gates): an
+// expert with more than `capacity` assignments keeps the `capacity` of largest
+// priority, equal priorities going to the earlier assignment in token order.  Kept
+// assignments take their rows in token order.  priority == nullptr is the position
+// policy.
+int ora_dispatch_priority(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, const double* priority,
+                          int32_t* counts, int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map,
+                          int32_t* slot_src, int64_t R) {
   const ora_cfg c = *cp;
   const int E = c.E, k = c.k;
-  for (int e = 0; e < E; ++e) counts[e] = 0;
-  for (int64_t i = 0; i < (int64_t)c.T * k; ++i) counts[topk_idx[i]]++;
-  for (int e = 0; e < E; ++e) counts[e] = std::min(counts[e], capacity);
+  const int64_t n = (int64_t)c.T * k;
+  // per expert, its assignments in token order (t-major, then j)
+  std::vector<std::vector<int64_t>> mine(E);
+  for (int64_t i = 0; i < n; ++i) mine[topk_idx[i]].push_back(i);
+  std::vector<char> keep(n, 0);
+  for (int e = 0; e < E; ++e) {
+    std::vector<int64_t> order = mine[e];
+    if (priority)  // stable: equal priorities stay in token order
+      std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return priority[a] > priority[b]; });
+    const size_t nk = std::min(order.size(), (size_t)std::max(capacity, 0));
+    for (size_t q = 0; q < nk; ++q) keep[order[q]] = 1;
+    counts[e] = (int32_t)nk;
+  }
   offsets[0] = 0;
   tile_offsets[0] = 0;
   for (int e = 0; e < E; ++e) {
@@ -454,17 +478,15 @@ int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t ca
   }
   if ((int64_t)offsets[E] > R) return -1;
   std::vector<int32_t> cursor(offsets, offsets + E);
-  for (int t = 0; t < c.T; ++t)
-    for (int j = 0; j < k; ++j) {
-      const int e = topk_idx[(size_t)t * k + j];
-      if (cursor[e] - offsets[e] >= counts[e]) {  // over capacity: dropped
-        row_id_map[(size_t)t * k + j] = -1;
-        continue;
-      }
-      const int32_t slot = cursor[e]++;
-      row_id_map[(size_t)t * k + j] = slot;
-      slot_src[slot] = t * k + j;
+  for (int64_t i = 0; i < n; ++i) {
+    if (!keep[i]) {
+      row_id_map[i] = -1;
+      continue;
     }
+    const int32_t slot = cursor[topk_idx[i]]++;
+    row_id_map[i] = slot;
+    slot_src[slot] = (int32_t)i;
+  }
   for (int e = 0; e < E; ++e)
     for (int32_t s = offsets[e] + counts[e]; s < offsets[e + 1]; ++s) slot_src[s] = -1;
   return 0;

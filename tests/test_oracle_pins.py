@@ -641,3 +641,49 @@ def test_capacity_finite_differences():
         assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (p, fd, an)
         checked += 1
     assert checked >= 6
+
+
+def test_capacity_priority_policy_brute_force():
+    rng = np.random.default_rng(22)
+    T, E, k = 150, 6, 3
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    pri = rng.integers(0, 5, size=(T, k)).astype(np.float64)  # many equal priorities
+    w = small(T=T, E=E, k=k)
+    c = O.cfg(w, align=8)
+    cap = 40
+    d = O.dispatch(c, idx, capacity=cap, priority=pri)
+    flat_e, flat_p = idx.ravel(), pri.ravel()
+    keep = np.zeros(T * k, bool)
+    for i in range(T * k):
+        same = np.flatnonzero(flat_e == flat_e[i])
+        better = ((flat_p[same] > flat_p[i]) | ((flat_p[same] == flat_p[i]) & (same < i))).sum()
+        keep[i] = better < cap
+    assert np.array_equal(d["row_id_map"].ravel() >= 0, keep)
+    assert (d["counts"] == np.minimum(np.bincount(flat_e, minlength=E), cap)).all()
+    rim = d["row_id_map"].ravel()
+    for e in range(E):
+        kept_i = [i for i in range(T * k) if flat_e[i] == e and keep[i]]
+        assert list(rim[kept_i]) == list(range(d["offsets"][e], d["offsets"][e] + len(kept_i)))
+    # constant priority is the position policy
+    flat = O.dispatch(c, idx, capacity=cap, priority=np.ones((T, k)))
+    pos = O.dispatch(c, idx, capacity=cap)
+    for key in pos:
+        assert np.array_equal(flat[key], pos[key]), key
+
+
+def test_capacity_drop_by_gate_keeps_largest_gates():
+    w = small(T=80, H=16, E=4, k=2, F=8, score_fn=0)
+    inp = inputs(w)
+    inp["W13"] = np.repeat(inp["W13"][:1], 4, axis=0)
+    inp["W2"] = np.repeat(inp["W2"][:1], 4, axis=0)
+    cap = 25
+    out = O.full_layer(w, inp, mirror=False, capacity=cap, drop_by_gate=True)
+    kept = out["row_id_map"] >= 0
+    g, idx = out["gates"], out["topk_idx"]
+    for e in range(4):
+        sel = idx == e
+        if sel.sum() > cap:
+            assert kept[sel].sum() == cap
+            assert g[sel & kept].min() >= g[sel & ~kept].max()
+    mlp = dense_swiglu(f32(inp["X"]), f32(inp["W13"][0]), f32(inp["W2"][0]))
+    assert np.allclose(out["Y"], (g * kept).sum(1, keepdims=True) * mlp, rtol=1e-12, atol=1e-14)
