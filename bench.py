@@ -155,7 +155,8 @@ def gpu_id_for_smi(torch, dev):
 # ---------------------------------------------------------------- our arm
 
 
-STAGES = ["router", "permute", "gemm_fwd", "combine", "combine_bwd", "gemm_bwd", "router_bwd", "permute_bwd"]
+STAGES = ["router", "permute", "quant_w", "gemm_fwd", "combine", "combine_bwd", "gemm_bwd", "router_bwd",
+          "permute_bwd"]
 
 
 def run_step(layer, X, dY, ev=None):
@@ -173,6 +174,8 @@ def run_step(layer, X, dY, ev=None):
     if layer.fp8:
         # the step re-quantizes the weights (as after every optimizer update) inside the timed region
         layer.quantize_weights()
+    rec(3)
+    if layer.fp8:
         M.moe_grouped_swiglu_mlp_fp8(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.W13q, layer.W13sc,
                                      layer.W2q, layer.W2sc, layer.GU, layer.A, layer.Yperm,
                                      X if c.F_shared else None, layer.W13q_s, layer.W13sc_s, layer.W2q_s,
@@ -181,12 +184,12 @@ def run_step(layer, X, dY, ev=None):
         M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
                                  layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
                                  layer.Yshared, layer.ws)
-    rec(3)
-    M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, layer.gates, layer.Yshared, layer.Y)
     rec(4)
+    M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, layer.gates, layer.Yshared, layer.Y)
+    rec(5)
     M.moe_unpermute_combine_bwd(c, dY, layer.Yperm, layer.row_id_map, layer.gates, layer.offsets, layer.counts,
                                 layer.dYperm, layer.dgates)
-    rec(5)
+    rec(6)
     sh = c.F_shared > 0
     if layer.fp8:
         M.moe_grouped_swiglu_mlp_bwd_fp8(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, layer.W13q,
@@ -200,13 +203,13 @@ def run_step(layer, X, dY, ev=None):
                                      layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm, layer.dW13, layer.dW2,
                                      X if sh else None, dY if sh else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
                                      layer.dGU_s, layer.dX_shared, layer.dW13_s, layer.dW2_s, layer.ws)
-    rec(6)
+    rec(7)
     M.moe_router_topk_bwd(c, X, w.W_r, layer.logits, layer.scores, layer.topk_idx, layer.gates, layer.dgates,
                           layer.dW_r, layer.dlogit_bias if w.logit_bias is not None else None, layer.dX_router,
                           layer.ws)
-    rec(7)
-    M.moe_permute_bwd(c, layer.dXperm, layer.row_id_map, layer.dX_router, layer.dX_shared, layer.dX)
     rec(8)
+    M.moe_permute_bwd(c, layer.dXperm, layer.row_id_map, layer.dX_router, layer.dX_shared, layer.dX)
+    rec(9)
 
 
 def launches_per_step(w):
@@ -232,12 +235,16 @@ def hbm_bytes(w):
     """Algorithmic bytes of the HBM-bound stages (index maps excluded)."""
     T, H, S_ = w.T, w.H, w.T * w.k
     sh = w.F_shared > 0
-    return {
+    d = {
         "permute": T * H * 2 + S_ * H * 2,
         "combine": S_ * H * 2 + T * H * 2 + (T * H * 2 if sh else 0),
         "combine_bwd": T * H * 2 + 2 * S_ * H * 2,
         "permute_bwd": S_ * H * 2 + T * H * 4 + T * H * 2 + (T * H * 2 if sh else 0),
     }
+    if w.fp8:  # bf16 weights read, E4M3 weights written (scales < 0.01%)
+        wel = 3 * w.E * w.F * w.H + 3 * w.F_shared * w.H
+        d["quant_w"] = wel * 2 + wel
+    return d
 
 
 def kernel_digest(files=("grouped_gemm.cu", "common.cuh")):

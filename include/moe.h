@@ -111,6 +111,17 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
                            const float* logit_bias, const float* sel_bias, float* logits, float* scores,
                            int32_t* topk_idx, float* gates, int32_t* counts, void* ws, void* stream);
 
+/* Router replay.  (Summary page, "Key claims": router replay for reinforcement-learning
+ * training, i.e. reusing routing decisions taken elsewhere.)  Same as moe_router_topk
+ * except that the selection is an input: topk_in [T,k] int32 (device) lists, per token, k
+ * distinct experts in [0,E) (not checked on the device; an id outside [0,E) is read as 0).
+ * logits and scores are computed as usual; gates are those of the given selection (renorm
+ * and gate_scale applied the same way); topk_idx receives a copy of topk_in; counts is the
+ * histogram of topk_in.  No group limit or selection bias is applied. */
+moe_status moe_router_replay(const moe_config* cfg, const moe_bf16* X, const float* W_r, const float* logit_bias,
+                             const int32_t* topk_in, float* logits, float* scores, int32_t* topk_idx, float* gates,
+                             int32_t* counts, void* ws, void* stream);
+
 /* Dispatch.  ("Method": the dispatcher permutes tokens so that the tokens of
  * one expert are contiguous, as the grouped GEMM needs; dropless, no capacity.)
  *  X            [T,H] bf16 (device)
@@ -123,6 +134,30 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
                        int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
                        moe_bf16* Xperm, void* ws, void* stream);
+
+/* Dispatch with capacity-controlled token dropping.  (Summary page, "Results": listed
+ * among the production features; the pages give no policy.)
+ * Two policies; kept gates are never renormalised:
+ *  - priority == NULL: each expert keeps its first `capacity` assignments in token order
+ *    (t-major, then j) and drops the rest, as a fixed-capacity dispatch does;
+ *  - priority [T,k] fp32 (device): an expert with more than `capacity` assignments keeps
+ *    the `capacity` of largest priority (pass the gates to drop the least-weighted ones);
+ *    equal priorities go to the earlier assignment in token order; -0 equals +0.
+ * Either way the kept assignments take their rows in token order.
+ * Arguments as moe_permute, plus:
+ *  capacity     int32 >= 0        slots per expert (e.g. ceil(capacity_factor * T * k / E));
+ *                                 a negative value is MOE_ERR_INVALID_ARG
+ *  priority     [T,k] fp32 (device, nullable), see above
+ *  kept_counts  [E] int32 out     min(counts[e], capacity)
+ * offsets and tile_offsets are built from kept_counts; row_id_map is -1 for a dropped
+ * assignment.  Pass kept_counts wherever a later call asks for counts (the grouped GEMMs'
+ * backward and moe_unpermute_combine_bwd).  Combine, combine backward and permute backward
+ * skip row -1, so a dropped assignment adds nothing to Y, gets dgates 0 and passes no
+ * gradient to X.  capacity >= max(counts) gives exactly moe_permute's results. */
+moe_status moe_permute_capacity(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx,
+                                const int32_t* counts, int32_t capacity, const float* priority,
+                                int32_t* kept_counts, int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map,
+                                int32_t* slot_src, moe_bf16* Xperm, void* ws, void* stream);
 
 /* Compute: all experts' SwiGLU MLPs in two grouped GEMM launches.  ("Method":
  * all local experts run in one grouped GEMM call; SwiGLU is the GLU variant of

@@ -26,13 +26,14 @@ from . import build as _build
 __all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
     "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd", "moe_router_topk_bwd", "moe_permute_bwd",
-    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc"]
+    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc", "moe_permute_capacity"]
 
 EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_workspace_init",
             "moe_read_device_error", "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp",
             "moe_unpermute_combine", "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd",
             "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc", "moe_fp8_workspace_size",
-            "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8"]
+            "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8",
+            "moe_router_replay", "moe_permute_capacity"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -76,6 +77,8 @@ def load(build: bool = True):
                 "moe_router_topk_bwd": [cfgp] + [vp] * 12,
                 "moe_permute_bwd": [cfgp] + [vp] * 6,
                 "moe_permute_noalloc": [cfgp] + [vp] * 9,
+                "moe_router_replay": [cfgp] + [vp] * 11,
+                "moe_permute_capacity": [cfgp, vp, vp, vp, ctypes.c_int32] + [vp] * 9,
                 "moe_fp8_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t)],
                 "moe_quantize_weights_fp8": [cfgp] + [vp] * 13,
                 "moe_grouped_swiglu_mlp_fp8": [cfgp] + [vp] * 20,
@@ -164,10 +167,29 @@ def moe_router_topk(cfg, X, W_r, logit_bias, sel_bias, logits, scores, topk_idx,
                                                ws)), _stream(stream))
 
 
+def moe_router_replay(cfg, X, W_r, logit_bias, topk_in, logits, scores, topk_idx, gates, counts, ws=None,
+                      stream=None):
+    _dev(X, W_r, logit_bias, topk_in, logits, scores, topk_idx, gates, counts, ws)
+    _call("moe_router_replay", cfg, *map(_ptr, (X, W_r, logit_bias, topk_in, logits, scores, topk_idx, gates, counts,
+                                                 ws)), _stream(stream))
+
+
 def moe_permute(cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, ws, stream=None):
     _dev(X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, ws)
     _call("moe_permute", cfg, *map(_ptr, (X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm,
                                            ws)), _stream(stream))
+
+
+def moe_permute_capacity(cfg, X, topk_idx, counts, capacity, priority, kept_counts, offsets, tile_offsets,
+                         row_id_map, slot_src, Xperm, ws, stream=None):
+    """moe_permute with a per-expert capacity.  priority None: each expert keeps its
+    first `capacity` assignments in token order; priority [T,k] fp32: the `capacity`
+    of largest priority (ties to the earlier assignment).  kept_counts [E] receives
+    min(counts, capacity); row_id_map is -1 for a dropped assignment."""
+    _dev(X, topk_idx, counts, priority, kept_counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, ws)
+    _call("moe_permute_capacity", cfg, _ptr(X), _ptr(topk_idx), _ptr(counts), ctypes.c_int32(int(capacity)),
+          *map(_ptr, (priority, kept_counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, ws)),
+          _stream(stream))
 
 
 def moe_permute_noalloc(cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm, stream=None):
@@ -269,10 +291,13 @@ class MoELayer:
     both can be captured in a CUDA graph.
     """
 
-    def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda", fp8: bool = False):
+    def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda", fp8: bool = False,
+                 capacity: int | None = None, drop_by_gate: bool = False):
         self.cfg = cfg
         self.w = weights
         self.fp8 = fp8
+        self.capacity = capacity
+        self.drop_by_gate = drop_by_gate
         T, H, E, k, F, Fs = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F, cfg.F_shared
         self.R = R = moe_max_rows(cfg)
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
@@ -282,6 +307,8 @@ class MoELayer:
         self.logits, self.scores = z(T, E, dt=f32), z(T, E, dt=f32)
         self.topk_idx, self.gates, self.counts = z(T, k, dt=i32), z(T, k, dt=f32), z(E, dt=i32)
         self.offsets, self.tile_offsets = z(E + 1, dt=i32), z(E + 1, dt=i32)
+        # with a capacity, the segment sizes every later stage uses are the kept counts
+        self.seg_counts = z(E, dt=i32) if capacity is not None else self.counts
         self.row_id_map, self.slot_src = z(T, k, dt=i32), z(R, dt=i32)
         self.Xperm, self.GU, self.A, self.Yperm = z(R, H), z(R, 2 * F), z(R, F), z(R, H)
         self.Y = z(T, H)
@@ -320,8 +347,13 @@ class MoELayer:
         self.X = X
         moe_router_topk(c, X, w.W_r, w.logit_bias, w.sel_bias, self.logits, self.scores, self.topk_idx, self.gates,
                         self.counts, self.ws)
-        moe_permute(c, X, self.topk_idx, self.counts, self.offsets, self.tile_offsets, self.row_id_map,
-                    self.slot_src, self.Xperm, self.ws)
+        if self.capacity is None:
+            moe_permute(c, X, self.topk_idx, self.counts, self.offsets, self.tile_offsets, self.row_id_map,
+                        self.slot_src, self.Xperm, self.ws)
+        else:
+            moe_permute_capacity(c, X, self.topk_idx, self.counts, self.capacity,
+                                 self.gates if self.drop_by_gate else None, self.seg_counts, self.offsets,
+                                 self.tile_offsets, self.row_id_map, self.slot_src, self.Xperm, self.ws)
         if self.fp8:
             self.quantize_weights()
             moe_grouped_swiglu_mlp_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.W13q, self.W13sc,
@@ -338,18 +370,18 @@ class MoELayer:
     def backward(self, dY: torch.Tensor) -> torch.Tensor:
         c, w = self.cfg, self.w
         self.dY = dY
-        moe_unpermute_combine_bwd(c, dY, self.Yperm, self.row_id_map, self.gates, self.offsets, self.counts,
+        moe_unpermute_combine_bwd(c, dY, self.Yperm, self.row_id_map, self.gates, self.offsets, self.seg_counts,
                                   self.dYperm, self.dgates)
         sh = c.F_shared > 0
         if self.fp8:
-            moe_grouped_swiglu_mlp_bwd_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.counts, self.W13q,
+            moe_grouped_swiglu_mlp_bwd_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.seg_counts, self.W13q,
                                            self.W13sc, self.W2q, self.W2sc, self.GU, self.A, self.dYperm, self.dGU,
                                            self.dXperm, self.dW13, self.dW2, self.X if sh else None,
                                            dY if sh else None, self.W13q_s, self.W13sc_s, self.W2q_s, self.W2sc_s,
                                            self.GU_s, self.A_s, self.dGU_s, self.dX_shared, self.dW13_s, self.dW2_s,
                                            self.fp8_ws, self.ws)
         else:
-            moe_grouped_swiglu_mlp_bwd(c, self.Xperm, self.offsets, self.tile_offsets, self.counts, w.W13, w.W2,
+            moe_grouped_swiglu_mlp_bwd(c, self.Xperm, self.offsets, self.tile_offsets, self.seg_counts, w.W13, w.W2,
                                        self.GU, self.A, self.dYperm, self.dGU, self.dXperm, self.dW13, self.dW2,
                                        self.X if sh else None, dY if sh else None, w.W13_s, w.W2_s, self.GU_s,
                                        self.A_s, self.dGU_s, self.dX_shared, self.dW13_s, self.dW2_s, self.ws)

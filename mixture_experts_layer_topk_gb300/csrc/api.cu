@@ -203,6 +203,22 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
                                         (cudaStream_t)stream, nsm));
 }
 
+moe_status moe_router_replay(const moe_config* cfg, const moe_bf16* X, const float* W_r, const float* logit_bias,
+                             const int32_t* topk_in, float* logits, float* scores, int32_t* topk_idx, float* gates,
+                             int32_t* counts, void* ws, void* stream) {
+  moe_status s = check_cfg(cfg, false);
+  if (s != MOE_OK) return s;
+  if (!tok_ok(cfg, X) || !W_r || !tok_ok(cfg, topk_in) || !tok_ok(cfg, logits) || !tok_ok(cfg, scores) ||
+      !tok_ok(cfg, topk_idx) || !tok_ok(cfg, gates) || !counts)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W_r) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  (void)ws;
+  const int nsm = num_sms();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  return cuda_status(launch_router_topk(*cfg, X, W_r, logit_bias, nullptr, logits, scores, topk_idx, gates, counts,
+                                        (cudaStream_t)stream, nsm, topk_in));
+}
+
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
                        int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
                        moe_bf16* Xperm, void* ws, void* stream) {
@@ -216,9 +232,33 @@ moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* 
   const WsLayout L = ws_layout(*cfg);
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  return cuda_status(launch_permute(*cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src, Xperm,
-                                    ws_ptr<int32_t>(ws, L.chunk_counts), ws_ptr<int32_t>(ws, L.chunk_base),
-                                    ws_ptr<int>(ws, L.err), nsm, (cudaStream_t)stream));
+  return cuda_status(launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, nullptr, offsets, tile_offsets,
+                                    row_id_map, slot_src, Xperm, ws_ptr<int32_t>(ws, L.chunk_counts),
+                                    ws_ptr<int32_t>(ws, L.chunk_base), nullptr, nullptr, ws_ptr<int>(ws, L.err), nsm,
+                                    (cudaStream_t)stream));
+}
+
+moe_status moe_permute_capacity(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx,
+                                const int32_t* counts, int32_t capacity, const float* priority,
+                                int32_t* kept_counts, int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map,
+                                int32_t* slot_src, moe_bf16* Xperm, void* ws, void* stream) {
+  moe_status s = check_cfg(cfg, false);
+  if (s != MOE_OK) return s;
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (priority && !tok_ok(cfg, priority)) return MOE_ERR_INVALID_ARG;
+  if (!tok_ok(cfg, X) || !tok_ok(cfg, topk_idx) || !counts || !kept_counts || !offsets || !tile_offsets ||
+      !tok_ok(cfg, row_id_map) || !slot_src || !Xperm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Xperm)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(*cfg);
+  const int nsm = num_sms();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute(*cfg, X, topk_idx, counts, capacity, priority, kept_counts, offsets,
+                                    tile_offsets, row_id_map, slot_src, Xperm, ws_ptr<int32_t>(ws, L.chunk_counts),
+                                    ws_ptr<int32_t>(ws, L.chunk_base), ws_ptr<int32_t>(ws, L.drop_order),
+                                    ws_ptr<int32_t>(ws, L.drop_start), ws_ptr<int>(ws, L.err), nsm,
+                                    (cudaStream_t)stream));
 }
 
 moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,

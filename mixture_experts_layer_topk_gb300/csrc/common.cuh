@@ -26,6 +26,9 @@ struct WsLayout {
   size_t dl_rows;       // bf16[3Tp * Ep]   dlogits row blocks hi, mid, lo (dW_r)
   size_t dl_cols;       // bf16[T * 6Ep]    dlogits column blocks hi, hi, mid, hi, lo, mid (dX_router)
   int Tp, Ep;
+  // capacity dropping by priority: assignments grouped by expert in token order
+  size_t drop_order;    // int32[T * k]
+  size_t drop_start;    // int32[E + 1] segment starts of drop_order
   size_t total;
 };
 
@@ -73,6 +76,10 @@ inline WsLayout ws_layout(const moe_config& c) {
   if (tc) o = align256(o + (size_t)3 * L.Tp * L.Ep * 2);
   L.dl_cols = o;
   if (tc) o = align256(o + (size_t)c.T * 6 * L.Ep * 2);
+  L.drop_order = o;
+  o = align256(o + (size_t)c.T * c.k * sizeof(int32_t));
+  L.drop_start = o;
+  o = align256(o + (size_t)(c.E + 1) * sizeof(int32_t));
   L.total = o;
   return L;
 }

@@ -39,14 +39,18 @@ struct RouterBwdScratch {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm);
+                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given = nullptr);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
                               float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,
                               cudaStream_t st);
+// cap: per-expert capacity (INT_MAX = dropless); priority [T,k] (nullable): drop
+// the lowest-priority assignments instead of the last ones in token order, which
+// needs kept, drop_order [T*k] and drop_start [E+1].
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
-                           int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
-                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, int nsm,
+                           int cap, const float* priority, int32_t* kept, int32_t* offsets, int32_t* tile_offsets,
+                           int32_t* row_id_map, int32_t* slot_src, uint16_t* Xperm, int32_t* chunk_counts,
+                           int32_t* chunk_base, int32_t* drop_order, int32_t* drop_start, int* err, int nsm,
                            cudaStream_t st);
 cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int32_t* row_id_map, const float* gates,
                            const uint16_t* Ysh, uint16_t* Y, cudaStream_t st);

@@ -13,6 +13,19 @@
 //   offsets[e] + #{t' < t : e selected by t'}     (tokens keep their order)
 // computed as chunk_base[c][e] + rank of the assignment among the chunk's
 // assignments to e, the rank taken with warp match/ballot in token-major order.
+//
+// Capacity-controlled token dropping (summary page, "Results": listed among the
+// production features, no policy given) reuses the same ranks: with a capacity C, an
+// assignment whose position within its expert, in token order, is C or more gets
+// no slot (row_id_map -1), and the segments are sized by the kept counts
+// min(counts[e], C).  Dropless dispatch is the case C = INT_MAX.
+//
+// Dropping by priority (an over-full expert keeps the C assignments of largest
+// priority, e.g. the gate; equal priorities to the earlier assignment): the
+// scatter only groups each expert's assignments in token order (drop_order), and
+// one CTA per expert finds the C-th largest priority by a 4-pass radix select on
+// order-preserving 32-bit keys, breaks ties in token order with a block scan, and
+// writes the kept assignments' rows, still in token order.
 #include "common.cuh"
 #include "moe_internal.h"
 
@@ -41,8 +54,10 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const int32_t* __restrict__ 
 // G threads per expert each own a contiguous range of chunks.
 __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ counts,
                                                const int32_t* __restrict__ chunk_counts, int nch, int E, int align,
+                                               int cap, int32_t* __restrict__ kept,
                                                int32_t* __restrict__ offsets, int32_t* __restrict__ tile_offsets,
-                                               int32_t* __restrict__ chunk_base, int* err) {
+                                               int32_t* __restrict__ chunk_base, int32_t* __restrict__ drop_start,
+                                               int* err) {
   __shared__ int part[1024];
   __shared__ int seg_start[257];
   const int G = 1024 / E >= 1 ? 1024 / E : 1;  // threads per expert
@@ -63,17 +78,21 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
   }
   __syncthreads();
   if (tid == 0) {
-    int off = 0, tiles = 0;
+    int off = 0, tiles = 0, doff = 0;
     offsets[0] = 0;
     tile_offsets[0] = 0;
     for (int x = 0; x < E; ++x) {
-      const int tot = seg_start[x];
+      if (drop_start) drop_start[x] = doff;
+      doff += seg_start[x];
+      const int tot = min(seg_start[x], cap);
+      if (kept) kept[x] = tot;
       seg_start[x] = off;
       off += (tot + align - 1) / align * align;
       tiles += (tot + 127) / 128;
       offsets[x + 1] = off;
       tile_offsets[x + 1] = tiles;
     }
+    if (drop_start) drop_start[E] = doff;
   }
   __syncthreads();
   if (e < E) {
@@ -96,8 +115,10 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
                                                  const int32_t* __restrict__ chunk_base,
                                                  const int32_t* __restrict__ counts,
                                                  const int32_t* __restrict__ offsets, int T, int H, int E, int k,
-                                                 int nch, int32_t* __restrict__ row_id_map,
-                                                 int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm) {
+                                                 int nch, int cap, int32_t* __restrict__ row_id_map,
+                                                 int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm,
+                                                 int32_t* __restrict__ drop_order,
+                                                 const int32_t* __restrict__ drop_start) {
   __shared__ int cursor[8][256];
   const int nvec = H / 8;
   if ((int)blockIdx.x >= nch) {
@@ -151,12 +172,122 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
     __syncwarp();
     if (ok) {
       const int slot = base + rank;
-      row_id_map[(size_t)t0 * k + i] = slot;
-      slot_src[slot] = t0 * k + i;
+      if (drop_order) {
+        drop_order[drop_start[e] + (slot - offsets[e])] = t0 * k + i;  // rows are assigned by k_drop_select
+      } else if (slot - offsets[e] < cap) {
+        row_id_map[(size_t)t0 * k + i] = slot;
+        slot_src[slot] = t0 * k + i;
+      } else {
+        row_id_map[(size_t)t0 * k + i] = -1;  // beyond the expert's capacity: dropped
+      }
       if (rank == 0) cursor[warp][e] = base + __popc(peers);
     }
     __syncwarp();
   }
+}
+
+// Order-preserving key of a priority: a larger float gives a larger key; -0 and +0
+// give the same key.
+__device__ __forceinline__ uint32_t priority_key(float f) {
+  const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix count of `flag` over the 1024 threads of the block, in thread
+// order; *total receives the block's count.  Every thread must call it.
+__device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned b = __ballot_sync(0xffffffffu, flag);
+  if (lane == 0) warp_tot[warp] = __popc(b);
+  __syncthreads();
+  int before = 0, all = 0;
+  for (int w = 0; w < 32; ++w) {
+    const int n = warp_tot[w];
+    before += w < warp ? n : 0;
+    all += n;
+  }
+  __syncthreads();
+  *total = all;
+  return before + __popc(b & ((1u << lane) - 1u));
+}
+
+// One CTA per expert: keep the cap assignments of largest priority (ties to the
+// earlier assignment in token order) and give them rows in token order.
+__global__ void __launch_bounds__(1024) k_drop_select(const float* __restrict__ priority,
+                                                      const int32_t* __restrict__ drop_order,
+                                                      const int32_t* __restrict__ drop_start,
+                                                      const int32_t* __restrict__ offsets,
+                                                      const int32_t* __restrict__ kept, int cap,
+                                                      int32_t* __restrict__ row_id_map,
+                                                      int32_t* __restrict__ slot_src, int* err) {
+  __shared__ int hist[256];
+  __shared__ int warp_tot[32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int s0 = drop_start[e], n = drop_start[e + 1] - s0;
+  const int row0 = offsets[e];
+  const int32_t* ord = drop_order + s0;
+  if (n <= cap) {  // nothing to drop
+    for (int i = tid; i < n; i += 1024) {
+      const int src = ord[i];
+      row_id_map[src] = row0 + i;
+      slot_src[row0 + i] = src;
+    }
+    return;
+  }
+  if (cap == 0) {
+    for (int i = tid; i < n; i += 1024) row_id_map[ord[i]] = -1;
+    return;
+  }
+  // radix select, 8 bits per pass from the top: prefix = the cap-th largest key,
+  // need = how many keys equal to it are kept
+  uint32_t prefix = 0;
+  int need = cap;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int b = tid; b < 256; b += 1024) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += 1024) {
+      const uint32_t key = priority_key(__ldg(priority + ord[i]));
+      if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int above = 0, b = 255;
+      for (; b > 0; --b) {
+        if (above + hist[b] >= need) break;
+        above += hist[b];
+      }
+      s_prefix = prefix | ((uint32_t)b << shift);
+      s_need = need - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+  }
+  // token-order pass: keep key > prefix, and the first `need` keys equal to it
+  int eq_run = 0, kept_run = 0;
+  for (int r0 = 0; r0 < n; r0 += 1024) {
+    const int i = r0 + tid;
+    const bool valid = i < n;
+    const int src = valid ? ord[i] : 0;
+    const uint32_t key = valid ? priority_key(__ldg(priority + src)) : 0u;
+    int eq_tot, kept_tot;
+    const bool eq = valid && key == prefix;
+    const int eq_rank = eq_run + block_excl_count(eq, warp_tot, &eq_tot);
+    const bool keep = valid && (key > prefix || (eq && eq_rank < need));
+    const int krank = kept_run + block_excl_count(keep, warp_tot, &kept_tot);
+    if (keep) {
+      row_id_map[src] = row0 + krank;
+      slot_src[row0 + krank] = src;
+    } else if (valid) {
+      row_id_map[src] = -1;
+    }
+    eq_run += eq_tot;
+    kept_run += kept_tot;
+  }
+  if (tid == 0 && kept_run != kept[e]) set_device_error(err, MOE_ERR_DEVICE, 3000 + e);
 }
 
 // Xperm[row_id_map[t,j]] = X[t]: 16-byte vectors over the whole grid, each
@@ -305,20 +436,31 @@ __global__ void __launch_bounds__(256) k_permute_bwd(const uint16_t* __restrict_
 }  // namespace
 
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
-                           int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
-                           uint16_t* Xperm, int32_t* chunk_counts, int32_t* chunk_base, int* err, int nsm,
+                           int cap, const float* priority, int32_t* kept, int32_t* offsets, int32_t* tile_offsets,
+                           int32_t* row_id_map, int32_t* slot_src, uint16_t* Xperm, int32_t* chunk_counts,
+                           int32_t* chunk_base, int32_t* drop_order, int32_t* drop_start, int* err, int nsm,
                            cudaStream_t st) {
+  if (priority && (!kept || !drop_order || !drop_start)) return cudaErrorInvalidValue;
+  if (!priority) drop_order = drop_start = nullptr;
   const int nch = (c.T + kChunk - 1) / kChunk;
   cudaError_t e;
   if (nch > 0) {
     k_chunk_hist<<<nch, 256, 0, st>>>(topk_idx, c.T, c.E, c.k, chunk_counts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  k_scan<<<1, 1024, 0, st>>>(counts, chunk_counts, nch, c.E, c.align, offsets, tile_offsets, chunk_base, err);
+  k_scan<<<1, 1024, 0, st>>>(counts, chunk_counts, nch, c.E, c.align, cap, kept, offsets, tile_offsets, chunk_base,
+                             drop_start, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(X, topk_idx, chunk_base, counts, offsets, c.T, c.H, c.E, c.k,
-                                                   nch, row_id_map, slot_src, Xperm);
+  // the padding CTAs size each segment's tail from the kept counts
+  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(X, topk_idx, chunk_base, kept ? kept : counts, offsets, c.T, c.H,
+                                                   c.E, c.k, nch, cap, row_id_map, slot_src, Xperm, drop_order,
+                                                   drop_start);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (priority) {
+    k_drop_select<<<c.E, 1024, 0, st>>>(priority, drop_order, drop_start, offsets, kept, cap, row_id_map, slot_src,
+                                        err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (c.T > 0) {
     const int64_t vec = (int64_t)c.T * (c.H / 8);
     int64_t blocks = (vec + 255) / 256;

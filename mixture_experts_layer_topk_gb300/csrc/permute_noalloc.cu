@@ -73,7 +73,8 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const moe_bf16*
   if (cudaMemsetAsync(scratch, 0, 64 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
   int32_t* chunk_counts = scratch + 64;
   int32_t* chunk_base = chunk_counts + nch * cfg->E;
-  const cudaError_t e = moe::launch_permute(*cfg, X, topk_idx, counts, offsets, tile_offsets, row_id_map, slot_src,
-                                            Xperm, chunk_counts, chunk_base, scratch, nsm, st);
+  const cudaError_t e =
+      moe::launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, nullptr, offsets, tile_offsets, row_id_map,
+                          slot_src, Xperm, chunk_counts, chunk_base, nullptr, nullptr, scratch, nsm, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

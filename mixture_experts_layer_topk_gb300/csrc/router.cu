@@ -36,6 +36,7 @@ struct RouteArgs {
   int score_fn, renorm;
   float gate_scale;
   int n_group, topk_group, group_score;
+  const int32_t* given;  // router replay: the selection to use instead of top-k (nullable)
 };
 
 // (value, index) maximum over the warp; ties to the lower index.  Lanes with
@@ -104,7 +105,7 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
     }
   }
   // group limit
-  if (a.n_group > 1) {
+  if (a.n_group > 1 && !a.given) {
     const int per = E / a.n_group;
     float my_gs = -FLT_MAX;
     for (int g = 0; g < a.n_group; ++g) {
@@ -149,9 +150,13 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
       if (e < E && !(keep >> (e / per) & 1)) excl |= 1u << i;
     }
   }
-  // top-k: lane j ends up holding the j-th selected expert
+  // top-k: lane j ends up holding the j-th selected expert (router replay: read it)
   int my_e = -1;
-  for (int j = 0; j < a.k; ++j) {
+  if (a.given && lane < a.k) {
+    my_e = a.given[(size_t)t * a.k + lane];
+    if ((unsigned)my_e >= (unsigned)E) my_e = 0;  // ids are validated on the host side of replay callers
+  }
+  for (int j = 0; j < (a.given ? 0 : a.k); ++j) {
     float v = -FLT_MAX;
     int e = INT_MAX;
 #pragma unroll
@@ -677,10 +682,10 @@ struct Bf16In {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm) {
+                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given) {
   RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
               c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
-              c.group_score};
+              c.group_score, given};
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
   if (e != cudaSuccess) return e;
   if (c.T == 0) return cudaSuccess;

@@ -436,7 +436,10 @@ int ora_dispatch(const ora_cfg* cp, const int32_t* topk_idx, int32_t* counts, in
                                R);
 }
 
-// Capacity-controlled dropping, position policy: expert e keeps its first `capacity`
+// Capacity-controlled token dropping ("Scalable Training of Mixture-of-Experts Models
+// with Megatron Core", summary page, "Results": a production feature, no policy given;
+// both policies below are readings).
+// Position policy: expert e keeps its first `capacity`
 // assignments in token order; a dropped assignment gets row_id_map = -1 and no row.
 // counts are the kept counts.
 int ora_dispatch_capacity(const ora_cfg* cp, const int32_t* topk_idx, int32_t capacity, int32_t* counts,

@@ -56,11 +56,12 @@ def logit_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     return float((np.abs(g - r).max(axis=1) / den).max())
 
 
-def make_layer(w: S.Workload, inp: dict, device="cuda"):
+def make_layer(w: S.Workload, inp: dict, device="cuda", capacity=None, drop_by_gate=False):
     import mixture_experts_layer_topk_gb300 as M
     cfg = M.config_from(w)
     weights = M.LayerWeights(
         W_r=to_dev(inp["W_r"]), W13=to_dev(inp["W13"]), W2=to_dev(inp["W2"]),
         logit_bias=to_dev(inp.get("logit_bias")), sel_bias=to_dev(inp.get("sel_bias")),
         W13_s=to_dev(inp.get("W13_s")), W2_s=to_dev(inp.get("W2_s")))
-    return M.MoELayer(cfg, weights, device=device, fp8=getattr(w, "fp8", False))
+    return M.MoELayer(cfg, weights, device=device, fp8=getattr(w, "fp8", False), capacity=capacity,
+                      drop_by_gate=drop_by_gate)

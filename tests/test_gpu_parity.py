@@ -299,3 +299,120 @@ def test_fp8_gemm_modes_match_torch():
         errs[f"fc1_wgrad[{e}]"] = slice_rel_err(host_f64(L.dW13[e]), dW13.cpu().numpy(), 2)
     bad = {k: v for k, v in errs.items() if not v < 1e-2}
     assert not bad, bad
+
+
+# ---------------------------------------------------------------- router replay
+
+
+@pytest.mark.parametrize("name", ["dsv3-mini", "ragged-softmax", "e128-norenorm"])
+def test_router_replay(name):
+    import mixture_experts_layer_topk_gb300 as M
+    w = CASES[name]
+    inp = S.host_inputs(w, weights=False)
+    cfg = M.config_from(w)
+    X, W_r = to_dev(inp["X"]), to_dev(inp["W_r"])
+    lb, sb = to_dev(inp.get("logit_bias")), to_dev(inp.get("sel_bias"))
+    T, E, k = w.T, w.E, w.k
+    f32, i32 = torch.float32, torch.int32
+    new = lambda *s, dt=f32: torch.empty(*s, dtype=dt, device="cuda")
+    ws = torch.zeros(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    logits, scores, idx, gates, counts = new(T, E), new(T, E), new(T, k, dt=i32), new(T, k), new(E, dt=i32)
+    M.moe_router_topk(cfg, X, W_r, lb, sb, logits, scores, idx, gates, counts, ws)
+    # replaying the router's own selection reproduces its gates and counts exactly
+    l2, s2, i2, g2, c2 = new(T, E), new(T, E), new(T, k, dt=i32), new(T, k), new(E, dt=i32)
+    M.moe_router_replay(cfg, X, W_r, lb, idx, l2, s2, i2, g2, c2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(i2, idx) and torch.equal(g2, gates) and torch.equal(c2, counts) and torch.equal(l2, logits)
+    # a different selection: every expert id shifted by one
+    other = ((idx + 1) % E).contiguous()
+    M.moe_router_replay(cfg, X, W_r, lb, other, l2, s2, i2, g2, c2, ws)
+    torch.cuda.synchronize()
+    o = other.cpu().numpy()
+    assert torch.equal(i2, other)
+    assert np.array_equal(c2.cpu().numpy(), np.bincount(o.ravel(), minlength=E))
+    c = O.cfg(w)
+    lg, _ = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
+    tol = TOL_ROUTER * max(1.0, float(np.abs(lg).max()))
+    assert slice_rel_err(g2.cpu().numpy(), O.gates(c, lg, o)) < 2 * tol
+
+
+# capacity cases: (workload, capacity as a fraction of the mean load T*k/E, drop by gate,
+# token rows repeated with this period (identical tokens give equal gates: ties))
+CAPACITY_CASES = {
+    "position-ragged": ("ragged-softmax", 0.8, False, 0),
+    "position-dsv3-mini": ("dsv3-mini", 1.0, False, 0),
+    "position-e16-sigmoid": ("e16-sigmoid", 1.25, False, 0),
+    "position-zero-capacity": ("k-equals-e", 0.0, False, 0),
+    "gate-ragged": ("ragged-softmax", 0.8, True, 0),
+    "gate-ragged-ties": ("ragged-softmax", 0.6, True, 37),
+    "gate-e128": ("e128-norenorm", 0.9, True, 0),
+    "gate-dsv3-mini-ties": ("dsv3-mini", 1.0, True, 11),
+}
+
+
+@pytest.mark.parametrize("name", list(CAPACITY_CASES))
+def test_capacity_dropping_parity(name):
+    wname, frac, by_gate, period = CAPACITY_CASES[name]
+    w = CASES[wname]
+    inp = S.host_inputs(w)
+    if period:
+        inp["X"] = np.ascontiguousarray(inp["X"][np.arange(w.T) % period])
+    cap = int(np.ceil(frac * w.T * w.k / w.E))
+    layer = make_layer(w, inp, capacity=cap, drop_by_gate=by_gate)
+    layer.forward(to_dev(inp["X"]))
+    layer.backward(to_dev(inp["dY"]))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    c = O.cfg(w, mirror=True)
+    logits, _ = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
+    idx = layer.topk_idx.cpu().numpy()
+    assert np.array_equal(idx, O.select(c, layer.logits.cpu().numpy(), layer.scores.cpu().numpy(),
+                                        inp.get("sel_bias")))
+    # the keep decision compares the kernel's own fp32 gates, as the kernel does
+    pri = layer.gates.cpu().numpy().astype(np.float64) if by_gate else None
+    d = O.dispatch(c, idx, R=layer.R, capacity=cap, priority=pri)
+    n_used = int(d["offsets"][-1])
+    assert np.array_equal(layer.counts.cpu().numpy(), np.bincount(idx.ravel(), minlength=w.E))
+    assert np.array_equal(layer.seg_counts.cpu().numpy(), d["counts"])
+    assert np.array_equal(layer.offsets.cpu().numpy(), d["offsets"])
+    assert np.array_equal(layer.tile_offsets.cpu().numpy(), d["tile_offsets"])
+    assert np.array_equal(layer.row_id_map.cpu().numpy(), d["row_id_map"])
+    assert np.array_equal(layer.slot_src.cpu().numpy()[:n_used], d["slot_src"][:n_used])
+    kept = (d["row_id_map"] >= 0).astype(np.int32)
+    assert kept.sum() == np.minimum(np.bincount(idx.ravel(), minlength=w.E), cap).sum()
+    if cap == 0:
+        assert n_used == 0
+    g = O.gates(c, logits, idx)
+    tk = O.tokens(c, inp, idx, logits, g, kept=kept)
+    assert slice_rel_err(host_f64(layer.Y), tk["Y"]) < TOL_BF16
+    dg = layer.dgates.cpu().numpy()
+    assert (dg[kept == 0] == 0).all()
+    # a token left with one kept assignment has a one-entry dgates row, whose reference
+    # can be ~0 by cancellation (one dot product): such rows are compared within the
+    # whole tensor as one slice; rows with every assignment kept as usual
+    full = kept.sum(1) == w.k
+    if full.any():
+        assert slice_rel_err(dg[full], tk["dgates"][full]) < TOL_BF16
+    assert slice_rel_err(dg.reshape(1, -1), tk["dgates"].reshape(1, -1)) < TOL_BF16
+    assert slice_rel_err(host_f64(layer.dX), tk["dX"]) < TOL_BF16
+    for e in range(w.E):
+        dW13, dW2 = O.expert_wgrad(c, inp, idx, g, e, kept=kept)
+        assert slice_rel_err(host_f64(layer.dW13[e]), dW13, 2) < TOL_BF16, e
+        assert slice_rel_err(host_f64(layer.dW2[e]), dW2, 2) < TOL_BF16, e
+    dWr, _ = O.router_wgrad(c, inp["X"], tk["dlogits"])
+    assert slice_rel_err(layer.dW_r.cpu().numpy(), dWr) < TOL_BF16
+
+
+@pytest.mark.parametrize("by_gate", [False, True])
+def test_capacity_at_max_load_equals_dropless(by_gate):
+    w = CASES["ragged-softmax"]
+    inp = S.host_inputs(w)
+    ref = run_layer(w, inp)
+    cap = int(ref.counts.max().item())
+    layer = make_layer(w, inp, capacity=cap, drop_by_gate=by_gate)
+    layer.forward(to_dev(inp["X"]))
+    layer.backward(to_dev(inp["dY"]))
+    torch.cuda.synchronize()
+    for name in ("offsets", "tile_offsets", "row_id_map", "Y", "dX", "dgates", "dW13", "dW2", "dW_r"):
+        assert torch.equal(getattr(layer, name), getattr(ref, name)), name
+    assert torch.equal(layer.seg_counts, ref.counts)
