@@ -75,6 +75,7 @@ struct GemmArgs {
   int ksplit_rows;          // WGRAD dense: > 0 splits the rows into chunks of this many ("experts")
   int kwrap;                // K-major A (FWD/DGRAD): the K coordinate wraps modulo kwrap;
                             // WGRAD: B's row coordinate wraps modulo kwrap (0: no wrap)
+  int n_fast;               // WGRAD: tiles walk N fastest (else M fastest) within an expert
   // FP8 block scales (UE8M0 bytes): A and B, addressed per mode (see the SF warps)
   const uint8_t* sfa;
   int64_t sfa_ld;
@@ -125,8 +126,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     const int per = g.m_tiles * g.n_tiles;
     const int e = t / per, local = t % per;
     r.e = e;
-    r.m0 = (local % g.m_tiles) * BM;
-    r.n0 = (local / g.m_tiles) * BN;
+    r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
+    r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
     if (g.dense_rows > 0 && g.ksplit_rows > 0) {
       r.k0 = e * g.ksplit_rows;
       const int rows = g.dense_rows - r.k0 < g.ksplit_rows ? g.dense_rows - r.k0 : g.ksplit_rows;
@@ -184,11 +185,11 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
     const int e = t / per, local = t % per;
-    const int m = 2 * (local % mpairs) + rank;
+    const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
     r.m0 = m * BM;  // past M when invalid: the MN-major A box reads zeros
-    r.n0 = (local / mpairs) * BN;
+    r.n0 = (g.n_fast ? local % g.n_tiles : local / mpairs) * BN;
     if (g.dense_rows > 0) {
       r.k0 = 0;
       r.kb = (g.dense_rows + BK - 1) / BK;
@@ -850,6 +851,13 @@ inline int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
 // B, halving its shared-memory operand traffic per MMA.
 constexpr bool use_pairs() { return true; }
 
+// Weight-gradient tile order.  Both operands of an expert's wgrad are its token rows:
+// A spans the M columns, B the N columns.  Walking the smaller dimension fastest keeps
+// that operand (all of its slices) resident in L2 while one slice of the larger
+// operand is shared by the concurrent tiles, so each byte of the larger one is read
+// from DRAM once.
+inline int wgrad_n_fast(int m, int n) { return m > n ? 1 : 0; }
+
 // pair tiles of a ragged launch: sum over experts of ceil(m tiles / 2) <= max_mtiles / 2 + E
 inline int pair_tiles(const GemmShape& s, int n_tiles) {
   const int mt = s.dense_rows > 0 ? (s.dense_rows + 127) / 128 : s.max_mtiles;
@@ -938,6 +946,7 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
   g.E = s.E; g.m_tiles = s.H / 128; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
+  g.n_fast = wgrad_n_fast(s.H, s.F);
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
   if (bn == 256 && use_pairs())
     return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(
@@ -958,6 +967,7 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
   g.E = s.E; g.m_tiles = 2 * s.F / 128; g.n_tiles = s.H / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
+  g.n_fast = wgrad_n_fast(2 * s.F, s.H);
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
   if (bn == 256 && use_pairs())
     return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(

@@ -126,6 +126,10 @@ WORKLOADS = {
     # shapes along K for FC1, 0.4 GB of expert weights: larger than L2, small enough
     # for a multi-pass profiler capture)
     "mixtral-small": Workload("mixtral-small", T=4096, H=4096, E=8, k=2, F=2048),
+    # profiling stand-in with DeepSeek-V3-style routing and small expert segments
+    # (about 64 rows per expert): 2.8 GB of expert weights, small enough for a full capture
+    "dsv3-small": Workload("dsv3-small", T=2048, H=7168, E=256, k=8, F=256, F_shared=256, score_fn=1,
+                           renorm=1, gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True),
 }
 
 SKEW_BETA = 2.0
