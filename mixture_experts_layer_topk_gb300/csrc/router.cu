@@ -5,7 +5,8 @@
 // states, kept in FP32, followed by softmax or sigmoid scoring and top-k
 // selection.  The kernels here fuse the projection (an FP32 GEMV / skinny
 // GEMM), the scoring, the optional group limit, the top-k (warp shuffles) and
-// the gate computation into one launch.
+// the gate computation into one launch for E <= 32; for larger E the projection is
+// a register-tiled split-K GEMM followed by a routing pass (two launches).
 //
 // Selection rule: key = logit (+ sel_bias) for softmax, sigmoid(logit)
 // (+ sel_bias) for sigmoid, formed in FP32; the k experts are listed in
@@ -268,136 +269,137 @@ __global__ void __launch_bounds__(256) k_router_small(RouteArgs a) {
 // 32 < E <= EP: a CTA computes the logits of BT tokens for all experts with a
 // register-tiled FP32 GEMM (TM tokens x 8 experts per thread), then its warps
 // route the tokens.
-template <int EP, int TM>
-struct LargeCfg {
-  static constexpr int TC = EP / 8;     // threads along experts
-  static constexpr int TR = 256 / TC;   // threads along tokens
-  static constexpr int BT = TR * TM;    // tokens per CTA
-  static constexpr int BK = 16;
-  static constexpr int LS = EP + 1;     // logits row stride in shared memory
-  static constexpr size_t smem = sizeof(float) * ((size_t)BK * BT + (size_t)BK * EP + (size_t)BT * LS) +
-                                 sizeof(int) * EP;
-};
+// ---------------------------------------------------------------- E > 32
+// Logits on the CUDA cores in two passes.  k_router_gemm: P = X W_r^T over one half
+// of K (FP32 FMA, register-tiled: a CTA computes 128 tokens x BE experts, each of its
+// 256 threads an 8 x BE/16 block), the two halves written to the logits and scores
+// buffers.  k_route_rows: one warp per token sums the halves in a fixed order, adds
+// the bias and routes the token (route_token), overwriting both rows.
+constexpr int kRgBT = 128, kRgBK = 16;
 
-template <int EP, int TM>
-__global__ void __launch_bounds__(256) k_router_large(RouteArgs a) {
-  using C = LargeCfg<EP, TM>;
-  extern __shared__ __align__(16) float sm[];
-  float* Xs = sm;                        // [BK][BT]
-  float* Ws = Xs + C::BK * C::BT;        // [BK][EP]
-  float* Ls = Ws + C::BK * EP;           // [BT][LS]
-  int* hist = reinterpret_cast<int*>(Ls + C::BT * C::LS);
-  const int tid = threadIdx.x;
-  const int tr = tid / C::TC, tc = tid % C::TC;
-  const int t0 = blockIdx.x * C::BT;
-  const int H = a.H, E = a.E;
-  for (int i = tid; i < EP; i += 256) hist[i] = 0;
-  float acc[TM][8];
+template <int BE>
+__global__ void __launch_bounds__(256, 2) k_router_gemm(const uint16_t* __restrict__ X, const float* __restrict__ Wr,
+                                                        int T, int H, int E, float* __restrict__ P0,
+                                                        float* __restrict__ P1) {
+  constexpr int BT = kRgBT, BK = kRgBK, NE = BE / 16;
+  constexpr int WV = BE * BK / 4 / 256;  // float4 W vectors per thread per K step
+  __shared__ __align__(16) float Xs[2][BK][BT];
+  __shared__ __align__(16) float Ws[2][BK][BE];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
+  const int half = H / BK / 2 * BK;  // K of the first pass
+  const int kbeg = blockIdx.z ? half : 0, kend = blockIdx.z ? H : half;
+  float* P = blockIdx.z ? P1 : P0;
+  float acc[8][NE];
 #pragma unroll
-  for (int m = 0; m < TM; ++m)
+  for (int m = 0; m < 8; ++m)
 #pragma unroll
-    for (int n = 0; n < 8; ++n) acc[m][n] = 0.f;
-  // Global loads of the next K tile are issued into registers before the current
-  // tile is consumed from shared memory (one tile of lookahead).
-  constexpr int XV = (C::BT * 2 + 255) / 256;   // 16-byte X vectors per thread
-  constexpr int WV = (EP * 4 + 255) / 256;      // float4 W vectors per thread
-  uint4 xr[XV];
+    for (int n = 0; n < NE; ++n) acc[m][n] = 0.f;
+  // loaders: X as 16-byte vectors (8 bf16 along K) of token tid % 128, W as float4
+  // (4 fp32 along K) of expert i % BE
+  const int xt = tid & 127, xh = tid >> 7;
+  const bool xok = t0 + xt < T;
+  uint4 xr;
   float4 wr[WV];
-  auto load_tile = [&](int k0) {
-#pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + 256 * v;
-      const int tt = i >> 1, half = i & 1;
-      xr[v] = make_uint4(0, 0, 0, 0);
-      if (i < C::BT * 2 && t0 + tt < a.T)
-        xr[v] = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + tt) * H + k0) + half);
-    }
+  auto load = [&](int k0) {
+    xr = xok ? __ldg(reinterpret_cast<const uint4*>(X + (size_t)(t0 + xt) * H + k0) + xh) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int v = 0; v < WV; ++v) {
-      const int i = tid + 256 * v;
-      const int e = i % EP, q4 = i / EP;
-      wr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < EP * 4 && e < E) wr[v] = __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)e * H + k0) + q4);
+      const int i = tid + 256 * v, e = i % BE, j = i / BE;
+      wr[v] = e0 + e < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)(e0 + e) * H + k0) + j)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  auto store_tile = [&]() {
+  auto store = [&](int b) {
+    float x[8];
+    unpack8(xr, x);
 #pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + 256 * v;
-      if (i < C::BT * 2) {
-        const int tt = i >> 1, half = i & 1;
-        float x[8];
-        unpack8(xr[v], x);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) Xs[(half * 8 + q) * C::BT + tt] = x[q];
-      }
-    }
+    for (int q = 0; q < 8; ++q) Xs[b][xh * 8 + q][xt] = x[q];
 #pragma unroll
     for (int v = 0; v < WV; ++v) {
-      const int i = tid + 256 * v;
-      if (i < EP * 4) {
-        const int e = i % EP, q4 = i / EP;
-        Ws[(4 * q4 + 0) * EP + e] = wr[v].x;
-        Ws[(4 * q4 + 1) * EP + e] = wr[v].y;
-        Ws[(4 * q4 + 2) * EP + e] = wr[v].z;
-        Ws[(4 * q4 + 3) * EP + e] = wr[v].w;
-      }
+      const int i = tid + 256 * v, e = i % BE, j = i / BE;
+      Ws[b][4 * j + 0][e] = wr[v].x;
+      Ws[b][4 * j + 1][e] = wr[v].y;
+      Ws[b][4 * j + 2][e] = wr[v].z;
+      Ws[b][4 * j + 3][e] = wr[v].w;
     }
   };
-  load_tile(0);
-  for (int k0 = 0; k0 < H; k0 += C::BK) {
-    store_tile();
-    __syncthreads();
-    if (k0 + C::BK < H) load_tile(k0 + C::BK);
+  if (kbeg < kend) {
+    load(kbeg);
+    store(0);
+  }
+  __syncthreads();
+  int b = 0;
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    const bool more = k0 + BK < kend;
+    if (more) load(k0 + BK);
 #pragma unroll
-    for (int kk = 0; kk < C::BK; ++kk) {
-      float xa[TM];
-#pragma unroll
-      for (int m = 0; m < TM; m += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(&Xs[kk * C::BT + tr * TM + m]);
-        xa[m] = v.x;
-        xa[m + 1] = v.y;
-        xa[m + 2] = v.z;
-        xa[m + 3] = v.w;
+    for (int kk = 0; kk < BK; ++kk) {
+      // rows ty*4..+3 and 64+ty*4..+3; columns tx*4..+3 (and 64+tx*4..+3 when BE = 128)
+      const float4 x0 = *reinterpret_cast<const float4*>(&Xs[b][kk][ty * 4]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&Xs[b][kk][64 + ty * 4]);
+      const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      float wb[NE];
+      const float4 w0 = *reinterpret_cast<const float4*>(&Ws[b][kk][tx * 4]);
+      wb[0] = w0.x; wb[1] = w0.y; wb[2] = w0.z; wb[3] = w0.w;
+      if constexpr (NE == 8) {
+        const float4 w1 = *reinterpret_cast<const float4*>(&Ws[b][kk][64 + tx * 4]);
+        wb[4] = w1.x; wb[5] = w1.y; wb[6] = w1.z; wb[7] = w1.w;
       }
-      const float4 b0 = *reinterpret_cast<const float4*>(&Ws[kk * EP + tc * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Ws[kk * EP + tc * 8 + 4]);
-      const float wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int m = 0; m < TM; ++m)
+      for (int m = 0; m < 8; ++m)
 #pragma unroll
-        for (int n = 0; n < 8; ++n) acc[m][n] = fmaf(xa[m], wb[n], acc[m][n]);
+        for (int n = 0; n < NE; ++n) acc[m][n] = fmaf(xa[m], wb[n], acc[m][n]);
     }
+    if (more) store(b ^ 1);
     __syncthreads();
+    b ^= 1;
   }
 #pragma unroll
-  for (int m = 0; m < TM; ++m)
+  for (int m = 0; m < 8; ++m) {
+    const int t = t0 + (m < 4 ? ty * 4 + m : 64 + ty * 4 + m - 4);
+    if (t >= T) continue;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int e = tc * 8 + n;
-      Ls[(tr * TM + m) * C::LS + e] = acc[m][n] + ((a.logit_bias && e < E) ? a.logit_bias[e] : 0.f);
+    for (int h = 0; h < NE / 4; ++h) {
+      const int e = e0 + h * 64 + tx * 4;
+      if (e < E)
+        *reinterpret_cast<float4*>(P + (size_t)t * E + e) =
+            make_float4(acc[m][4 * h], acc[m][4 * h + 1], acc[m][4 * h + 2], acc[m][4 * h + 3]);
     }
+  }
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
+  __shared__ float lrows[8][32 * V];
+  __shared__ int hist[32 * V];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * V; i += 256) hist[i] = 0;
   __syncthreads();
-  const int warp = tid >> 5;
-  for (int tt = warp; tt < C::BT; tt += 8)
-    if (t0 + tt < a.T) route_token<EP / 32>(a, t0 + tt, Ls + tt * C::LS, hist);
+  const int E = a.E;
+  for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
+    // the first half of the product is in logits, the second in scores
+    for (int e = lane; e < E; e += 32)
+      lrows[warp][e] = (a.logits[(size_t)t * E + e] + a.scores[(size_t)t * E + e]) +
+                       (a.logit_bias ? a.logit_bias[e] : 0.f);
+    __syncwarp();
+    route_token<V>(a, t, lrows[warp], hist);
+    __syncwarp();
+  }
   __syncthreads();
-  for (int e = tid; e < E; e += 256)
+  for (int e = threadIdx.x; e < E; e += 256)
     if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
 }
 
-template <int EP, int TM>
-cudaError_t launch_large(const RouteArgs& a, cudaStream_t st) {
-  using C = LargeCfg<EP, TM>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_large<EP, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int grid = (a.T + C::BT - 1) / C::BT;
-  k_router_large<EP, TM><<<grid, 256, C::smem, st>>>(a);
+template <int BE, int V>
+cudaError_t launch_two_pass(const RouteArgs& a, cudaStream_t st, int nsm) {
+  dim3 g1((a.T + kRgBT - 1) / kRgBT, (a.E + BE - 1) / BE, 2);
+  k_router_gemm<BE><<<g1, 256, 0, st>>>(a.X, a.Wr, a.T, a.H, a.E, a.logits, a.scores);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int g2 = (a.T + 7) / 8;
+  g2 = g2 < 2 * nsm ? g2 : 2 * nsm;
+  k_route_rows<V><<<g2, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -696,9 +698,9 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
   // accumulation drifts by about half an ulp per MMA step, ~5e-5 relative over K=3H
   // split terms, which the 1e-5 logit bound does not allow; the backward products,
   // held to bf16-class bounds, do run on the tensor cores.)
-  if (c.E <= 64) return launch_large<64, 4>(a, st);
-  if (c.E <= 128) return launch_large<128, 4>(a, st);
-  return launch_large<256, 4>(a, st);
+  if (c.E <= 64) return launch_two_pass<64, 2>(a, st, nsm);
+  if (c.E <= 128) return launch_two_pass<128, 4>(a, st, nsm);
+  return launch_two_pass<128, 8>(a, st, nsm);
 }
 
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
