@@ -176,8 +176,27 @@ moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, 
                                   const moe_bf16* W13_s, const moe_bf16* W2_s, moe_bf16* GU_s, moe_bf16* A_s,
                                   moe_bf16* Yshared, void* ws, void* stream);
 
+/* Memory-efficient expert MLP (gated rows).  (Summary page, "Method": memory-efficient
+ * permutation and fine-grained activation recomputation are named among the memory
+ * recipes; the pages give no mechanism, so this is a reading.)  The gate of permuted row r,
+ * gates[slot_src[r]] (0 for padding rows), is applied to the activation before FC2:
+ *  A  [R,F] bf16 out       gate * silu(g) * u
+ *  Yperm [R,H] bf16 out    A W2^T, i.e. the gate-weighted expert outputs: combine them with
+ *                          moe_unpermute_combine(gates = NULL).  Yperm is needed by nothing
+ *                          in the backward, and A is recomputed there, so neither has to be
+ *                          kept between the passes.
+ * Other arguments as moe_grouped_swiglu_mlp; slot_src [R] int32 from moe_permute, gates
+ * [T,k] fp32 from the router.  The shared expert (gate 1) is computed as there. */
+moe_status moe_grouped_swiglu_mlp_gated(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                        const int32_t* tile_offsets, const int32_t* slot_src, const float* gates,
+                                        const moe_bf16* W13, const moe_bf16* W2, moe_bf16* GU, moe_bf16* A,
+                                        moe_bf16* Yperm, const moe_bf16* X, const moe_bf16* W13_s,
+                                        const moe_bf16* W2_s, moe_bf16* GU_s, moe_bf16* A_s, moe_bf16* Yshared,
+                                        void* ws, void* stream);
+
 /* Combine.  ("Method": the fourth stage sums each token's gate-weighted expert outputs.)
  *  Y[t] = sum_j gates[t,j] * Yperm[row_id_map[t,j]] (+ Yshared[t]), FP32 sum, one bf16 rounding.
+ *  gates NULL: unit weights (rows already gated by moe_grouped_swiglu_mlp_gated).
  *  Yshared [T,H] bf16 (device, nullable);  Y [T,H] bf16 out. */
 moe_status moe_unpermute_combine(const moe_config* cfg, const moe_bf16* Yperm, const int32_t* row_id_map,
                                  const float* gates, const moe_bf16* Yshared, moe_bf16* Y, void* stream);
@@ -186,7 +205,9 @@ moe_status moe_unpermute_combine(const moe_config* cfg, const moe_bf16* Yperm, c
  *  dYperm[row_id_map[t,j]] = bf16(gates[t,j] * dY[t]); padding rows of dYperm are zeroed
  *    (offsets, counts locate them);
  *  dgates[t,j] = <dY[t], Yperm[row_id_map[t,j]]>, FP32 accumulation.
- *  dYperm [R,H] bf16 out; dgates [T,k] fp32 out. */
+ *  dYperm [R,H] bf16 out; dgates [T,k] fp32 out.
+ *  gates NULL: unit weights; dgates NULL: no gate gradient (Yperm is then not read and may
+ *  be NULL).  The gated path passes both as NULL: dYperm rows are copies of dY. */
 moe_status moe_unpermute_combine_bwd(const moe_config* cfg, const moe_bf16* dY, const moe_bf16* Yperm,
                                      const int32_t* row_id_map, const float* gates, const int32_t* offsets,
                                      const int32_t* counts, moe_bf16* dYperm, float* dgates, void* stream);
@@ -206,6 +227,26 @@ moe_status moe_grouped_swiglu_mlp_bwd(const moe_config* cfg, const moe_bf16* Xpe
                                       const moe_bf16* W13_s, const moe_bf16* W2_s, const moe_bf16* GU_s,
                                       const moe_bf16* A_s, moe_bf16* dGU_s, moe_bf16* dX_shared,
                                       moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws, void* stream);
+
+/* Backward of moe_grouped_swiglu_mlp_gated.  dYperm is the gradient of the gated rows, i.e.
+ * moe_unpermute_combine_bwd(gates = NULL, dgates = NULL).  With a = silu(g) * u recomputed from
+ * the saved GU and gate = gates[slot_src[r]]:
+ *  dA' = dYperm_e W2_e; dgates[t,j] = <dA'[r], a[r]> for r = row_id_map[t,j] (0 if dropped),
+ *  summed over the FC2-dgrad tiles in a fixed order; dA = gate * dA', then dG, dU as above;
+ *  A      [R,F] bf16 out   gate * a, rewritten here for dW2 (scratch: nothing reads it after)
+ *  dW2    = dYperm_e^T A_e; dXperm, dW13 as in moe_grouped_swiglu_mlp_bwd.
+ * counts are required; row_id_map [T,k], slot_src [R] from the dispatch; gates [T,k].
+ * Shared expert: as in moe_grouped_swiglu_mlp_bwd (its A_s is the saved one). */
+moe_status moe_grouped_swiglu_mlp_bwd_gated(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                            const int32_t* tile_offsets, const int32_t* counts,
+                                            const int32_t* slot_src, const int32_t* row_id_map, const float* gates,
+                                            const moe_bf16* W13, const moe_bf16* W2, const moe_bf16* GU,
+                                            const moe_bf16* dYperm, moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* A,
+                                            moe_bf16* dW13, moe_bf16* dW2, float* dgates, const moe_bf16* X,
+                                            const moe_bf16* dY, const moe_bf16* W13_s, const moe_bf16* W2_s,
+                                            const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                            moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws,
+                                            void* stream);
 
 /* Backward of the router.  dlogits = exact gradient of the gates w.r.t. the
  * logits for the fixed selection (zero for unselected experts when renorm=1);

@@ -26,14 +26,16 @@ from . import build as _build
 __all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
     "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd", "moe_router_topk_bwd", "moe_permute_bwd",
-    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc", "moe_permute_capacity"]
+    "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc", "moe_permute_capacity",
+    "moe_grouped_swiglu_mlp_gated", "moe_grouped_swiglu_mlp_bwd_gated"]
 
 EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_workspace_init",
             "moe_read_device_error", "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp",
             "moe_unpermute_combine", "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd",
             "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc", "moe_fp8_workspace_size",
             "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8",
-            "moe_router_replay", "moe_permute_capacity"]
+            "moe_router_replay", "moe_permute_capacity", "moe_grouped_swiglu_mlp_gated",
+            "moe_grouped_swiglu_mlp_bwd_gated"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -79,6 +81,8 @@ def load(build: bool = True):
                 "moe_permute_noalloc": [cfgp] + [vp] * 9,
                 "moe_router_replay": [cfgp] + [vp] * 11,
                 "moe_permute_capacity": [cfgp, vp, vp, vp, ctypes.c_int32] + [vp] * 9,
+                "moe_grouped_swiglu_mlp_gated": [cfgp] + [vp] * 18,
+                "moe_grouped_swiglu_mlp_bwd_gated": [cfgp] + [vp] * 29,
                 "moe_fp8_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t)],
                 "moe_quantize_weights_fp8": [cfgp] + [vp] * 13,
                 "moe_grouped_swiglu_mlp_fp8": [cfgp] + [vp] * 20,
@@ -208,6 +212,27 @@ def moe_grouped_swiglu_mlp(cfg, Xperm, offsets, tile_offsets, W13, W2, GU, A, Yp
                                                       W2_s, GU_s, A_s, Yshared, ws)), _stream(stream))
 
 
+def moe_grouped_swiglu_mlp_gated(cfg, Xperm, offsets, tile_offsets, slot_src, gates, W13, W2, GU, A, Yperm, X=None,
+                                 W13_s=None, W2_s=None, GU_s=None, A_s=None, Yshared=None, ws=None, stream=None):
+    """The expert MLP with each permuted row's gate applied before FC2 (A and Yperm are
+    gated); combine with gates=None."""
+    ts = (Xperm, offsets, tile_offsets, slot_src, gates, W13, W2, GU, A, Yperm, X, W13_s, W2_s, GU_s, A_s, Yshared,
+          ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_gated", cfg, *map(_ptr, ts), _stream(stream))
+
+
+def moe_grouped_swiglu_mlp_bwd_gated(cfg, Xperm, offsets, tile_offsets, counts, slot_src, row_id_map, gates, W13, W2,
+                                     GU, dYperm, dGU, dXperm, A, dW13, dW2, dgates, X=None, dY=None, W13_s=None,
+                                     W2_s=None, GU_s=None, A_s=None, dGU_s=None, dX_shared=None, dW13_s=None,
+                                     dW2_s=None, ws=None, stream=None):
+    """Backward of the gated MLP: recomputes the activations from GU into A and writes dgates."""
+    ts = (Xperm, offsets, tile_offsets, counts, slot_src, row_id_map, gates, W13, W2, GU, dYperm, dGU, dXperm, A,
+          dW13, dW2, dgates, X, dY, W13_s, W2_s, GU_s, A_s, dGU_s, dX_shared, dW13_s, dW2_s, ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_bwd_gated", cfg, *map(_ptr, ts), _stream(stream))
+
+
 def moe_unpermute_combine(cfg, Yperm, row_id_map, gates, Yshared, Y, stream=None):
     _dev(Yperm, row_id_map, gates, Yshared, Y)
     _call("moe_unpermute_combine", cfg, *map(_ptr, (Yperm, row_id_map, gates, Yshared, Y)), _stream(stream))
@@ -292,10 +317,13 @@ class MoELayer:
     """
 
     def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda", fp8: bool = False,
-                 capacity: int | None = None, drop_by_gate: bool = False):
+                 capacity: int | None = None, drop_by_gate: bool = False, memory_efficient: bool = False):
+        if memory_efficient and fp8:
+            raise ValueError("the memory-efficient path is built for the bf16 expert GEMMs")
         self.cfg = cfg
         self.w = weights
         self.fp8 = fp8
+        self.memory_efficient = memory_efficient
         self.capacity = capacity
         self.drop_by_gate = drop_by_gate
         T, H, E, k, F, Fs = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F, cfg.F_shared
@@ -354,6 +382,12 @@ class MoELayer:
             moe_permute_capacity(c, X, self.topk_idx, self.counts, self.capacity,
                                  self.gates if self.drop_by_gate else None, self.seg_counts, self.offsets,
                                  self.tile_offsets, self.row_id_map, self.slot_src, self.Xperm, self.ws)
+        if self.memory_efficient:
+            moe_grouped_swiglu_mlp_gated(c, self.Xperm, self.offsets, self.tile_offsets, self.slot_src, self.gates,
+                                         w.W13, w.W2, self.GU, self.A, self.Yperm, X if c.F_shared else None,
+                                         w.W13_s, w.W2_s, self.GU_s, self.A_s, self.Yshared, self.ws)
+            moe_unpermute_combine(c, self.Yperm, self.row_id_map, None, self.Yshared, self.Y)
+            return self.Y
         if self.fp8:
             self.quantize_weights()
             moe_grouped_swiglu_mlp_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.W13q, self.W13sc,
@@ -370,9 +404,23 @@ class MoELayer:
     def backward(self, dY: torch.Tensor) -> torch.Tensor:
         c, w = self.cfg, self.w
         self.dY = dY
+        sh = c.F_shared > 0
+        if self.memory_efficient:
+            moe_unpermute_combine_bwd(c, dY, None, self.row_id_map, None, self.offsets, self.seg_counts,
+                                      self.dYperm, None)
+            moe_grouped_swiglu_mlp_bwd_gated(c, self.Xperm, self.offsets, self.tile_offsets, self.seg_counts,
+                                             self.slot_src, self.row_id_map, self.gates, w.W13, w.W2, self.GU,
+                                             self.dYperm, self.dGU, self.dXperm, self.A, self.dW13, self.dW2,
+                                             self.dgates, self.X if sh else None, dY if sh else None, w.W13_s,
+                                             w.W2_s, self.GU_s, self.A_s, self.dGU_s, self.dX_shared, self.dW13_s,
+                                             self.dW2_s, self.ws)
+            moe_router_topk_bwd(c, self.X, w.W_r, self.logits, self.scores, self.topk_idx, self.gates, self.dgates,
+                                self.dW_r, self.dlogit_bias if w.logit_bias is not None else None, self.dX_router,
+                                self.ws)
+            moe_permute_bwd(c, self.dXperm, self.row_id_map, self.dX_router, self.dX_shared, self.dX)
+            return self.dX
         moe_unpermute_combine_bwd(c, dY, self.Yperm, self.row_id_map, self.gates, self.offsets, self.seg_counts,
                                   self.dYperm, self.dgates)
-        sh = c.F_shared > 0
         if self.fp8:
             moe_grouped_swiglu_mlp_bwd_fp8(c, self.Xperm, self.offsets, self.tile_offsets, self.seg_counts, self.W13q,
                                            self.W13sc, self.W2q, self.W2sc, self.GU, self.A, self.dYperm, self.dGU,

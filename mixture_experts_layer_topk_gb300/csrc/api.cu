@@ -294,11 +294,49 @@ moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, 
   return MOE_OK;
 }
 
+moe_status moe_grouped_swiglu_mlp_gated(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                        const int32_t* tile_offsets, const int32_t* slot_src, const float* gates,
+                                        const moe_bf16* W13, const moe_bf16* W2, moe_bf16* GU, moe_bf16* A,
+                                        moe_bf16* Yperm, const moe_bf16* X, const moe_bf16* W13_s,
+                                        const moe_bf16* W2_s, moe_bf16* GU_s, moe_bf16* A_s, moe_bf16* Yshared,
+                                        void* ws, void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!slot_src || !tok_ok(cfg, gates)) return MOE_ERR_INVALID_ARG;
+  // the argument checks and the shared expert are those of the plain call, which runs
+  // after the gated routed pass below
+  if (!Xperm || !offsets || !tile_offsets || !W13 || !W2 || !GU || !A || !Yperm) return MOE_ERR_INVALID_ARG;
+  const void* al[] = {Xperm, W13, W2, GU, A, Yperm};
+  for (const void* p : al)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0) {
+    if (!tok_ok(cfg, X) || !W13_s || !W2_s || !tok_ok(cfg, GU_s) || !tok_ok(cfg, A_s) || !tok_ok(cfg, Yshared))
+      return MOE_ERR_INVALID_ARG;
+    const void* al2[] = {X, W13_s, W2_s, GU_s, A_s, Yshared};
+    for (const void* p : al2)
+      if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int* err = err_word(ws, *cfg);
+  const GemmShape rs = routed_shape(*cfg, offsets, tile_offsets, nullptr);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  const Gating gt{slot_src, gates, nullptr, nullptr};
+  MOE_TRY(launch_fc1_fwd(rs, Xperm, W13, GU, A, err, st, &gt));
+  MOE_TRY(launch_fc2_fwd(rs, A, W2, Yperm, err, st));
+  if (cfg->F_shared > 0 && cfg->T > 0) {
+    const GemmShape ss = shared_shape(*cfg);
+    MOE_TRY(launch_fc1_fwd(ss, X, W13_s, GU_s, A_s, err, st));
+    MOE_TRY(launch_fc2_fwd(ss, A_s, W2_s, Yshared, err, st));
+  }
+  return MOE_OK;
+}
+
 moe_status moe_unpermute_combine(const moe_config* cfg, const moe_bf16* Yperm, const int32_t* row_id_map,
                                  const float* gates, const moe_bf16* Yshared, moe_bf16* Y, void* stream) {
   moe_status s = check_cfg(cfg, false);
   if (s != MOE_OK) return s;
-  if (!Yperm || !tok_ok(cfg, row_id_map) || !tok_ok(cfg, gates) || !tok_ok(cfg, Y)) return MOE_ERR_INVALID_ARG;
+  if (!Yperm || !tok_ok(cfg, row_id_map) || !tok_ok(cfg, Y)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(Yperm) || !aligned16(Y) || (Yshared && !aligned16(Yshared))) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_combine(*cfg, Yperm, row_id_map, gates, Yshared, Y, (cudaStream_t)stream));
 }
@@ -308,10 +346,9 @@ moe_status moe_unpermute_combine_bwd(const moe_config* cfg, const moe_bf16* dY, 
                                      const int32_t* counts, moe_bf16* dYperm, float* dgates, void* stream) {
   moe_status s = check_cfg(cfg, false);
   if (s != MOE_OK) return s;
-  if (!tok_ok(cfg, dY) || !Yperm || !tok_ok(cfg, row_id_map) || !tok_ok(cfg, gates) || !offsets || !counts ||
-      !dYperm || !tok_ok(cfg, dgates))
+  if (!tok_ok(cfg, dY) || (dgates && !Yperm) || !tok_ok(cfg, row_id_map) || !offsets || !counts || !dYperm)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dY) || !aligned16(Yperm) || !aligned16(dYperm)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dY) || (Yperm && !aligned16(Yperm)) || !aligned16(dYperm)) return MOE_ERR_INVALID_ARG;
   return cuda_status(
       launch_combine_bwd(*cfg, dY, Yperm, row_id_map, gates, offsets, counts, dYperm, dgates, (cudaStream_t)stream));
 }
@@ -346,6 +383,62 @@ moe_status moe_grouped_swiglu_mlp_bwd(const moe_config* cfg, const moe_bf16* Xpe
   const GemmShape rs = routed_shape(*cfg, offsets, tile_offsets, counts);
   if (rs.nsm <= 0) return MOE_ERR_CUDA;
   MOE_TRY(launch_fc2_dgrad(rs, dYperm, W2, GU, dGU, err, st));
+  MOE_TRY(launch_fc2_wgrad(rs, dYperm, A, dW2, err, st));
+  MOE_TRY(launch_fc1_dgrad(rs, dGU, W13, dXperm, err, st));
+  MOE_TRY(launch_fc1_wgrad(rs, dGU, Xperm, dW13, err, st));
+  if (cfg->F_shared > 0) {
+    if (cfg->T == 0) {
+      MOE_TRY(cudaMemsetAsync(dW13_s, 0, sizeof(moe_bf16) * 2 * cfg->F_shared * cfg->H, st));
+      MOE_TRY(cudaMemsetAsync(dW2_s, 0, sizeof(moe_bf16) * cfg->F_shared * cfg->H, st));
+      return MOE_OK;
+    }
+    const GemmShape ss = shared_shape(*cfg);
+    MOE_TRY(launch_fc2_dgrad(ss, dY, W2_s, GU_s, dGU_s, err, st));
+    MOE_TRY(launch_fc2_wgrad(ss, dY, A_s, dW2_s, err, st));
+    MOE_TRY(launch_fc1_dgrad(ss, dGU_s, W13_s, dX_shared, err, st));
+    MOE_TRY(launch_fc1_wgrad(ss, dGU_s, X, dW13_s, err, st));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_grouped_swiglu_mlp_bwd_gated(const moe_config* cfg, const moe_bf16* Xperm, const int32_t* offsets,
+                                            const int32_t* tile_offsets, const int32_t* counts,
+                                            const int32_t* slot_src, const int32_t* row_id_map, const float* gates,
+                                            const moe_bf16* W13, const moe_bf16* W2, const moe_bf16* GU,
+                                            const moe_bf16* dYperm, moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* A,
+                                            moe_bf16* dW13, moe_bf16* dW2, float* dgates, const moe_bf16* X,
+                                            const moe_bf16* dY, const moe_bf16* W13_s, const moe_bf16* W2_s,
+                                            const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                            moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws,
+                                            void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (!slot_src || !tok_ok(cfg, row_id_map) || !tok_ok(cfg, gates) || !tok_ok(cfg, dgates))
+    return MOE_ERR_INVALID_ARG;
+  if (!Xperm || !offsets || !tile_offsets || !counts || !W13 || !W2 || !GU || !A || !dYperm || !dGU || !dXperm ||
+      !dW13 || !dW2)
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {Xperm, W13, W2, GU, A, dYperm, dGU, dXperm, dW13, dW2};
+  for (const void* p : al)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0) {
+    if (!tok_ok(cfg, X) || !tok_ok(cfg, dY) || !W13_s || !W2_s || !tok_ok(cfg, GU_s) || !tok_ok(cfg, A_s) ||
+        !tok_ok(cfg, dGU_s) || !tok_ok(cfg, dX_shared) || !dW13_s || !dW2_s)
+      return MOE_ERR_INVALID_ARG;
+    const void* al2[] = {X, dY, W13_s, W2_s, GU_s, A_s, dGU_s, dX_shared, dW13_s, dW2_s};
+    for (const void* p : al2)
+      if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*cfg);
+  int* err = ws_ptr<int>(ws, L.err);
+  const GemmShape rs = routed_shape(*cfg, offsets, tile_offsets, counts);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  float* part = ws_ptr<float>(ws, L.dg_part);
+  const Gating gt{slot_src, gates, part, A};
+  MOE_TRY(launch_fc2_dgrad(rs, dYperm, W2, GU, dGU, err, st, &gt));
+  MOE_TRY(launch_dgates_reduce(*cfg, row_id_map, part, cfg->F / fc2_dgrad_tile_n(cfg->F), dgates, rs.nsm, st));
   MOE_TRY(launch_fc2_wgrad(rs, dYperm, A, dW2, err, st));
   MOE_TRY(launch_fc1_dgrad(rs, dGU, W13, dXperm, err, st));
   MOE_TRY(launch_fc1_wgrad(rs, dGU, Xperm, dW13, err, st));

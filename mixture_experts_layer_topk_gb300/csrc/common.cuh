@@ -29,6 +29,8 @@ struct WsLayout {
   // capacity dropping by priority: assignments grouped by expert in token order
   size_t drop_order;    // int32[T * k]
   size_t drop_start;    // int32[E + 1] segment starts of drop_order
+  // gated path: per-row, per-FC2-dgrad-tile partials of the gate gradient
+  size_t dg_part;       // float[(T*k + E*(align-1)) * F/128]
   size_t total;
 };
 
@@ -80,6 +82,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + (size_t)c.T * c.k * sizeof(int32_t));
   L.drop_start = o;
   o = align256(o + (size_t)(c.E + 1) * sizeof(int32_t));
+  L.dg_part = o;
+  o = align256(o + ((size_t)c.T * c.k + (size_t)c.E * (c.align - 1)) * (size_t)(c.F / 128) * sizeof(float));
   L.total = o;
   return L;
 }

@@ -76,6 +76,16 @@ struct GemmArgs {
   int kwrap;                // K-major A (FWD/DGRAD): the K coordinate wraps modulo kwrap;
                             // WGRAD: B's row coordinate wraps modulo kwrap (0: no wrap)
   int n_fast;               // WGRAD: tiles walk N fastest (else M fastest) within an expert
+  // gated rows (the memory-efficient path): row r carries gate gates[slot_src[r]], 0 for
+  // a padding row.  SWIGLU: the activation output is gate * silu(g) * u.  DSWIGLU: the
+  // accumulator is the gradient of the gated activation; the epilogue recomputes
+  // a = silu(g) * u from GU, writes gate * a to a_out, the per-tile partial of
+  // <accumulator row, a> to dg_part[row * n_tiles + tile], and backpropagates gate * acc.
+  const int32_t* slot_src;
+  const float* gates;
+  float* dg_part;
+  uint16_t* a_out;
+  int64_t lda_out;
   // FP8 block scales (UE8M0 bytes): A and B, addressed per mode (see the SF warps)
   const uint8_t* sfa;
   int64_t sfa_ld;
@@ -564,6 +574,11 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool valid = tl.valid && (g.dense_rows <= 0 || MODE == MODE_WGRAD || row < g.dense_rows);
+      float rg = 1.0f;  // the row's gate on the gated path
+      if (EPI != EPI_STORE && EPI != EPI_F32 && g.gates && valid) {
+        const int sr = g.slot_src[row];
+        rg = sr >= 0 ? g.gates[sr] : 0.0f;
+      }
       if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -578,7 +593,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
               gv[i] = __uint_as_float(gr[i]);
               uv[i] = __uint_as_float(ur[i]);
               // silu(g) * u with the fast reciprocal (outputs are bf16; exp(-g) = inf gives 0)
-              av[i] = __fdividef(gv[i], 1.0f + __expf(-gv[i])) * uv[i];
+              av[i] = rg * (__fdividef(gv[i], 1.0f + __expf(-gv[i])) * uv[i]);
             }
             const int col = tl.n0 + c * 32;
             store32(g.D + row * g.ldd + col, gv);
@@ -590,6 +605,8 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         __syncwarp();
         if (lane == 0) release(acc);
       } else if constexpr (EPI == EPI_DSWIGLU) {
+        const bool gated = g.gates != nullptr;
+        float dot = 0.0f;  // gated: <accumulator row, silu(g) * u> over this tile's columns
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t dr[32];
@@ -605,6 +622,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           if (valid) {
             const uint4* gp = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + col);
             const uint4* up = reinterpret_cast<const uint4*>(g.GU + row * g.ldgu + g.F + col);
+            float ag[32];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float gf[8], uf[8];
@@ -612,13 +630,18 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
               unpack8(up[v], uf);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float da = __uint_as_float(dr[8 * v + i]);
+                const float acc_v = __uint_as_float(dr[8 * v + i]);
                 const float s = __fdividef(1.0f, 1.0f + __expf(-gf[i]));  // sigmoid, fast reciprocal
                 const float sl = gf[i] * s;
+                const float a = sl * uf[i];
+                dot = fmaf(acc_v, a, dot);
+                ag[8 * v + i] = rg * a;
+                const float da = rg * acc_v;
                 dg[8 * v + i] = da * uf[i] * (s * (1.0f + gf[i] * (1.0f - s)));
                 du[8 * v + i] = da * sl;
               }
             }
+            if (gated) store32(g.a_out + row * g.lda_out + col, ag);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;
@@ -629,6 +652,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           const int hx[2] = {0, 1}, xs[2] = {col, g.F + col};
           publish(2, hx, xs, tl.m0, 0, tl.valid);
         }
+        if (gated && valid) g.dg_part[row * g.n_tiles + tl.n0 / BN] = dot;
       } else {
         int nch = BN / 32;
         if (g.n_valid > 0) {
@@ -866,9 +890,11 @@ inline int pair_tiles(const GemmShape& s, int n_tiles) {
 
 }  // namespace
 
+int fc2_dgrad_tile_n(int F) { return pick_bn(F); }
+
 // X1 = rows of A [rows, K] (Xperm or X), W13 [E, 2F, K]: GU [rows, 2F], A [rows, F].
 cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
-                           int* err, cudaStream_t st) {
+                           int* err, cudaStream_t st, const Gating* gate) {
   CUtensorMap ma, mb;
   if (!map2d(&ma, X1, s.H, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 128))
     return cudaErrorInvalidValue;
@@ -876,6 +902,10 @@ cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = GU; g.ldd = 2 * (int64_t)s.F; g.D2 = Aact; g.ldd2 = s.F; g.F = s.F; g.err = err;
+  if (gate) {
+    g.slot_src = gate->slot_src;
+    g.gates = gate->gates;
+  }
   if (use_pairs()) return launch<MODE_FWD, EPI_SWIGLU, 256, false, true>(ma, mb, ma, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, ma, g, s.max_mtiles * g.n_tiles, s.nsm, st);
 }
@@ -900,7 +930,7 @@ cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint1
 
 // dY [rows, H], W2 [E, H, F], GU [rows, 2F]: dGU [rows, 2F].
 cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
-                             uint16_t* dGU, int* err, cudaStream_t st) {
+                             uint16_t* dGU, int* err, cudaStream_t st, const Gating* gate) {
   const int bn = pick_bn(s.F);
   CUtensorMap ma, mb, md;
   if (!map2d(&ma, dYp, s.H, s.rows, 64, 128) || !map3d(&mb, W2, s.F, s.H, s.E, 64, 64) ||
@@ -910,6 +940,13 @@ cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / bn; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dGU; g.ldd = 2 * (int64_t)s.F; g.GU = GU; g.ldgu = 2 * (int64_t)s.F; g.F = s.F; g.err = err;
+  if (gate) {
+    g.slot_src = gate->slot_src;
+    g.gates = gate->gates;
+    g.dg_part = gate->dg_part;
+    g.a_out = gate->a_out;
+    g.lda_out = s.F;
+  }
   if (bn == 256 && use_pairs())
     return launch<MODE_DGRAD, EPI_DSWIGLU, 256, false, true>(ma, mb, md, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return bn == 256 ? launch<MODE_DGRAD, EPI_DSWIGLU, 256>(ma, mb, md, g, s.max_mtiles * g.n_tiles, s.nsm, st)

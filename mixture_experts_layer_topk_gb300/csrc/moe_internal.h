@@ -57,15 +57,32 @@ cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int
 cudaError_t launch_combine_bwd(const moe_config& c, const uint16_t* dY, const uint16_t* Yperm,
                                const int32_t* row_id_map, const float* gates, const int32_t* offsets,
                                const int32_t* counts, uint16_t* dYperm, float* dgates, cudaStream_t st);
+cudaError_t launch_dgates_reduce(const moe_config& c, const int32_t* row_id_map, const float* part, int ntile,
+                                 float* dgates, int nsm, cudaStream_t st);
 cudaError_t launch_permute_bwd(const moe_config& c, const uint16_t* dXperm, const int32_t* row_id_map,
                                const float* dXr, const uint16_t* dXs, uint16_t* dX, cudaStream_t st);
 
+// The memory-efficient (gated) path: row r of the permuted buffers carries gate
+// gates[slot_src[r]] (0 for padding rows).  FC1's epilogue then writes the gated
+// activation gate * silu(g) * u; FC2-dgrad's epilogue takes the gradient of the gated
+// activation, recomputes a = silu(g) * u from GU, writes gate * a to a_out [rows, F]
+// (for FC2's wgrad) and per-tile partials of the gate gradient to dg_part
+// [rows, F / tile width].
+struct Gating {
+  const int32_t* slot_src;
+  const float* gates;
+  float* dg_part;
+  uint16_t* a_out;
+};
+
 cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
-                           int* err, cudaStream_t st);
+                           int* err, cudaStream_t st, const Gating* gate = nullptr);
 cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
                            cudaStream_t st);
 cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
-                             uint16_t* dGU, int* err, cudaStream_t st);
+                             uint16_t* dGU, int* err, cudaStream_t st, const Gating* gate = nullptr);
+// columns of one FC2-dgrad tile (the dg_part row length is F / this)
+int fc2_dgrad_tile_n(int F);
 cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* W13, uint16_t* dX1, int* err,
                              cudaStream_t st);
 cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* Aact, uint16_t* dW2, int* err,

@@ -33,6 +33,9 @@ namespace moe {
 
 namespace {
 
+// 16-byte vectors per lane per source row that the gather kernels load before using any
+constexpr int kGatherUnroll = 4;
+
 // Per-chunk expert histogram: chunk_counts[c][e].
 __global__ void __launch_bounds__(256) k_chunk_hist(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                                                     int32_t* __restrict__ chunk_counts) {
@@ -308,44 +311,63 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ 
 }
 
 // Y[t] = sum_j g[t,j] Yperm[row_id_map[t,j]] (+ Yshared[t]); one warp per token.
+// gates == nullptr: unit weights (the rows are gated already).
 __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ Yperm,
                                                  const int32_t* __restrict__ row_id_map,
                                                  const float* __restrict__ gates, const uint16_t* __restrict__ Ysh,
                                                  uint16_t* __restrict__ Y, int T, int H, int k) {
+  constexpr int U = kGatherUnroll;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : 0;
-  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.f;
+  const float my_g = lane < k ? (gates ? gates[(size_t)t * k + lane] : 1.0f) : 0.f;
   const int nvec = H / 8;
-  // every lane runs every iteration (the shuffles need the full warp)
-  for (int v0 = 0; v0 < nvec; v0 += 32) {
-    const int v = v0 + lane;
-    const bool ok = v < nvec;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // U vectors per lane per source row are loaded before any is used; every lane runs
+  // every iteration (the shuffles need the full warp)
+  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
     for (int j = 0; j < k; ++j) {
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);
       const float g = __shfl_sync(0xffffffffu, my_g, j);
-      if (!ok || slot < 0) continue;
-      const uint4 y = __ldg(reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H) + v);
-      float f[8];
-      unpack8(y, f);
+      if (slot < 0) continue;  // the same for the whole warp
+      const uint4* src = reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H);
+      uint4 y[U];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, f[q], acc[q]);
-    }
-    if (!ok) continue;
-    if (Ysh) {
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(Ysh + (size_t)t * H) + v), f);
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        y[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      for (int u = 0; u < U; ++u) {
+        float f[8];
+        unpack8(y[u], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] = fmaf(g, f[q], acc[u][q]);
+      }
     }
-    reinterpret_cast<uint4*>(Y + (size_t)t * H)[v] = pack8(acc);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u + lane;
+      if (v >= nvec) continue;
+      if (Ysh) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(Ysh + (size_t)t * H) + v), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+      }
+      reinterpret_cast<uint4*>(Y + (size_t)t * H)[v] = pack8(acc[u]);
+    }
   }
 }
 
 // dYperm[slot] = bf16(g dY[t]); dgates[t,j] = <dY[t], Yperm[slot]>.
 // CTAs past the token range zero the padding rows, kPadSplit CTAs per expert.
+// gates == nullptr: g = 1 (gated rows); dgates == nullptr: no gate gradient.
 __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict__ dY,
                                                      const uint16_t* __restrict__ Yperm,
                                                      const int32_t* __restrict__ row_id_map,
@@ -370,28 +392,51 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict_
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : 0;
-  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.f;
+  const float my_g = lane < k ? (gates ? gates[(size_t)t * k + lane] : 1.0f) : 0.f;
+  constexpr int U = kGatherUnroll;
   float my_dot = 0.f;
+  const uint4* dyr = reinterpret_cast<const uint4*>(dY + (size_t)t * H);
   for (int j = 0; j < k; ++j) {
     const int slot = __shfl_sync(0xffffffffu, my_slot, j);
     const float g = __shfl_sync(0xffffffffu, my_g, j);
     float dot = 0.f;
-    for (int v = lane; v < nvec && slot >= 0; v += 32) {
-      float dy[8], y[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dY + (size_t)t * H) + v), dy);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H) + v), y);
-      float o[8];
+    if (slot >= 0) {  // the same for the whole warp
+      const uint4* yr = reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H);
+      uint4* outr = reinterpret_cast<uint4*>(dYperm + (size_t)slot * H);
+      for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+        uint4 dy[U], y[U];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        dot = fmaf(dy[q], y[q], dot);
-        o[q] = g * dy[q];
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + 32 * u + lane;
+          dy[u] = v < nvec ? __ldg(dyr + v) : make_uint4(0, 0, 0, 0);
+          y[u] = dgates && v < nvec ? __ldg(yr + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + 32 * u + lane;
+          if (v >= nvec) continue;
+          if (dgates || g != 1.0f) {
+            float df[8], yf[8], o[8];
+            unpack8(dy[u], df);
+            unpack8(y[u], yf);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dot = fmaf(df[q], yf[q], dot);
+              o[q] = g * df[q];
+            }
+            outr[v] = pack8(o);
+          } else {
+            outr[v] = dy[u];  // a unit gate: the row is a copy
+          }
+        }
       }
-      reinterpret_cast<uint4*>(dYperm + (size_t)slot * H)[v] = pack8(o);
     }
-    dot = warp_sum(dot);
-    if (lane == j) my_dot = dot;
+    if (dgates) {
+      dot = warp_sum(dot);
+      if (lane == j) my_dot = dot;
+    }
   }
-  if (lane < k) dgates[(size_t)t * k + lane] = my_dot;
+  if (dgates && lane < k) dgates[(size_t)t * k + lane] = my_dot;
 }
 
 // dX[t] = sum_j dXperm[row_id_map[t,j]] + dX_router[t] + dX_shared[t].
@@ -399,41 +444,82 @@ __global__ void __launch_bounds__(256) k_permute_bwd(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ row_id_map,
                                                      const float* __restrict__ dXr, const uint16_t* __restrict__ dXs,
                                                      uint16_t* __restrict__ dX, int T, int H, int k) {
+  constexpr int U = kGatherUnroll;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : 0;
   const int nvec = H / 8;
-  for (int v0 = 0; v0 < nvec; v0 += 32) {
-    const int v = v0 + lane;
-    const bool ok = v < nvec;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
     for (int j = 0; j < k; ++j) {
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      if (!ok || slot < 0) continue;
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dXperm + (size_t)slot * H) + v), f);
+      if (slot < 0) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(dXperm + (size_t)slot * H);
+      uint4 x[U];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
-    }
-    if (!ok) continue;
-    if (dXr) {
-      const float4* r = reinterpret_cast<const float4*>(dXr + (size_t)t * H) + 2 * v;
-      const float4 a = __ldg(r), b = __ldg(r + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-    }
-    if (dXs) {
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dXs + (size_t)t * H) + v), f);
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        x[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      for (int u = 0; u < U; ++u) {
+        float f[8];
+        unpack8(x[u], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+      }
     }
-    reinterpret_cast<uint4*>(dX + (size_t)t * H)[v] = pack8(acc);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u + lane;
+      if (v >= nvec) continue;
+      if (dXr) {
+        const float4* rr = reinterpret_cast<const float4*>(dXr + (size_t)t * H) + 2 * v;
+        const float4 a = __ldg(rr), b = __ldg(rr + 1);
+        acc[u][0] += a.x; acc[u][1] += a.y; acc[u][2] += a.z; acc[u][3] += a.w;
+        acc[u][4] += b.x; acc[u][5] += b.y; acc[u][6] += b.z; acc[u][7] += b.w;
+      }
+      if (dXs) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dXs + (size_t)t * H) + v), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+      }
+      reinterpret_cast<uint4*>(dX + (size_t)t * H)[v] = pack8(acc[u]);
+    }
+  }
+}
+
+// Gated path: dgates[t,j] = sum over n of part[row][n] (fixed order), row =
+// row_id_map[t,j]; 0 for a dropped assignment.
+__global__ void __launch_bounds__(256) k_dgates_reduce(const int32_t* __restrict__ row_id_map,
+                                                       const float* __restrict__ part, int ntile, int64_t n,
+                                                       float* __restrict__ dgates) {
+  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int row = row_id_map[i];
+    float s = 0.f;
+    if (row >= 0)
+      for (int c = 0; c < ntile; ++c) s += part[(int64_t)row * ntile + c];
+    dgates[i] = s;
   }
 }
 
 }  // namespace
+
+cudaError_t launch_dgates_reduce(const moe_config& c, const int32_t* row_id_map, const float* part, int ntile,
+                                 float* dgates, int nsm, cudaStream_t st) {
+  const int64_t n = (int64_t)c.T * c.k;
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4LL * nsm) blocks = 4LL * nsm;
+  k_dgates_reduce<<<(int)blocks, 256, 0, st>>>(row_id_map, part, ntile, n, dgates);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
                            int cap, const float* priority, int32_t* kept, int32_t* offsets, int32_t* tile_offsets,

@@ -32,7 +32,7 @@ class OraCfg(ctypes.Structure):
                 ("gate_scale", ctypes.c_double), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("group_score", ctypes.c_int32),
                 ("align", ctypes.c_int32), ("BM", ctypes.c_int32), ("mirror", ctypes.c_int32),
-                ("nthreads", ctypes.c_int32), ("fp8", ctypes.c_int32)]
+                ("nthreads", ctypes.c_int32), ("fp8", ctypes.c_int32), ("gated", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -56,11 +56,14 @@ def _load():
 
 
 def cfg(w, mirror: bool = True, align: int = 128, BM: int = 128, nthreads: int = 0,
-        group_score: int = 0, fp8: bool | None = None) -> OraCfg:
-    """Oracle configuration from a moe_synth.Workload (fp8 defaults to the workload's flag)."""
+        group_score: int = 0, fp8: bool | None = None, gated: bool = False) -> OraCfg:
+    """Oracle configuration from a moe_synth.Workload (fp8 defaults to the workload's flag).
+    gated: routed experts take their gate before the down projection (the memory-efficient
+    path's form of the same function; it only moves the mirror-mode roundings)."""
     f8 = getattr(w, "fp8", False) if fp8 is None else fp8
     return OraCfg(w.T, w.H, w.E, w.k, w.F, w.F_shared, w.score_fn, w.renorm, float(w.gate_scale),
-                  w.n_group, w.topk_group, group_score, align, BM, 1 if mirror else 0, nthreads, 1 if f8 else 0)
+                  w.n_group, w.topk_group, group_score, align, BM, 1 if mirror else 0, nthreads, 1 if f8 else 0,
+                  1 if gated else 0)
 
 
 def _p(a):
@@ -221,13 +224,13 @@ def round_bf16(x):
 
 
 def full_layer(w, inp: dict, mirror: bool = True, sel_scores=None, nthreads: int = 0, capacity=None,
-               drop_by_gate: bool = False):
+               drop_by_gate: bool = False, gated: bool = False):
     """Whole-layer forward and backward for every token and every expert (small cases).
 
     sel_scores: optional (logits_f32, scores_f32) from another implementation;
     when given, the selection runs on them in float32 (identical-scores rule).
     """
-    c = cfg(w, mirror=mirror, nthreads=nthreads)
+    c = cfg(w, mirror=mirror, nthreads=nthreads, gated=gated)
     if c.fp8:
         inp = fp8_inputs(inp)
     logits, scores = router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))

@@ -32,6 +32,14 @@
 // path stores bf16 tensors (GU, A, Yperm, Y, dYperm, dGU, dXperm, dX, dW) and
 // nowhere else; in "pure" mode nothing is rounded (for finite differences).
 //
+// "Gated" mode (the memory-efficient path: summary page, "Method", memory recipes)
+// computes the same function with each routed expert's gate applied to its
+// activation before the down projection, so the expert output is already gate-
+// weighted and the gate gradient is <dA', a> with dA' = W2^T dY and a = silu(g) u
+// recomputed from the stored g, u.  In pure mode it equals the plain layer up to
+// rounding; in mirror mode it rounds where that path stores bf16 (A' = g a, the
+// gated expert output, the recomputed g a for dW2).
+//
 // The dispatch maps are built by a plain stable counting sort over tokens in
 // increasing order, which the GPU path does not use.
 //
@@ -62,6 +70,7 @@ typedef struct {
   int32_t mirror;      // 1: round to bf16 where the GPU stores bf16; 0: pure double
   int32_t nthreads;    // 0: all host cores
   int32_t fp8;         // 1: every expert GEMM operand passes through FP8 E4M3 block quantization
+  int32_t gated;       // 1: routed experts take their gate before the down projection (see above)
 } ora_cfg;
 }
 
@@ -280,8 +289,9 @@ void token_dlogits(const ora_cfg& c, const double* l, const int32_t* sel, const 
 // One SwiGLU expert applied to one token.  w13: [2F,H] (gate rows then up rows),
 // w2: [H,F].  Outputs (all length as named): gr,ur (F) = stored pre-activations,
 // ar (F) = stored activation, yr (H) = stored expert output.
+// gate: multiplies the activation before the down projection (gated mode; 1 otherwise)
 void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* x_in,
-                double* gr, double* ur, double* ar, double* yr) {
+                double* gr, double* ur, double* ar, double* yr, double gate = 1.0) {
   const int H = c.H;
   // FP8: the token row enters FC1 as 1x128 blocks along H, the activation enters
   // FC2 as 1x128 blocks along F; the weights are passed already block-quantized.
@@ -302,7 +312,7 @@ void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
     }
     gr[f] = maybe_r(c, g);
     ur[f] = maybe_r(c, u);
-    ar[f] = maybe_r(c, silu(g) * u);  // the activation is formed from the unrounded g, u
+    ar[f] = maybe_r(c, gate * (silu(g) * u));  // the activation is formed from the unrounded g, u
   }
   const double* a = ar;
   if (c.fp8) {
@@ -319,9 +329,13 @@ void expert_fwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
 }
 
 // Backward of one expert for one token, given the upstream gradient dyp (H) of
-// its output.  Produces dG, dU (F, as stored) and dx (H, as stored).
+// its output.  Produces dG, dU (F, as stored) and dx (H, as stored).  Gated
+// mode (dgate != null): dyp is the gradient of the gate-weighted output; the gate
+// gradient <W2^T dyp, silu(g) u> goes to *dgate and the activation gradient is
+// gate * W2^T dyp.
 void expert_bwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2, const double* gr,
-                const double* ur, const double* dyp_in, double* dG, double* dU, double* dx) {
+                const double* ur, const double* dyp_in, double* dG, double* dU, double* dx, double gate = 1.0,
+                double* dgate = nullptr) {
   const int H = c.H;
   std::vector<double> dA(F, 0.0), dq;
   const double* dyp = dyp_in;
@@ -334,6 +348,12 @@ void expert_bwd(const ora_cfg& c, int F, const uint16_t* w13, const uint16_t* w2
     const uint16_t* w = w2 + (size_t)h * F;
     const double d = dyp[h];
     for (int f = 0; f < F; ++f) dA[f] += bf(w[f]) * d;
+  }
+  if (dgate) {
+    double s = 0;
+    for (int f = 0; f < F; ++f) s += dA[f] * (silu(gr[f]) * ur[f]);
+    *dgate = s;
+    for (int f = 0; f < F; ++f) dA[f] *= gate;
   }
   for (int f = 0; f < F; ++f) {
     dG[f] = maybe_r(c, dA[f] * ur[f] * dsilu(gr[f]));
@@ -542,6 +562,16 @@ void ora_tokens_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, 
       const int e = sel[j];
       const uint16_t* w13 = W13 + (size_t)e * 2 * F * H;
       const uint16_t* w2 = W2 + (size_t)e * H * F;
+      if (c.gated) {  // the expert's output is gate-weighted already
+        expert_fwd(c, F, w13, w2, x.data(), gr.data(), ur.data(), ar.data(), ye.data(), gt[j]);
+        for (int h = 0; h < H; ++h) y[h] += ye[h];
+        if (bwd) {
+          expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dy.data(), dG.data(), dU.data(), dxe.data(), gt[j],
+                     &dg[j]);
+          for (int h = 0; h < H; ++h) dx[h] += dxe[h];
+        }
+        continue;
+      }
       expert_fwd(c, F, w13, w2, x.data(), gr.data(), ur.data(), ar.data(), ye.data());
       for (int h = 0; h < H; ++h) y[h] += gt[j] * ye[h];
       if (bwd) {
@@ -635,6 +665,17 @@ void ora_expert_wgrad_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t*
       double* dyp = &dyps[(size_t)i * H];
       for (int h = 0; h < H; ++h) x[h] = bf(X[(size_t)t * H + h]);
       expert_fwd(c, F, w13, w2, x, gr.data(), ur.data(), &as[(size_t)i * F], ye.data());
+      if (c.gated && expert >= 0) {
+        // the gradient of the gated output is dY itself; dW2 pairs it with the gated
+        // activation recomputed from the stored g, u
+        const double gj = gsel[c0 + i];
+        double dgate;
+        for (int h = 0; h < H; ++h) dyp[h] = bf(dY[(size_t)t * H + h]);
+        for (int f = 0; f < F; ++f) as[(size_t)i * F + f] = maybe_r(c, gj * (silu(gr[f]) * ur[f]));
+        expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dyp, &dGs[(size_t)i * F], &dUs[(size_t)i * F],
+                   dxe.data(), gj, &dgate);
+        return;
+      }
       for (int h = 0; h < H; ++h) dyp[h] = maybe_r(c, gsel[c0 + i] * bf(dY[(size_t)t * H + h]));
       expert_bwd(c, F, w13, w2, gr.data(), ur.data(), dyp, &dGs[(size_t)i * F], &dUs[(size_t)i * F], dxe.data());
     });

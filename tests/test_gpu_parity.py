@@ -416,3 +416,67 @@ def test_capacity_at_max_load_equals_dropless(by_gate):
     for name in ("offsets", "tile_offsets", "row_id_map", "Y", "dX", "dgates", "dW13", "dW2", "dW_r"):
         assert torch.equal(getattr(layer, name), getattr(ref, name)), name
     assert torch.equal(layer.seg_counts, ref.counts)
+
+
+# ---------------------------------------------------------------- memory-efficient (gated) path
+
+GATED_CASES = ["tiny", "ragged-softmax", "dsv3-mini", "e128-norenorm", "e1-k1", "k-equals-e"]
+
+
+@pytest.mark.parametrize("name", GATED_CASES)
+def test_memory_efficient_path_parity(name):
+    """Gates applied before FC2, Yperm unused in the backward, A recomputed from GU: the
+    same layer values as the oracle within the bf16 bound."""
+    w = CASES[name]
+    inp = S.host_inputs(w)
+    layer = make_layer(w, inp, memory_efficient=True)
+    layer.forward(to_dev(inp["X"]))
+    layer.backward(to_dev(inp["dY"]))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    logits, idx, g, d = check_routing(w, inp, layer, O.cfg(w, mirror=True))
+    # the oracle in the same form, rounding where this path stores bf16
+    c = O.cfg(w, mirror=True, gated=True)
+    tk = O.tokens(c, inp, idx, logits, g)
+    assert slice_rel_err(host_f64(layer.Y), tk["Y"]) < TOL_BF16
+    assert slice_rel_err(layer.dgates.cpu().numpy(), tk["dgates"]) < TOL_BF16
+    assert slice_rel_err(host_f64(layer.dX), tk["dX"]) < TOL_BF16
+    for e in range(w.E):
+        dW13, dW2 = O.expert_wgrad(c, inp, idx, g, e)
+        assert slice_rel_err(host_f64(layer.dW13[e]), dW13, 2) < TOL_BF16, e
+        assert slice_rel_err(host_f64(layer.dW2[e]), dW2, 2) < TOL_BF16, e
+    dWr, _ = O.router_wgrad(c, inp["X"], tk["dlogits"])
+    assert slice_rel_err(layer.dW_r.cpu().numpy(), dWr) < TOL_BF16
+    # the gated activations: A = gate * silu(g) * u on the kept rows
+    n_used = int(d["offsets"][-1])
+    src = d["slot_src"][:n_used]
+    real = src >= 0
+    gr = np.zeros(n_used)
+    gr[real] = layer.gates.cpu().numpy().ravel()[src[real]]
+    GU = host_f64(layer.GU[:n_used])
+    a = GU[:, :w.F] / (1.0 + np.exp(-GU[:, :w.F])) * GU[:, w.F:]
+    A = host_f64(layer.A[:n_used])  # rows past the used segments are never written
+    assert slice_rel_err(A[real], (gr[:, None] * a)[real]) < TOL_BF16
+    assert (A[~real] == 0).all()
+
+
+def test_memory_efficient_path_with_capacity():
+    w = CASES["dsv3-mini"]
+    inp = S.host_inputs(w)
+    cap = int(np.ceil(0.8 * w.T * w.k / w.E))
+    layer = make_layer(w, inp, capacity=cap, memory_efficient=True)
+    layer.forward(to_dev(inp["X"]))
+    layer.backward(to_dev(inp["dY"]))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = make_layer(w, inp, capacity=cap)
+    ref.forward(to_dev(inp["X"]))
+    ref.backward(to_dev(inp["dY"]))
+    torch.cuda.synchronize()
+    assert torch.equal(layer.row_id_map, ref.row_id_map)
+    for name in ("Y", "dX", "dW13", "dW2", "dW_r"):
+        a, b = host_f64(getattr(layer, name)), host_f64(getattr(ref, name))
+        assert slice_rel_err(a.reshape(a.shape[0], -1), b.reshape(b.shape[0], -1)) < TOL_BF16, name
+    dg, dgr = layer.dgates.cpu().numpy(), ref.dgates.cpu().numpy()
+    assert (dg[ref.row_id_map.cpu().numpy() < 0] == 0).all()
+    assert slice_rel_err(dg.reshape(1, -1), dgr.reshape(1, -1)) < TOL_BF16

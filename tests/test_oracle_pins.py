@@ -687,3 +687,25 @@ def test_capacity_drop_by_gate_keeps_largest_gates():
             assert g[sel & kept].min() >= g[sel & ~kept].max()
     mlp = dense_swiglu(f32(inp["X"]), f32(inp["W13"][0]), f32(inp["W2"][0]))
     assert np.allclose(out["Y"], (g * kept).sum(1, keepdims=True) * mlp, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- gated (memory-efficient) form
+
+
+@pytest.mark.parametrize("wname", ["pins-softmax", "pins-sigmoid-shared"])
+def test_gated_form_is_the_same_function(wname):
+    """Gate before the down projection vs gate in the combine: identical in exact arithmetic."""
+    w = {"pins-softmax": small("g1", T=40, H=32, E=4, k=2, F=16),
+         "pins-sigmoid-shared": small("g2", T=40, H=32, E=8, k=3, F=16, F_shared=16, score_fn=1, gate_scale=2.5,
+                                      n_group=2, topk_group=1)}[wname]
+    inp = inputs(w)
+    a = O.full_layer(w, inp, mirror=False)
+    b = O.full_layer(w, inp, mirror=False, gated=True)
+    for key in ["Y", "dX", "dgates", "dW13", "dW2", "dW_r"]:
+        assert np.allclose(a[key], b[key], rtol=1e-12, atol=1e-14), key
+    # with bf16 storage the two forms round in different places, within bf16 noise
+    am = O.full_layer(w, inp, mirror=True)
+    bm = O.full_layer(w, inp, mirror=True, gated=True)
+    for key in ["Y", "dX", "dW13", "dW2"]:
+        err = np.abs(am[key] - bm[key]).max() / np.abs(am[key]).max()
+        assert 0 < err < 2e-2, (key, err)
