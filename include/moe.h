@@ -130,7 +130,8 @@ moe_status moe_router_replay(const moe_config* cfg, const moe_bf16* X, const flo
  *  tile_offsets [E+1] int32 out   prefix sums of ceil(counts[e]/128) (the grouped GEMM's M-tile schedule)
  *  row_id_map   [T,k] int32 out   permuted row of assignment (t,j); tokens keep their order within an expert
  *  slot_src     [R] int32 out     inverse map: row -> t*k+j, or -1 for a padding row
- *  Xperm        [R,H] bf16 out    permuted tokens; padding rows are zero */
+ *  Xperm        [R,H] bf16 out    permuted tokens; padding rows are zero.  NULL: the maps only
+ *                                 (for moe_grouped_swiglu_mlp_gather); X may then be NULL too */
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,
                        int32_t* offsets, int32_t* tile_offsets, int32_t* row_id_map, int32_t* slot_src,
                        moe_bf16* Xperm, void* ws, void* stream);
@@ -175,6 +176,35 @@ moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, 
                                   moe_bf16* GU, moe_bf16* A, moe_bf16* Yperm, const moe_bf16* X,
                                   const moe_bf16* W13_s, const moe_bf16* W2_s, moe_bf16* GU_s, moe_bf16* A_s,
                                   moe_bf16* Yshared, void* ws, void* stream);
+
+/* Gathered-rows expert MLP: the dispatch without a permuted copy of the tokens.  (Summary
+ * page, "Method": kernel fusion among the compute recipes; fusing the permutation into
+ * the GEMM is a reading.)  FC1 reads row r of each expert segment as token
+ * slot_src[r] / k of X [T,H] (zeros for padding rows, slot_src[r] < 0), through TMA
+ * four-row gathers, so moe_permute can be called with Xperm = NULL (maps only).
+ * Outputs and results are those of moe_grouped_swiglu_mlp on the Xperm that moe_permute
+ * would have written.  Requires H % 256 == 0 (else MOE_ERR_UNSUPPORTED).
+ *  X [T,H] bf16 (device): the token rows (also the shared expert's input)
+ *  slot_src [R] int32 (device): from moe_permute / moe_permute_capacity
+ *  other arguments as moe_grouped_swiglu_mlp. */
+moe_status moe_grouped_swiglu_mlp_gather(const moe_config* cfg, const moe_bf16* X, const int32_t* slot_src,
+                                         const int32_t* offsets, const int32_t* tile_offsets, const moe_bf16* W13,
+                                         const moe_bf16* W2, moe_bf16* GU, moe_bf16* A, moe_bf16* Yperm,
+                                         const moe_bf16* W13_s, const moe_bf16* W2_s, moe_bf16* GU_s,
+                                         moe_bf16* A_s, moe_bf16* Yshared, void* ws, void* stream);
+
+/* Backward of moe_grouped_swiglu_mlp_gather: as moe_grouped_swiglu_mlp_bwd, with FC1's
+ * weight gradient gathering the token rows of X along K (dW13_e = dGU_e^T X[rows of e]);
+ * dXperm is still the permuted input gradient (moe_permute_bwd reduces it into dX). */
+moe_status moe_grouped_swiglu_mlp_bwd_gather(const moe_config* cfg, const moe_bf16* X, const int32_t* slot_src,
+                                             const int32_t* offsets, const int32_t* tile_offsets,
+                                             const int32_t* counts, const moe_bf16* W13, const moe_bf16* W2,
+                                             const moe_bf16* GU, const moe_bf16* A, const moe_bf16* dYperm,
+                                             moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* dW13, moe_bf16* dW2,
+                                             const moe_bf16* dY, const moe_bf16* W13_s, const moe_bf16* W2_s,
+                                             const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                             moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws,
+                                             void* stream);
 
 /* Memory-efficient expert MLP (gated rows).  (Summary page, "Method": memory-efficient
  * permutation and fine-grained activation recomputation are named among the memory

@@ -27,7 +27,8 @@ __all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
     "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd", "moe_router_topk_bwd", "moe_permute_bwd",
     "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc", "moe_permute_capacity",
-    "moe_grouped_swiglu_mlp_gated", "moe_grouped_swiglu_mlp_bwd_gated"]
+    "moe_grouped_swiglu_mlp_gated", "moe_grouped_swiglu_mlp_bwd_gated", "moe_grouped_swiglu_mlp_gather",
+    "moe_grouped_swiglu_mlp_bwd_gather"]
 
 EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_workspace_init",
             "moe_read_device_error", "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp",
@@ -35,7 +36,7 @@ EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_work
             "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc", "moe_fp8_workspace_size",
             "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8",
             "moe_router_replay", "moe_permute_capacity", "moe_grouped_swiglu_mlp_gated",
-            "moe_grouped_swiglu_mlp_bwd_gated"]
+            "moe_grouped_swiglu_mlp_bwd_gated", "moe_grouped_swiglu_mlp_gather", "moe_grouped_swiglu_mlp_bwd_gather"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -82,6 +83,8 @@ def load(build: bool = True):
                 "moe_router_replay": [cfgp] + [vp] * 11,
                 "moe_permute_capacity": [cfgp, vp, vp, vp, ctypes.c_int32] + [vp] * 9,
                 "moe_grouped_swiglu_mlp_gated": [cfgp] + [vp] * 18,
+                "moe_grouped_swiglu_mlp_gather": [cfgp] + [vp] * 16,
+                "moe_grouped_swiglu_mlp_bwd_gather": [cfgp] + [vp] * 25,
                 "moe_grouped_swiglu_mlp_bwd_gated": [cfgp] + [vp] * 29,
                 "moe_fp8_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t)],
                 "moe_quantize_weights_fp8": [cfgp] + [vp] * 13,
@@ -233,6 +236,24 @@ def moe_grouped_swiglu_mlp_bwd_gated(cfg, Xperm, offsets, tile_offsets, counts, 
     _call("moe_grouped_swiglu_mlp_bwd_gated", cfg, *map(_ptr, ts), _stream(stream))
 
 
+def moe_grouped_swiglu_mlp_gather(cfg, X, slot_src, offsets, tile_offsets, W13, W2, GU, A, Yperm, W13_s=None,
+                                  W2_s=None, GU_s=None, A_s=None, Yshared=None, ws=None, stream=None):
+    """The expert MLP with FC1 gathering the token rows of X through slot_src (no Xperm)."""
+    ts = (X, slot_src, offsets, tile_offsets, W13, W2, GU, A, Yperm, W13_s, W2_s, GU_s, A_s, Yshared, ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_gather", cfg, *map(_ptr, ts), _stream(stream))
+
+
+def moe_grouped_swiglu_mlp_bwd_gather(cfg, X, slot_src, offsets, tile_offsets, counts, W13, W2, GU, A, dYperm, dGU,
+                                      dXperm, dW13, dW2, dY=None, W13_s=None, W2_s=None, GU_s=None, A_s=None,
+                                      dGU_s=None, dX_shared=None, dW13_s=None, dW2_s=None, ws=None, stream=None):
+    """Backward of the gathered-rows MLP (FC1's weight gradient gathers X along K)."""
+    ts = (X, slot_src, offsets, tile_offsets, counts, W13, W2, GU, A, dYperm, dGU, dXperm, dW13, dW2, dY, W13_s,
+          W2_s, GU_s, A_s, dGU_s, dX_shared, dW13_s, dW2_s, ws)
+    _dev(*ts)
+    _call("moe_grouped_swiglu_mlp_bwd_gather", cfg, *map(_ptr, ts), _stream(stream))
+
+
 def moe_unpermute_combine(cfg, Yperm, row_id_map, gates, Yshared, Y, stream=None):
     _dev(Yperm, row_id_map, gates, Yshared, Y)
     _call("moe_unpermute_combine", cfg, *map(_ptr, (Yperm, row_id_map, gates, Yshared, Y)), _stream(stream))
@@ -317,9 +338,13 @@ class MoELayer:
     """
 
     def __init__(self, cfg: MoeConfig, weights: LayerWeights, device="cuda", fp8: bool = False,
-                 capacity: int | None = None, drop_by_gate: bool = False, memory_efficient: bool = False):
+                 capacity: int | None = None, drop_by_gate: bool = False, memory_efficient: bool = False,
+                 gather_rows: bool = False):
         if memory_efficient and fp8:
             raise ValueError("the memory-efficient path is built for the bf16 expert GEMMs")
+        if gather_rows and (fp8 or memory_efficient):
+            raise ValueError("gathered rows are built for the plain bf16 path")
+        self.gather_rows = gather_rows
         self.cfg = cfg
         self.w = weights
         self.fp8 = fp8
@@ -338,7 +363,8 @@ class MoELayer:
         # with a capacity, the segment sizes every later stage uses are the kept counts
         self.seg_counts = z(E, dt=i32) if capacity is not None else self.counts
         self.row_id_map, self.slot_src = z(T, k, dt=i32), z(R, dt=i32)
-        self.Xperm, self.GU, self.A, self.Yperm = z(R, H), z(R, 2 * F), z(R, F), z(R, H)
+        self.Xperm = None if gather_rows else z(R, H)
+        self.GU, self.A, self.Yperm = z(R, 2 * F), z(R, F), z(R, H)
         self.Y = z(T, H)
         self.dYperm, self.dgates, self.dGU, self.dXperm = z(R, H), z(T, k, dt=f32), z(R, 2 * F), z(R, H)
         self.dW13, self.dW2 = z(E, 2 * F, H), z(E, H, F)
@@ -382,6 +408,12 @@ class MoELayer:
             moe_permute_capacity(c, X, self.topk_idx, self.counts, self.capacity,
                                  self.gates if self.drop_by_gate else None, self.seg_counts, self.offsets,
                                  self.tile_offsets, self.row_id_map, self.slot_src, self.Xperm, self.ws)
+        if self.gather_rows:
+            moe_grouped_swiglu_mlp_gather(c, X, self.slot_src, self.offsets, self.tile_offsets, w.W13, w.W2, self.GU,
+                                          self.A, self.Yperm, w.W13_s, w.W2_s, self.GU_s, self.A_s, self.Yshared,
+                                          self.ws)
+            moe_unpermute_combine(c, self.Yperm, self.row_id_map, self.gates, self.Yshared, self.Y)
+            return self.Y
         if self.memory_efficient:
             moe_grouped_swiglu_mlp_gated(c, self.Xperm, self.offsets, self.tile_offsets, self.slot_src, self.gates,
                                          w.W13, w.W2, self.GU, self.A, self.Yperm, X if c.F_shared else None,
@@ -405,6 +437,19 @@ class MoELayer:
         c, w = self.cfg, self.w
         self.dY = dY
         sh = c.F_shared > 0
+        if self.gather_rows:
+            moe_unpermute_combine_bwd(c, dY, self.Yperm, self.row_id_map, self.gates, self.offsets, self.seg_counts,
+                                      self.dYperm, self.dgates)
+            moe_grouped_swiglu_mlp_bwd_gather(c, self.X, self.slot_src, self.offsets, self.tile_offsets,
+                                              self.seg_counts, w.W13, w.W2, self.GU, self.A, self.dYperm, self.dGU,
+                                              self.dXperm, self.dW13, self.dW2, dY if sh else None, w.W13_s, w.W2_s,
+                                              self.GU_s, self.A_s, self.dGU_s, self.dX_shared, self.dW13_s,
+                                              self.dW2_s, self.ws)
+            moe_router_topk_bwd(c, self.X, w.W_r, self.logits, self.scores, self.topk_idx, self.gates, self.dgates,
+                                self.dW_r, self.dlogit_bias if w.logit_bias is not None else None, self.dX_router,
+                                self.ws)
+            moe_permute_bwd(c, self.dXperm, self.row_id_map, self.dX_router, self.dX_shared, self.dX)
+            return self.dX
         if self.memory_efficient:
             moe_unpermute_combine_bwd(c, dY, None, self.row_id_map, None, self.offsets, self.seg_counts,
                                       self.dYperm, None)

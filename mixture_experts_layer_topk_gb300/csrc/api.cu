@@ -224,10 +224,11 @@ moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* 
                        moe_bf16* Xperm, void* ws, void* stream) {
   moe_status s = check_cfg(cfg, false);
   if (s != MOE_OK) return s;
-  if (!tok_ok(cfg, X) || !tok_ok(cfg, topk_idx) || !counts || !offsets || !tile_offsets ||
-      !tok_ok(cfg, row_id_map) || !slot_src || !Xperm)
+  // Xperm NULL: the dispatch maps only (X is then not read)
+  if ((Xperm && !tok_ok(cfg, X)) || !tok_ok(cfg, topk_idx) || !counts || !offsets || !tile_offsets ||
+      !tok_ok(cfg, row_id_map) || !slot_src)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(Xperm)) return MOE_ERR_INVALID_ARG;
+  if (Xperm && (!aligned16(X) || !aligned16(Xperm))) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*cfg);
   const int nsm = num_sms();
@@ -246,10 +247,10 @@ moe_status moe_permute_capacity(const moe_config* cfg, const moe_bf16* X, const 
   if (s != MOE_OK) return s;
   if (capacity < 0) return MOE_ERR_INVALID_ARG;
   if (priority && !tok_ok(cfg, priority)) return MOE_ERR_INVALID_ARG;
-  if (!tok_ok(cfg, X) || !tok_ok(cfg, topk_idx) || !counts || !kept_counts || !offsets || !tile_offsets ||
-      !tok_ok(cfg, row_id_map) || !slot_src || !Xperm)
+  if ((Xperm && !tok_ok(cfg, X)) || !tok_ok(cfg, topk_idx) || !counts || !kept_counts || !offsets ||
+      !tile_offsets || !tok_ok(cfg, row_id_map) || !slot_src)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(Xperm)) return MOE_ERR_INVALID_ARG;
+  if (Xperm && (!aligned16(X) || !aligned16(Xperm))) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*cfg);
   const int nsm = num_sms();
@@ -290,6 +291,101 @@ moe_status moe_grouped_swiglu_mlp(const moe_config* cfg, const moe_bf16* Xperm, 
     const GemmShape ss = shared_shape(*cfg);
     MOE_TRY(launch_fc1_fwd(ss, X, W13_s, GU_s, A_s, err, st));
     MOE_TRY(launch_fc2_fwd(ss, A_s, W2_s, Yshared, err, st));
+  }
+  return MOE_OK;
+}
+
+// Gathered-rows variants: FC1 reads the token rows of X through slot_src instead of a
+// permuted copy.  The CTA-pair kernels do the gathering, so H must be a multiple of 256.
+moe_status moe_grouped_swiglu_mlp_gather(const moe_config* cfg, const moe_bf16* X, const int32_t* slot_src,
+                                         const int32_t* offsets, const int32_t* tile_offsets, const moe_bf16* W13,
+                                         const moe_bf16* W2, moe_bf16* GU, moe_bf16* A, moe_bf16* Yperm,
+                                         const moe_bf16* W13_s, const moe_bf16* W2_s, moe_bf16* GU_s,
+                                         moe_bf16* A_s, moe_bf16* Yshared, void* ws, void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (cfg->H % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!tok_ok(cfg, X) || !slot_src || !offsets || !tile_offsets || !W13 || !W2 || !GU || !A || !Yperm)
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {X, W13, W2, GU, A, Yperm};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0) {
+    if (!W13_s || !W2_s || !tok_ok(cfg, GU_s) || !tok_ok(cfg, A_s) || !tok_ok(cfg, Yshared))
+      return MOE_ERR_INVALID_ARG;
+    const void* al2[] = {W13_s, W2_s, GU_s, A_s, Yshared};
+    for (const void* p : al2)
+      if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int* err = err_word(ws, *cfg);
+  const GemmShape rs = routed_shape(*cfg, offsets, tile_offsets, nullptr);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  if (cfg->T > 0) {
+    const RowGather rg{slot_src, cfg->k, cfg->T};
+    MOE_TRY(launch_fc1_fwd(rs, X, W13, GU, A, err, st, nullptr, &rg));
+  }
+  MOE_TRY(launch_fc2_fwd(rs, A, W2, Yperm, err, st));
+  if (cfg->F_shared > 0 && cfg->T > 0) {
+    const GemmShape ss = shared_shape(*cfg);
+    MOE_TRY(launch_fc1_fwd(ss, X, W13_s, GU_s, A_s, err, st));
+    MOE_TRY(launch_fc2_fwd(ss, A_s, W2_s, Yshared, err, st));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_grouped_swiglu_mlp_bwd_gather(const moe_config* cfg, const moe_bf16* X, const int32_t* slot_src,
+                                             const int32_t* offsets, const int32_t* tile_offsets,
+                                             const int32_t* counts, const moe_bf16* W13, const moe_bf16* W2,
+                                             const moe_bf16* GU, const moe_bf16* A, const moe_bf16* dYperm,
+                                             moe_bf16* dGU, moe_bf16* dXperm, moe_bf16* dW13, moe_bf16* dW2,
+                                             const moe_bf16* dY, const moe_bf16* W13_s, const moe_bf16* W2_s,
+                                             const moe_bf16* GU_s, const moe_bf16* A_s, moe_bf16* dGU_s,
+                                             moe_bf16* dX_shared, moe_bf16* dW13_s, moe_bf16* dW2_s, void* ws,
+                                             void* stream) {
+  moe_status s = check_cfg(cfg, true);
+  if (s != MOE_OK) return s;
+  if (cfg->H % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!tok_ok(cfg, X) || !slot_src || !offsets || !tile_offsets || !counts || !W13 || !W2 || !GU || !A ||
+      !dYperm || !dGU || !dXperm || !dW13 || !dW2)
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {X, W13, W2, GU, A, dYperm, dGU, dXperm, dW13, dW2};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (cfg->F_shared > 0) {
+    if (!tok_ok(cfg, dY) || !W13_s || !W2_s || !tok_ok(cfg, GU_s) || !tok_ok(cfg, A_s) || !tok_ok(cfg, dGU_s) ||
+        !tok_ok(cfg, dX_shared) || !dW13_s || !dW2_s)
+      return MOE_ERR_INVALID_ARG;
+    const void* al2[] = {dY, W13_s, W2_s, GU_s, A_s, dGU_s, dX_shared, dW13_s, dW2_s};
+    for (const void* p : al2)
+      if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int* err = err_word(ws, *cfg);
+  const GemmShape rs = routed_shape(*cfg, offsets, tile_offsets, counts);
+  if (rs.nsm <= 0) return MOE_ERR_CUDA;
+  MOE_TRY(launch_fc2_dgrad(rs, dYperm, W2, GU, dGU, err, st));
+  MOE_TRY(launch_fc2_wgrad(rs, dYperm, A, dW2, err, st));
+  MOE_TRY(launch_fc1_dgrad(rs, dGU, W13, dXperm, err, st));
+  if (cfg->T > 0) {
+    const RowGather rg{slot_src, cfg->k, cfg->T};
+    MOE_TRY(launch_fc1_wgrad(rs, dGU, X, dW13, err, st, &rg));
+  } else {  // no tokens: every expert's gradient is zero
+    MOE_TRY(cudaMemsetAsync(dW13, 0, sizeof(moe_bf16) * (size_t)cfg->E * 2 * cfg->F * cfg->H, st));
+  }
+  if (cfg->F_shared > 0) {
+    if (cfg->T == 0) {
+      MOE_TRY(cudaMemsetAsync(dW13_s, 0, sizeof(moe_bf16) * 2 * cfg->F_shared * cfg->H, st));
+      MOE_TRY(cudaMemsetAsync(dW2_s, 0, sizeof(moe_bf16) * cfg->F_shared * cfg->H, st));
+      return MOE_OK;
+    }
+    const GemmShape ss = shared_shape(*cfg);
+    MOE_TRY(launch_fc2_dgrad(ss, dY, W2_s, GU_s, dGU_s, err, st));
+    MOE_TRY(launch_fc2_wgrad(ss, dY, A_s, dW2_s, err, st));
+    MOE_TRY(launch_fc1_dgrad(ss, dGU_s, W13_s, dX_shared, err, st));
+    MOE_TRY(launch_fc1_wgrad(ss, dGU_s, X, dW13_s, err, st));
   }
   return MOE_OK;
 }

@@ -86,6 +86,12 @@ struct GemmArgs {
   float* dg_part;
   uint16_t* a_out;
   int64_t lda_out;
+  // gathered rows (CTA pairs; FWD: the A rows, WGRAD: the B rows along K): permuted row
+  // r is row gather_src[r] / gather_k of the mapped tensor, or past it (zeros) when
+  // gather_src[r] < 0; the map has one-row boxes.  gather_rows bounds r.
+  const int32_t* gather_src;
+  int gather_k, gather_oob;
+  int64_t gather_rows;
   // FP8 block scales (UE8M0 bytes): A and B, addressed per mode (see the SF warps)
   const uint8_t* sfa;
   int64_t sfa_ld;
@@ -323,7 +329,86 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
   const int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
   const int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
 
-  if (warp == 0) {
+  if (warp == 0 && PAIR && (MODE == MODE_FWD || MODE == MODE_WGRAD) && g.gather_src) {
+    // ------------------------------------------------------------ TMA producer, gathered rows
+    // Every lane gathers four of the operand's rows per stage (tile::gather4); lane 0
+    // waits for the stage, arms the barrier and loads the other operand.
+    auto src_row = [&](int64_t r) -> int {
+      if (r < 0 || r >= g.gather_rows) return g.gather_oob;
+      const int sr = __ldg(g.gather_src + r);
+      return sr >= 0 ? sr / g.gather_k : g.gather_oob;
+    };
+    int idx[4];
+    auto rows_of = [&](const Tile& tt, int k_b) {
+      const int64_t base = MODE == MODE_FWD ? (int64_t)tt.m0 + 4 * lane
+                                            : (int64_t)tt.k0 + (int64_t)k_b * BK + 4 * (lane & 15);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) idx[i] = src_row(base + i);
+    };
+    int stage = 0;
+    uint32_t phase = 0, used = 0, last_par = 0;
+    bool ok = true;
+    int t = t_first;
+    Tile tl;
+    auto next_work = [&]() {  // the next tile with k-blocks, and its first rows
+      while (t < total) {
+        tl = decode(t);
+        if (tl.kb > 0) break;
+        t += t_step;
+      }
+      if (t < total) rows_of(tl, 0);
+    };
+    next_work();
+    while (t < total && ok) {
+      for (int kb = 0; kb < tl.kb; ++kb) {
+        const int w_ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(&empty[stage], phase ^ 1) : 0, 0);
+        if (!w_ok) {
+          if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
+          ok = false;
+          break;
+        }
+        uint8_t* sa = tiles + stage * STAGE;
+        uint8_t* sb = sa + A_BYTES;
+        uint64_t* bar = &full[stage];
+        const int kc = kb * BK;
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar, 2 * STAGE);
+        const uint32_t cbar = mapa_shared(smem_u32(bar), 0);
+        if constexpr (MODE == MODE_FWD) {
+          tma_gather4_pair(sa + lane * 512, &mapA, cbar, kc, idx[0], idx[1], idx[2], idx[3]);
+          if (lane == 0) {
+            const int brow = EPI == EPI_SWIGLU ? (rank ? g.F + tl.n0 : tl.n0) : tl.n0 + rank * BNL;
+            tma_load_3d_pair(sb, &mapB, cbar, kc, brow, tl.e);
+          }
+        } else {
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d_pair(sa + j * 8192, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
+          }
+          // B: two 64-column MN-major boxes of 64 K rows, 16 four-row gathers each
+          const int j = lane >> 4, q = lane & 15;
+          tma_gather4_pair(sb + j * 8192 + q * 512, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, idx[0], idx[1],
+                           idx[2], idx[3]);
+        }
+        if (lane == 0) {
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == ST) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (MODE == MODE_WGRAD && kb + 1 < tl.kb) rows_of(tl, kb + 1);
+      }
+      if (!ok) break;
+      t += t_step;
+      next_work();
+    }
+    if (lane == 0 && rank == 0)
+      for (int s2 = 0; s2 < ST; ++s2)
+        if (used >> s2 & 1)
+          if (!mbar_wait(&full[s2], last_par >> s2 & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -894,10 +979,11 @@ int fc2_dgrad_tile_n(int F) { return pick_bn(F); }
 
 // X1 = rows of A [rows, K] (Xperm or X), W13 [E, 2F, K]: GU [rows, 2F], A [rows, F].
 cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
-                           int* err, cudaStream_t st, const Gating* gate) {
+                           int* err, cudaStream_t st, const Gating* gate, const RowGather* gather) {
   CUtensorMap ma, mb;
-  if (!map2d(&ma, X1, s.H, s.rows, 64, 128) || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 128))
-    return cudaErrorInvalidValue;
+  // gathered rows: X1 is the token matrix [gather->src_rows, H], read a row at a time
+  const bool ok_a = gather ? map2d(&ma, X1, s.H, gather->src_rows, 64, 1) : map2d(&ma, X1, s.H, s.rows, 64, 128);
+  if (!ok_a || !map3d(&mb, W13, s.H, 2 * (uint64_t)s.F, s.E, 64, 128)) return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = s.E; g.K = s.H; g.n_tiles = s.F / 128; g.dense_rows = s.dense_rows;
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
@@ -905,6 +991,13 @@ cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_
   if (gate) {
     g.slot_src = gate->slot_src;
     g.gates = gate->gates;
+  }
+  if (gather) {
+    g.gather_src = gather->slot_src;
+    g.gather_k = gather->k;
+    g.gather_oob = (int)gather->src_rows;
+    g.gather_rows = s.rows;
+    return launch<MODE_FWD, EPI_SWIGLU, 256, false, true>(ma, mb, ma, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   }
   if (use_pairs()) return launch<MODE_FWD, EPI_SWIGLU, 256, false, true>(ma, mb, ma, g, pair_tiles(s, g.n_tiles), s.nsm, st);
   return launch<MODE_FWD, EPI_SWIGLU, 256>(ma, mb, ma, g, s.max_mtiles * g.n_tiles, s.nsm, st);
@@ -994,10 +1087,12 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
 
 // dW13 [E, 2F, H] = dGU^T X per expert.
 cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, const RowGather* gather) {
   const int bn = pick_bn(s.H);
+  if (gather && bn != 256) return cudaErrorInvalidValue;  // gathered rows need the CTA-pair kernel
   CUtensorMap ma, mb, md;
-  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !map2d(&mb, X1, s.H, s.rows, 64, 64) ||
+  const bool ok_b = gather ? map2d(&mb, X1, s.H, gather->src_rows, 64, 1) : map2d(&mb, X1, s.H, s.rows, 64, 64);
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !ok_b ||
       !map_out(&md, dW13, s.H, 2 * (uint64_t)s.F, s.dense_rows > 0 ? 1 : s.E))
     return cudaErrorInvalidValue;
   GemmArgs g{};
@@ -1005,6 +1100,12 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
   g.seg_off = s.offsets; g.tile_off = s.tile_offsets; g.counts = s.counts;
   g.D = dW13; g.ldd = s.H; g.d_estride = 2 * (int64_t)s.F * s.H; g.err = err;
   g.n_fast = wgrad_n_fast(2 * s.F, s.H);
+  if (gather) {
+    g.gather_src = gather->slot_src;
+    g.gather_k = gather->k;
+    g.gather_oob = (int)gather->src_rows;
+    g.gather_rows = s.rows;
+  }
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
   if (bn == 256 && use_pairs())
     return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(

@@ -75,8 +75,17 @@ struct Gating {
   uint16_t* a_out;
 };
 
+// Gathered rows (no permuted copy of X): permuted row r of FC1's input is token
+// slot_src[r] / k of X [src_rows, H], or zeros for a padding row (slot_src[r] < 0).
+struct RowGather {
+  const int32_t* slot_src;
+  int k;
+  int64_t src_rows;
+};
+
 cudaError_t launch_fc1_fwd(const GemmShape& s, const uint16_t* X1, const uint16_t* W13, uint16_t* GU, uint16_t* Aact,
-                           int* err, cudaStream_t st, const Gating* gate = nullptr);
+                           int* err, cudaStream_t st, const Gating* gate = nullptr,
+                           const RowGather* gather = nullptr);
 cudaError_t launch_fc2_fwd(const GemmShape& s, const uint16_t* Aact, const uint16_t* W2, uint16_t* Y, int* err,
                            cudaStream_t st);
 cudaError_t launch_fc2_dgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* W2, const uint16_t* GU,
@@ -88,7 +97,7 @@ cudaError_t launch_fc1_dgrad(const GemmShape& s, const uint16_t* dGU, const uint
 cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint16_t* Aact, uint16_t* dW2, int* err,
                              cudaStream_t st);
 cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint16_t* X1, uint16_t* dW13, int* err,
-                             cudaStream_t st);
+                             cudaStream_t st, const RowGather* gather = nullptr);
 
 cudaError_t launch_fc1_fwd_fp8(const GemmShape& s, const Fp8Op& X1, const Fp8Op& W13, uint16_t* GU, uint16_t* Aact,
                                int* err, cudaStream_t st);

@@ -54,48 +54,81 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const int32_t* __restrict__ 
 }
 
 // One CTA: offsets (aligned segments), tile_offsets, and the per-chunk bases.
-// G threads per expert each own a contiguous range of chunks.
+// G threads per expert each own a contiguous range of chunks.  The chunk histogram
+// is first copied into shared memory with coalesced loads when it fits
+// (kScanStage entries); the per-expert prefix sums run on warp 0 (each lane a run
+// of consecutive experts, then a shuffle scan across the lanes).
+constexpr int kScanStage = 24576;
 __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ counts,
                                                const int32_t* __restrict__ chunk_counts, int nch, int E, int align,
                                                int cap, int32_t* __restrict__ kept,
                                                int32_t* __restrict__ offsets, int32_t* __restrict__ tile_offsets,
                                                int32_t* __restrict__ chunk_base, int32_t* __restrict__ drop_start,
                                                int* err) {
+  extern __shared__ int cc_s[];
   __shared__ int part[1024];
-  __shared__ int seg_start[257];
+  __shared__ int tot_s[256];
+  __shared__ int seg_start[256];
+  const bool staged = nch * E <= kScanStage;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (staged)
+    for (int i = tid; i < nch * E; i += 1024) cc_s[i] = chunk_counts[i];
+  __syncthreads();
+  const int32_t* cc = staged ? cc_s : chunk_counts;
   const int G = 1024 / E >= 1 ? 1024 / E : 1;  // threads per expert
-  const int tid = threadIdx.x;
   const int e = tid / G, g = tid % G;
   const int per = (nch + G - 1) / G;
   const int c0 = g * per, c1 = min(nch, c0 + per);
   int s = 0;
   if (e < E)
-    for (int c = c0; c < c1; ++c) s += chunk_counts[(size_t)c * E + e];
+    for (int c = c0; c < c1; ++c) s += cc[c * E + e];
   part[tid] = s;
   __syncthreads();
   if (g == 0 && e < E) {
     int tot = 0;
     for (int y = 0; y < G; ++y) tot += part[e * G + y];
     if (tot != counts[e]) set_device_error(err, MOE_ERR_DEVICE, 1000 + e);
-    seg_start[e] = tot;
+    tot_s[e] = tot;
   }
   __syncthreads();
-  if (tid == 0) {
-    int off = 0, tiles = 0, doff = 0;
-    offsets[0] = 0;
-    tile_offsets[0] = 0;
-    for (int x = 0; x < E; ++x) {
-      if (drop_start) drop_start[x] = doff;
-      doff += seg_start[x];
-      const int tot = min(seg_start[x], cap);
-      if (kept) kept[x] = tot;
-      seg_start[x] = off;
-      off += (tot + align - 1) / align * align;
-      tiles += (tot + 127) / 128;
-      offsets[x + 1] = off;
-      tile_offsets[x + 1] = tiles;
+  if (tid < 32) {
+    const int pl = (E + 31) / 32;
+    const int x0 = lane * pl, x1 = min(E, x0 + pl);
+    int sa = 0, sb = 0, sd = 0;  // aligned rows, M tiles, rows before capacity
+    for (int x = x0; x < x1; ++x) {
+      const int kt = min(tot_s[x], cap);
+      sa += (kt + align - 1) / align * align;
+      sb += (kt + 127) / 128;
+      sd += tot_s[x];
     }
-    if (drop_start) drop_start[E] = doff;
+    int ia = sa, ib = sb, id = sd;  // inclusive scans across the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o),
+                td = __shfl_up_sync(0xffffffffu, id, o);
+      if (lane >= o) {
+        ia += ta;
+        ib += tb;
+        id += td;
+      }
+    }
+    int oa = ia - sa, ob = ib - sb, od = id - sd;
+    for (int x = x0; x < x1; ++x) {
+      const int tot = tot_s[x], kt = min(tot, cap);
+      if (drop_start) drop_start[x] = od;
+      od += tot;
+      if (kept) kept[x] = kt;
+      seg_start[x] = oa;
+      oa += (kt + align - 1) / align * align;
+      ob += (kt + 127) / 128;
+      offsets[x + 1] = oa;
+      tile_offsets[x + 1] = ob;
+    }
+    if (lane == 0) {
+      offsets[0] = 0;
+      tile_offsets[0] = 0;
+    }
+    if (lane == 31 && drop_start) drop_start[E] = id;
   }
   __syncthreads();
   if (e < E) {
@@ -103,7 +136,7 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
     for (int y = 0; y < g; ++y) base += part[e * G + y];
     for (int c = c0; c < c1; ++c) {
       chunk_base[(size_t)c * E + e] = base;
-      base += chunk_counts[(size_t)c * E + e];
+      base += cc[c * E + e];
     }
   }
 }
@@ -133,8 +166,9 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
     const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
     for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
-      reinterpret_cast<uint4*>(Xperm)[i] = z;
+    if (Xperm)
+      for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
+        reinterpret_cast<uint4*>(Xperm)[i] = z;
     return;
   }
   const int c = blockIdx.x;
@@ -534,8 +568,18 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
     k_chunk_hist<<<nch, 256, 0, st>>>(topk_idx, c.T, c.E, c.k, chunk_counts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  k_scan<<<1, 1024, 0, st>>>(counts, chunk_counts, nch, c.E, c.align, cap, kept, offsets, tile_offsets, chunk_base,
-                             drop_start, err);
+  const size_t scan_smem = nch * c.E <= kScanStage ? sizeof(int) * (size_t)nch * c.E : 0;
+  if (scan_smem > 48 * 1024) {
+    static bool attr = false;
+    if (!attr) {
+      if ((e = cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(sizeof(int) * kScanStage))) !=
+          cudaSuccess)
+        return e;
+      attr = true;
+    }
+  }
+  k_scan<<<1, 1024, scan_smem, st>>>(counts, chunk_counts, nch, c.E, c.align, cap, kept, offsets, tile_offsets,
+                                     chunk_base, drop_start, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the padding CTAs size each segment's tail from the kept counts
   k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(X, topk_idx, chunk_base, kept ? kept : counts, offsets, c.T, c.H,
@@ -547,7 +591,7 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
                                         err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (c.T > 0) {
+  if (c.T > 0 && Xperm) {  // no Xperm: the maps only (the grouped GEMM gathers the rows)
     const int64_t vec = (int64_t)c.T * (c.H / 8);
     int64_t blocks = (vec + 255) / 256;
     if (blocks > 8LL * nsm) blocks = 8LL * nsm;

@@ -57,7 +57,7 @@ def logit_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
 
 
 def make_layer(w: S.Workload, inp: dict, device="cuda", capacity=None, drop_by_gate=False,
-               memory_efficient=False):
+               memory_efficient=False, gather_rows=False):
     import mixture_experts_layer_topk_gb300 as M
     cfg = M.config_from(w)
     weights = M.LayerWeights(
@@ -65,4 +65,4 @@ def make_layer(w: S.Workload, inp: dict, device="cuda", capacity=None, drop_by_g
         logit_bias=to_dev(inp.get("logit_bias")), sel_bias=to_dev(inp.get("sel_bias")),
         W13_s=to_dev(inp.get("W13_s")), W2_s=to_dev(inp.get("W2_s")))
     return M.MoELayer(cfg, weights, device=device, fp8=getattr(w, "fp8", False), capacity=capacity,
-                      drop_by_gate=drop_by_gate, memory_efficient=memory_efficient)
+                      drop_by_gate=drop_by_gate, memory_efficient=memory_efficient, gather_rows=gather_rows)
