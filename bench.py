@@ -241,6 +241,8 @@ def hbm_bytes(w):
         "combine_bwd": T * H * 2 + 2 * S_ * H * 2,
         "permute_bwd": S_ * H * 2 + T * H * 4 + T * H * 2 + (T * H * 2 if sh else 0),
     }
+    if w.E <= 32:  # the fused router streams X once (W_r, logits, scores, selection besides)
+        d["router"] = T * H * 2 + w.E * H * 4 + T * w.E * 4 * 2 + T * w.k * 8 + w.E * 4
     if w.fp8:  # bf16 weights read, E4M3 weights written (scales < 0.01%)
         wel = 3 * w.E * w.F * w.H + 3 * w.F_shared * w.H
         d["quant_w"] = wel * 2 + wel
@@ -342,28 +344,61 @@ def bench_ours(args, w):
     if layer.device_error() != 0:
         raise RuntimeError("device error during the timed steps")
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: every step copies its inputs (X, dY)
+    # up from pinned host memory and its results (Y, dX) back.  A copy stream moves the
+    # next step's inputs and the previous step's results while the current step
+    # computes; inputs and outputs alternate between two device buffers each.
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     dYh = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
     Xh.copy_(X)
     dYh.copy_(dY)
-    Yh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
-    dXh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
-    Xd = torch.empty_like(X)
-    dYd = torch.empty_like(dY)
+    Yh = [torch.empty(X.shape, dtype=X.dtype, pin_memory=True) for _ in range(2)]
+    dXh = [torch.empty(X.shape, dtype=X.dtype, pin_memory=True) for _ in range(2)]
+    Xd = [torch.empty_like(X) for _ in range(2)]
+    dYd = [torch.empty_like(dY) for _ in range(2)]
+    Yd = [layer.Y, torch.empty_like(layer.Y)]
+    dXd = [layer.dX, torch.empty_like(layer.dX)]
+    cs = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # results of buffer b are on the host
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        Xd[0].copy_(Xh, non_blocking=True)
+        dYd[0].copy_(dYh, non_blocking=True)
+        ev_in[0].record(cs)
     for i in range(args.steps):
-        Xd.copy_(Xh, non_blocking=True)
-        dYd.copy_(dYh, non_blocking=True)
-        run_step(layer, Xd, dYd)
-        Yh.copy_(layer.Y, non_blocking=True)
-        dXh.copy_(layer.dX, non_blocking=True)
+        b = i % 2
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])
+        layer.Y, layer.dX = Yd[b], dXd[b]
+        run_step(layer, Xd[b], dYd[b])
+        ev_done[b].record(stream)
+        with torch.cuda.stream(cs):
+            if i >= 1:  # the previous step's results, then the next step's inputs into its buffers
+                cs.wait_event(ev_done[1 - b])
+                Yh[1 - b].copy_(Yd[1 - b], non_blocking=True)
+                dXh[1 - b].copy_(dXd[1 - b], non_blocking=True)
+                ev_out[1 - b].record(cs)
+            if i + 1 < args.steps:
+                Xd[1 - b].copy_(Xh, non_blocking=True)
+                dYd[1 - b].copy_(dYh, non_blocking=True)
+                ev_in[1 - b].record(cs)
+    last = (args.steps - 1) % 2
+    with torch.cuda.stream(cs):
+        cs.wait_event(ev_done[last])
+        Yh[last].copy_(Yd[last], non_blocking=True)
+        dXh[last].copy_(dXd[last], non_blocking=True)
+    stream.wait_stream(cs)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
+    layer.Y, layer.dX = Yd[0], dXd[0]
 
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device=dev)
     if rank != 0:

@@ -196,51 +196,69 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
 }
 
 // E <= 32: one warp per token (TPW tokens at a time), lanes split H.
-template <int EMAX, int TPW>
+// E <= 32: a CTA routes 8 * TPW tokens (TPW per warp).  W_r goes through shared memory
+// in chunks of KC columns (EMAX * KC * 4 = 32 KB), loaded once per CTA; each warp
+// streams its tokens' X over the chunk and accumulates from shared memory.
+template <int EMAX, int TPW, int KC>
 __global__ void __launch_bounds__(256) k_router_small(RouteArgs a) {
+  __shared__ __align__(16) float wsm[EMAX * KC];
   __shared__ float lrows[8][TPW][EMAX];
   __shared__ int hist[EMAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < EMAX; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
   const int H = a.H, E = a.E;
-  const int nvec = H / 8;  // 16-byte vectors per row
-  const int gw = blockIdx.x * 8 + warp, nw = gridDim.x * 8;
-  for (int t0 = gw * TPW; t0 < a.T; t0 += nw * TPW) {
+  for (int base = blockIdx.x * 8 * TPW; base < a.T; base += gridDim.x * 8 * TPW) {
+    const int t0 = base + warp * TPW;
     float acc[TPW][EMAX];
 #pragma unroll
     for (int u = 0; u < TPW; ++u)
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) acc[u][e] = 0.f;
-    for (int c = lane; c < nvec; c += 32) {
-      float x[TPW][8];
+    for (int k0 = 0; k0 < H; k0 += KC) {
+      const int kc = H - k0 < KC ? H - k0 : KC;  // a multiple of 8
+      __syncthreads();                            // the previous chunk is consumed
+      for (int i = threadIdx.x; i < EMAX * (kc / 4); i += 256) {
+        const int e = i / (kc / 4), j = i % (kc / 4);
+        const float4 w = e < E ? __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)e * H + k0) + j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(&wsm[e * KC + 4 * j]) = w;
+      }
+      __syncthreads();
+      // all of this lane's X vectors of the chunk are loaded before any is used
+      constexpr int IT = KC / 256;  // 16-byte vectors per lane per token and chunk
+      uint4 xv[IT][TPW];
 #pragma unroll
-      for (int u = 0; u < TPW; ++u) {
-        if (t0 + u < a.T) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + u) * H) + c);
-          unpack8(v, x[u]);
-        } else {
+      for (int it = 0; it < IT; ++it) {
+        const int c = it * 32 + lane;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = 0.f;
-        }
+        for (int u = 0; u < TPW; ++u)
+          xv[it][u] = c < kc / 8 && t0 + u < a.T
+                          ? __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(t0 + u) * H + k0) + c)
+                          : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        if (e < E) {
-          const float4* w = reinterpret_cast<const float4*>(a.Wr + (size_t)e * H) + 2 * c;
-          const float4 w0 = __ldg(w), w1 = __ldg(w + 1);
+      for (int it = 0; it < IT; ++it) {
+        const int c = it * 32 + lane;
+        if (c >= kc / 8) continue;
+        float x[TPW][8];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) unpack8(xv[it][u], x[u]);
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          const float4 w0 = *reinterpret_cast<const float4*>(&wsm[e * KC + 8 * c]);
+          const float4 w1 = *reinterpret_cast<const float4*>(&wsm[e * KC + 8 * c + 4]);
 #pragma unroll
           for (int u = 0; u < TPW; ++u) {
-            float s = acc[u][e];
-            s = fmaf(x[u][0], w0.x, s);
-            s = fmaf(x[u][1], w0.y, s);
-            s = fmaf(x[u][2], w0.z, s);
-            s = fmaf(x[u][3], w0.w, s);
-            s = fmaf(x[u][4], w1.x, s);
-            s = fmaf(x[u][5], w1.y, s);
-            s = fmaf(x[u][6], w1.z, s);
-            s = fmaf(x[u][7], w1.w, s);
-            acc[u][e] = s;
+            float sum = acc[u][e];
+            sum = fmaf(x[u][0], w0.x, sum);
+            sum = fmaf(x[u][1], w0.y, sum);
+            sum = fmaf(x[u][2], w0.z, sum);
+            sum = fmaf(x[u][3], w0.w, sum);
+            sum = fmaf(x[u][4], w1.x, sum);
+            sum = fmaf(x[u][5], w1.y, sum);
+            sum = fmaf(x[u][6], w1.z, sum);
+            sum = fmaf(x[u][7], w1.w, sum);
+            acc[u][e] = sum;
           }
         }
       }
@@ -403,12 +421,11 @@ cudaError_t launch_two_pass(const RouteArgs& a, cudaStream_t st, int nsm) {
   return cudaGetLastError();
 }
 
-template <int EMAX, int TPW>
+template <int EMAX, int TPW, int KC>
 cudaError_t launch_small(const RouteArgs& a, cudaStream_t st, int nsm) {
-  const int warps_needed = (a.T + TPW - 1) / TPW;
-  int grid = (warps_needed + 7) / 8;
-  grid = grid < 4 * nsm ? grid : 4 * nsm;
-  k_router_small<EMAX, TPW><<<grid, 256, 0, st>>>(a);
+  const int groups = (a.T + 8 * TPW - 1) / (8 * TPW);  // 8 * TPW tokens per CTA
+  const int grid = groups < 8 * nsm ? groups : 8 * nsm;
+  k_router_small<EMAX, TPW, KC><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -691,9 +708,9 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
   if (e != cudaSuccess) return e;
   if (c.T == 0) return cudaSuccess;
-  if (c.E <= 8) return launch_small<8, 4>(a, st, nsm);
-  if (c.E <= 16) return launch_small<16, 2>(a, st, nsm);
-  if (c.E <= 32) return launch_small<32, 1>(a, st, nsm);
+  if (c.E <= 8) return launch_small<8, 2, 1024>(a, st, nsm);
+  if (c.E <= 16) return launch_small<16, 2, 512>(a, st, nsm);
+  if (c.E <= 32) return launch_small<32, 1, 256>(a, st, nsm);
   // E > 32: FP32 register-tiled GEMM on the CUDA cores.  (The tensor cores' FP32
   // accumulation drifts by about half an ulp per MMA step, ~5e-5 relative over K=3H
   // split terms, which the 1e-5 logit bound does not allow; the backward products,
