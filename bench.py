@@ -215,7 +215,7 @@ def run_step(layer, X, dY, ev=None):
 def launches_per_step(w):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
-    n = 2 if w.E > 32 else 1               # router (E > 32: logits GEMM, then routing)
+    n = 3 if w.E > 32 else 1               # router (E > 32: W_r split, tensor-core logits, routing)
     n += 4                                 # chunk histogram, scan, scatter, row copy
     n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
     n += 2                                 # combine, combine backward
@@ -241,8 +241,8 @@ def hbm_bytes(w):
         "combine_bwd": T * H * 2 + 2 * S_ * H * 2,
         "permute_bwd": S_ * H * 2 + T * H * 4 + T * H * 2 + (T * H * 2 if sh else 0),
     }
-    if w.E <= 32:  # the fused router streams X once (W_r, logits, scores, selection besides)
-        d["router"] = T * H * 2 + w.E * H * 4 + T * w.E * 4 * 2 + T * w.k * 8 + w.E * 4
+    # the router streams X once (W_r, logits, scores, selection besides)
+    d["router"] = T * H * 2 + w.E * H * 4 + T * w.E * 4 * 2 + T * w.k * 8 + w.E * 4
     if w.fp8:  # bf16 weights read, E4M3 weights written (scales < 0.01%)
         wel = 3 * w.E * w.F * w.H + 3 * w.F_shared * w.H
         d["quant_w"] = wel * 2 + wel

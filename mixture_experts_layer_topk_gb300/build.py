@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "permute_noalloc.cu", "fp8.cu"]
+SOURCES = ["api.cu", "router.cu", "router_tc.cu", "permute.cu", "grouped_gemm.cu", "permute_noalloc.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"] + ARCH

@@ -22,9 +22,9 @@ struct WsLayout {
   size_t rbwd_part;     // E <= 32: float[splits * E * H] token-split partials of dW_r
   int rbwd_splits;
   // E > 32 (router GEMMs on the tensor cores, exact three-term bf16 splits):
-  size_t wb;            // bf16[6Ep * H]    W_r row blocks hi, mid, hi, lo, hi, mid (dX_router)
+  size_t wb;            // bf16[3Ep * H]    W_r row blocks: hi, mid, lo (router forward) or hi, mid, hi (dX_router)
   size_t dl_rows;       // bf16[3Tp * Ep]   dlogits row blocks hi, mid, lo (dW_r)
-  size_t dl_cols;       // bf16[T * 6Ep]    dlogits column blocks hi, hi, mid, hi, lo, mid (dX_router)
+  size_t dl_cols;       // bf16[T * 3Ep]    dlogits column blocks hi, hi, mid (dX_router)
   int Tp, Ep;
   // capacity dropping by priority: assignments grouped by expert in token order
   size_t drop_order;    // int32[T * k]
@@ -73,11 +73,11 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.Ep = (c.E + 31) / 32 * 32;
   const bool tc = c.E > 32;
   L.wb = o;
-  if (tc) o = align256(o + (size_t)6 * L.Ep * c.H * 2);
+  if (tc) o = align256(o + (size_t)3 * L.Ep * c.H * 2);
   L.dl_rows = o;
   if (tc) o = align256(o + (size_t)3 * L.Tp * L.Ep * 2);
   L.dl_cols = o;
-  if (tc) o = align256(o + (size_t)c.T * 6 * L.Ep * 2);
+  if (tc) o = align256(o + (size_t)c.T * 3 * L.Ep * 2);
   L.drop_order = o;
   o = align256(o + (size_t)c.T * c.k * sizeof(int32_t));
   L.drop_start = o;

@@ -1227,16 +1227,17 @@ cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint
                    : launch<MODE_WGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);
 }
 
-// dX_r[T,H] (fp32) = dlA[T,6Ep] . WB[6Ep,H] (the six significant products of the two splits).
+// dX_r[T,H] (fp32) = dlA[T,3Ep] . WB[3Ep,H]: the products hi.hi + hi.mid + mid.hi of the bf16
+// splits of dlogits and W_r (relative error ~2^-16; dX_r is added into a bf16 dX).
 cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const uint16_t* WB, float* dXr, int* err,
                                 int nsm, cudaStream_t st) {
   const int bn = H % 256 == 0 ? 256 : 128;
   CUtensorMap ma, mb, md;
-  if (!map2d(&ma, dlA, 6 * (uint64_t)Ep, T, 64, 128) || !map3d(&mb, WB, H, 6 * (uint64_t)Ep, 1, 64, 64) ||
+  if (!map2d(&ma, dlA, 3 * (uint64_t)Ep, T, 64, 128) || !map3d(&mb, WB, H, 3 * (uint64_t)Ep, 1, 64, 64) ||
       !map_out_f32(&md, dXr, H, T, 1))
     return cudaErrorInvalidValue;
   GemmArgs g{};
-  g.E = 1; g.K = 6 * Ep; g.n_tiles = H / bn; g.dense_rows = T; g.err = err;
+  g.E = 1; g.K = 3 * Ep; g.n_tiles = H / bn; g.dense_rows = T; g.err = err;
   const int tiles = ((T + 127) / 128) * g.n_tiles;
   return bn == 256 ? launch<MODE_DGRAD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
                    : launch<MODE_DGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);

@@ -32,14 +32,21 @@ struct RouterBwdScratch {
   float* part;        // [splits,E,H] partial dW_r (token splits)
   int splits;
   uint16_t* dl_rows;  // E > 32: [3*Tp, Ep] bf16 split of dl (row blocks hi, mid, lo)
-  uint16_t* dl_cols;  // E > 32: [T, 6*Ep] bf16 split of dl (column blocks hi, hi, mid, hi, lo, mid)
-  uint16_t* wb;       // E > 32: [6*Ep, H] bf16 split of W_r (row blocks hi, mid, hi, lo, hi, mid)
+  uint16_t* dl_cols;  // E > 32: [T, 3*Ep] bf16 split of dl (column blocks hi, hi, mid)
+  uint16_t* wb;       // E > 32: [3*Ep, H] bf16 split of W_r (row blocks hi, mid, hi)
   int Tp, Ep;
 };
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given = nullptr);
+                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given = nullptr,
+                               uint16_t* wsplit = nullptr, int* err = nullptr);
+// E > 32: P = X W_r^T on the tensor cores from wsplit = [3*Ep,H] bf16 (row blocks hi,
+// mid, lo of W_r).  With router_tc_ksplits(T,E,nsm) == 2 the two K halves go to P0 and
+// P1 (to be added), else the whole product to P0.
+int router_tc_ksplits(int T, int E, int nsm);
+cudaError_t launch_router_logits_tc(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0,
+                                    float* P1, int* err, int nsm, cudaStream_t st);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
                               float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,

@@ -5,8 +5,10 @@
 // states, kept in FP32, followed by softmax or sigmoid scoring and top-k
 // selection.  The kernels here fuse the projection (an FP32 GEMV / skinny
 // GEMM), the scoring, the optional group limit, the top-k (warp shuffles) and
-// the gate computation into one launch for E <= 32; for larger E the projection is
-// a register-tiled split-K GEMM followed by a routing pass (two launches).
+// the gate computation into one launch for E <= 32; for larger E the projection
+// runs on the tensor cores (router_tc.cu: exact bf16 split of W_r, block sums
+// promoted to FP32 registers) followed by a routing pass; without a workspace it
+// is a register-tiled split-K FP32 GEMM on the CUDA cores instead.
 //
 // Selection rule: key = logit (+ sel_bias) for softmax, sigmoid(logit)
 // (+ sel_bias) for sigmoid, formed in FP32; the k experts are listed in
@@ -38,20 +40,28 @@ struct RouteArgs {
   float gate_scale;
   int n_group, topk_group, group_score;
   const int32_t* given;  // router replay: the selection to use instead of top-k (nullable)
+  int halves;            // k_route_rows: the product is split in two K halves (logits + scores)
 };
 
-// (value, index) maximum over the warp; ties to the lower index.  Lanes with
-// no candidate pass (-inf, INT_MAX).
+// Order-preserving map of an fp32 key to uint32: a < b as floats iff ord_key(a) <
+// ord_key(b).  -0 is first turned into +0, so the two zeros tie as they do under
+// float comparison.
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord_val(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// (value, index) maximum over the warp; ties to the lower index: the warp-wide
+// maximum of the ordered keys (one redux.sync), then the least index among the
+// lanes that hold it (another).  Lanes with no candidate pass (-FLT_MAX, INT_MAX).
 __device__ __forceinline__ void warp_argmax(float& v, int& e) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
-    if (ov > v || (ov == v && oe < e)) {
-      v = ov;
-      e = oe;
-    }
-  }
+  const uint32_t u = ord_key(v);
+  const uint32_t m = __reduce_max_sync(0xffffffffu, u);
+  e = (int)__reduce_min_sync(0xffffffffu, u == m ? (uint32_t)e : 0xffffffffu);
+  v = ord_val(m);
 }
 
 // ---------------------------------------------------------------- exact bf16 splits
@@ -108,6 +118,9 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
   // group limit
   if (a.n_group > 1 && !a.given) {
     const int per = E / a.n_group;
+    int gi[V];  // group of each of this lane's experts
+#pragma unroll
+    for (int i = 0; i < V; ++i) gi[i] = (lane + 32 * i) / per;
     float my_gs = -FLT_MAX;
     for (int g = 0; g < a.n_group; ++g) {
       float v1 = -FLT_MAX;
@@ -115,7 +128,7 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
 #pragma unroll
       for (int i = 0; i < V; ++i) {
         const int e = lane + 32 * i;
-        if (!(excl >> i & 1) && e / per == g && (key[i] > v1 || (key[i] == v1 && e < e1))) {
+        if (!(excl >> i & 1) && gi[i] == g && (key[i] > v1 || (key[i] == v1 && e < e1))) {
           v1 = key[i];
           e1 = e;
         }
@@ -128,7 +141,7 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
 #pragma unroll
         for (int i = 0; i < V; ++i) {
           const int e = lane + 32 * i;
-          if (!(excl >> i & 1) && e / per == g && e != e1 && (key[i] > v2 || (key[i] == v2 && e < e2))) {
+          if (!(excl >> i & 1) && gi[i] == g && e != e1 && (key[i] > v2 || (key[i] == v2 && e < e2))) {
             v2 = key[i];
             e2 = e;
           }
@@ -148,7 +161,7 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !(keep >> (e / per) & 1)) excl |= 1u << i;
+      if (e < E && !(keep >> gi[i] & 1)) excl |= 1u << i;
     }
   }
   // top-k: lane j ends up holding the j-th selected expert (router replay: read it)
@@ -396,10 +409,12 @@ __global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
   __syncthreads();
   const int E = a.E;
   for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
-    // the first half of the product is in logits, the second in scores
-    for (int e = lane; e < E; e += 32)
-      lrows[warp][e] = (a.logits[(size_t)t * E + e] + a.scores[(size_t)t * E + e]) +
-                       (a.logit_bias ? a.logit_bias[e] : 0.f);
+    // the product (or its first K half) is in logits, the second half (if any) in scores
+    for (int e = lane; e < E; e += 32) {
+      float p = a.logits[(size_t)t * E + e];
+      if (a.halves == 2) p += a.scores[(size_t)t * E + e];
+      lrows[warp][e] = p + (a.logit_bias ? a.logit_bias[e] : 0.f);
+    }
     __syncwarp();
     route_token<V>(a, t, lrows[warp], hist);
     __syncwarp();
@@ -409,16 +424,23 @@ __global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
     if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
 }
 
+template <int V>
+cudaError_t launch_route_rows(const RouteArgs& a, cudaStream_t st, int nsm) {
+  // a token's routing is a chain of dependent warp reductions: many warps per SM hide it
+  int g2 = (a.T + 7) / 8;
+  g2 = g2 < 8 * nsm ? g2 : 8 * nsm;
+  k_route_rows<V><<<g2, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <int BE, int V>
-cudaError_t launch_two_pass(const RouteArgs& a, cudaStream_t st, int nsm) {
+cudaError_t launch_two_pass(RouteArgs a, cudaStream_t st, int nsm) {
   dim3 g1((a.T + kRgBT - 1) / kRgBT, (a.E + BE - 1) / BE, 2);
   k_router_gemm<BE><<<g1, 256, 0, st>>>(a.X, a.Wr, a.T, a.H, a.E, a.logits, a.scores);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int g2 = (a.T + 7) / 8;
-  g2 = g2 < 2 * nsm ? g2 : 2 * nsm;
-  k_route_rows<V><<<g2, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  a.halves = 2;
+  return launch_route_rows<V>(a, st, nsm);
 }
 
 template <int EMAX, int TPW, int KC>
@@ -442,7 +464,7 @@ struct RouteBwdArgs {
   float gate_scale;
   // optional exact bf16 splits of dl for the tensor-core router GEMMs
   uint16_t* dl_rows;  // [3*Tp, Ep]: rows t, Tp+t, 2Tp+t hold hi, mid, lo
-  uint16_t* dl_cols;  // [T, 6*Ep]: column blocks hi, hi, mid, hi, lo, mid
+  uint16_t* dl_cols;  // [T, 3*Ep]: column blocks hi, hi, mid
   int Tp, Ep;
 };
 
@@ -521,13 +543,10 @@ __global__ void __launch_bounds__(256) k_router_dlogits(RouteBwdArgs a) {
       a.dl_rows[(size_t)t * a.Ep + e] = hi;
       a.dl_rows[((size_t)a.Tp + t) * a.Ep + e] = mid;
       a.dl_rows[((size_t)2 * a.Tp + t) * a.Ep + e] = lo;
-      uint16_t* c = a.dl_cols + (size_t)t * 6 * a.Ep + e;
+      uint16_t* c = a.dl_cols + (size_t)t * 3 * a.Ep + e;
       c[0] = hi;
       c[a.Ep] = hi;
       c[2 * a.Ep] = mid;
-      c[3 * a.Ep] = hi;
-      c[4 * a.Ep] = lo;
-      c[5 * a.Ep] = mid;
     }
   }
 }
@@ -669,8 +688,8 @@ __global__ void __launch_bounds__(256) k_reduce_splits(const float* __restrict__
   }
 }
 
-// W_r [E,H] fp32 -> fwd [E,3H] (hi | mid | lo along K) and/or bwd [6*Ep,H] (row blocks
-// hi, mid, hi, lo, hi, mid; rows E..Ep-1 of each block zero).
+// W_r [E,H] fp32 -> fwd [3*Ep,H] (row blocks hi, mid, lo) and/or bwd [3*Ep,H] (row blocks
+// hi, mid, hi); rows E..Ep-1 of each block zero.
 __global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, int E, int H, int Ep,
                                                   uint16_t* __restrict__ fwd, uint16_t* __restrict__ bwd) {
   const int64_t n = (int64_t)Ep * H;
@@ -678,16 +697,15 @@ __global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, 
     const int e = (int)(i / H), h = (int)(i % H);
     uint16_t hi = 0, mid = 0, lo = 0;
     if (e < E) split3(Wr[i], hi, mid, lo);
-    if (fwd && e < E) {
-      uint16_t* row = fwd + (size_t)e * 3 * H;
-      row[h] = hi;
-      row[H + h] = mid;
-      row[2 * H + h] = lo;
+    if (fwd) {
+      fwd[i] = hi;
+      fwd[n + i] = mid;
+      fwd[2 * n + i] = lo;
     }
     if (bwd) {
-      const uint16_t seg[6] = {hi, mid, hi, lo, hi, mid};
-#pragma unroll
-      for (int k = 0; k < 6; ++k) bwd[((size_t)k * Ep + e) * H + h] = seg[k];
+      bwd[i] = hi;
+      bwd[n + i] = mid;
+      bwd[2 * n + i] = hi;
     }
   }
 }
@@ -701,20 +719,35 @@ struct Bf16In {
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
-                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given) {
+                               int32_t* counts, cudaStream_t st, int nsm, const int32_t* given,
+                               uint16_t* wsplit, int* err) {
   RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
               c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
-              c.group_score, given};
+              c.group_score, given, 1};
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
   if (e != cudaSuccess) return e;
   if (c.T == 0) return cudaSuccess;
   if (c.E <= 8) return launch_small<8, 2, 1024>(a, st, nsm);
   if (c.E <= 16) return launch_small<16, 2, 512>(a, st, nsm);
   if (c.E <= 32) return launch_small<32, 1, 256>(a, st, nsm);
-  // E > 32: FP32 register-tiled GEMM on the CUDA cores.  (The tensor cores' FP32
-  // accumulation drifts by about half an ulp per MMA step, ~5e-5 relative over K=3H
-  // split terms, which the 1e-5 logit bound does not allow; the backward products,
-  // held to bf16-class bounds, do run on the tensor cores.)
+  // E > 32 with a workspace: the logits on the tensor cores from the exact bf16 split of
+  // W_r, block sums promoted to FP32 registers every 64 columns of K (router_tc.cu),
+  // then one warp per token routes.
+  if (wsplit) {
+    const int Ep = (c.E + 31) / 32 * 32;
+    int blocks = (int)(((int64_t)Ep * c.H + 255) / 256);
+    blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
+    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, Ep, wsplit, nullptr);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_router_logits_tc(c.T, c.H, c.E, Ep, X, wsplit, logits, scores, err, nsm, st)) != cudaSuccess)
+      return e;
+    a.halves = router_tc_ksplits(c.T, c.E, nsm);
+    if (c.E <= 64) return launch_route_rows<2>(a, st, nsm);
+    if (c.E <= 128) return launch_route_rows<4>(a, st, nsm);
+    return launch_route_rows<8>(a, st, nsm);
+  }
+  // Without a workspace: an FP32 register-tiled GEMM on the CUDA cores, then the
+  // routing pass.
   if (c.E <= 64) return launch_two_pass<64, 2>(a, st, nsm);
   if (c.E <= 128) return launch_two_pass<128, 4>(a, st, nsm);
   return launch_two_pass<128, 8>(a, st, nsm);

@@ -126,6 +126,9 @@ WORKLOADS = {
     # shapes along K for FC1, 0.4 GB of expert weights: larger than L2, small enough
     # for a multi-pass profiler capture)
     "mixtral-small": Workload("mixtral-small", T=4096, H=4096, E=8, k=2, F=2048),
+    # profiling stand-in with the Qwen3-style layer's router (X of 134 MB, 128 experts,
+    # top-8) and a narrow FFN, so that the whole layer holds a few GB
+    "qwen3-small": Workload("qwen3-small", T=16384, H=4096, E=128, k=8, F=128),
     # profiling stand-in with DeepSeek-V3-style routing and small expert segments
     # (about 64 rows per expert): 2.8 GB of expert weights, small enough for a full capture
     "dsv3-small": Workload("dsv3-small", T=2048, H=7168, E=256, k=8, F=256, F_shared=256, score_fn=1,
