@@ -327,19 +327,34 @@ __global__ void __launch_bounds__(1024) k_drop_select(const float* __restrict__ 
   if (tid == 0 && kept_run != kept[e]) set_device_error(err, MOE_ERR_DEVICE, 3000 + e);
 }
 
-// Xperm[row_id_map[t,j]] = X[t]: 16-byte vectors over the whole grid, each
-// token vector read once and written to its k rows.
+// Xperm[row_id_map[t,j]] = X[t]: one warp per token, its k destination rows read once;
+// each lane loads U 16-byte vectors of the row before storing them to every kept row.
 __global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ X,
                                                    const int32_t* __restrict__ row_id_map, int T, int H, int k,
                                                    uint16_t* __restrict__ Xperm) {
+  constexpr int U = kGatherUnroll;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : -1;
   const int nvec = H / 8;
-  const int64_t total = (int64_t)T * nvec;
-  for (int64_t v = blockIdx.x * 256LL + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
-    const int t = (int)(v / nvec), c = (int)(v % nvec);
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(X + (size_t)t * H) + c);
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)t * H);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    uint4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u + lane;
+      x[u] = v < nvec ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+    }
     for (int j = 0; j < k; ++j) {
-      const int slot = __ldg(row_id_map + (size_t)t * k + j);
-      if (slot >= 0) reinterpret_cast<uint4*>(Xperm + (size_t)slot * H)[c] = x;
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      if (slot < 0) continue;  // dropped by capacity: no row
+      uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < nvec) out[v] = x[u];
+      }
     }
   }
 }
@@ -400,7 +415,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ Yp
 }
 
 // dYperm[slot] = bf16(g dY[t]); dgates[t,j] = <dY[t], Yperm[slot]>.
-// CTAs past the token range zero the padding rows, kPadSplit CTAs per expert.
+// One warp per assignment a = t*k + j, so that the k assignments of a token stream
+// independently; they sit in consecutive warps, so dY[t] comes from DRAM once.
+// CTAs past the assignment range zero the padding rows, kPadSplit CTAs per expert.
 // gates == nullptr: g = 1 (gated rows); dgates == nullptr: no gate gradient.
 __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict__ dY,
                                                      const uint16_t* __restrict__ Yperm,
@@ -408,10 +425,10 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict_
                                                      const float* __restrict__ gates,
                                                      const int32_t* __restrict__ offsets,
                                                      const int32_t* __restrict__ counts, uint16_t* __restrict__ dYperm,
-                                                     float* __restrict__ dgates, int T, int H, int k, int tok_blocks) {
+                                                     float* __restrict__ dgates, int T, int H, int k, int asg_blocks) {
   const int nvec = H / 8;
-  if ((int)blockIdx.x >= tok_blocks) {
-    const int p = blockIdx.x - tok_blocks;
+  if ((int)blockIdx.x >= asg_blocks) {
+    const int p = blockIdx.x - asg_blocks;
     const int e = p / kPadSplit, part = p % kPadSplit;
     const int r1e = offsets[e + 1];
     const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
@@ -423,54 +440,49 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const uint16_t* __restrict_
     return;
   }
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : 0;
-  const float my_g = lane < k ? (gates ? gates[(size_t)t * k + lane] : 1.0f) : 0.f;
-  constexpr int U = kGatherUnroll;
-  float my_dot = 0.f;
-  const uint4* dyr = reinterpret_cast<const uint4*>(dY + (size_t)t * H);
-  for (int j = 0; j < k; ++j) {
-    const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-    const float g = __shfl_sync(0xffffffffu, my_g, j);
-    float dot = 0.f;
-    if (slot >= 0) {  // the same for the whole warp
-      const uint4* yr = reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H);
-      uint4* outr = reinterpret_cast<uint4*>(dYperm + (size_t)slot * H);
-      for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
-        uint4 dy[U], y[U];
+  const int64_t a = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (a >= (int64_t)T * k) return;
+  const int slot = row_id_map[a];
+  float dot = 0.f;
+  if (slot >= 0) {  // a dropped assignment (capacity) has no row and a zero gate gradient
+    const int t = (int)(a / k);
+    const float g = gates ? gates[a] : 1.0f;
+    constexpr int U = kGatherUnroll;
+    const uint4* dyr = reinterpret_cast<const uint4*>(dY + (size_t)t * H);
+    const uint4* yr = reinterpret_cast<const uint4*>(Yperm + (size_t)slot * H);
+    uint4* outr = reinterpret_cast<uint4*>(dYperm + (size_t)slot * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint4 dy[U], y[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + 32 * u + lane;
-          dy[u] = v < nvec ? __ldg(dyr + v) : make_uint4(0, 0, 0, 0);
-          y[u] = dgates && v < nvec ? __ldg(yr + v) : make_uint4(0, 0, 0, 0);
-        }
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        dy[u] = v < nvec ? __ldg(dyr + v) : make_uint4(0, 0, 0, 0);
+        y[u] = dgates && v < nvec ? __ldg(yr + v) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + 32 * u + lane;
-          if (v >= nvec) continue;
-          if (dgates || g != 1.0f) {
-            float df[8], yf[8], o[8];
-            unpack8(dy[u], df);
-            unpack8(y[u], yf);
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v >= nvec) continue;
+        if (dgates || g != 1.0f) {
+          float df[8], yf[8], o[8];
+          unpack8(dy[u], df);
+          unpack8(y[u], yf);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              dot = fmaf(df[q], yf[q], dot);
-              o[q] = g * df[q];
-            }
-            outr[v] = pack8(o);
-          } else {
-            outr[v] = dy[u];  // a unit gate: the row is a copy
+          for (int q = 0; q < 8; ++q) {
+            dot = fmaf(df[q], yf[q], dot);
+            o[q] = g * df[q];
           }
+          outr[v] = pack8(o);
+        } else {
+          outr[v] = dy[u];  // a unit gate: the row is a copy
         }
       }
     }
-    if (dgates) {
-      dot = warp_sum(dot);
-      if (lane == j) my_dot = dot;
-    }
   }
-  if (dgates && lane < k) dgates[(size_t)t * k + lane] = my_dot;
+  if (dgates) {
+    dot = warp_sum(dot);
+    if (lane == 0) dgates[a] = dot;
+  }
 }
 
 // dX[t] = sum_j dXperm[row_id_map[t,j]] + dX_router[t] + dX_shared[t].
@@ -592,10 +604,7 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (c.T > 0 && Xperm) {  // no Xperm: the maps only (the grouped GEMM gathers the rows)
-    const int64_t vec = (int64_t)c.T * (c.H / 8);
-    int64_t blocks = (vec + 255) / 256;
-    if (blocks > 8LL * nsm) blocks = 8LL * nsm;
-    k_copy_rows<<<(int)blocks, 256, 0, st>>>(X, row_id_map, c.T, c.H, c.k, Xperm);
+    k_copy_rows<<<(c.T + 7) / 8, 256, 0, st>>>(X, row_id_map, c.T, c.H, c.k, Xperm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -611,9 +620,9 @@ cudaError_t launch_combine(const moe_config& c, const uint16_t* Yperm, const int
 cudaError_t launch_combine_bwd(const moe_config& c, const uint16_t* dY, const uint16_t* Yperm,
                                const int32_t* row_id_map, const float* gates, const int32_t* offsets,
                                const int32_t* counts, uint16_t* dYperm, float* dgates, cudaStream_t st) {
-  const int tb = (c.T + 7) / 8;
-  k_combine_bwd<<<tb + c.E * kPadSplit, 256, 0, st>>>(dY, Yperm, row_id_map, gates, offsets, counts, dYperm, dgates, c.T, c.H,
-                                           c.k, tb);
+  const int ab = (int)(((int64_t)c.T * c.k + 7) / 8);
+  k_combine_bwd<<<ab + c.E * kPadSplit, 256, 0, st>>>(dY, Yperm, row_id_map, gates, offsets, counts, dYperm, dgates, c.T,
+                                                      c.H, c.k, ab);
   return cudaGetLastError();
 }
 
