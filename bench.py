@@ -215,7 +215,7 @@ def run_step(layer, X, dY, ev=None):
 def launches_per_step(w):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
-    n = 3 if w.E > 32 else 1               # router (E > 32: W_r split, tensor-core logits, routing)
+    n = 3                                  # router: W_r split, tensor-core logits, routing
     n += 4                                 # chunk histogram, scan, scatter, row copy
     n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
     n += 2                                 # combine, combine backward

@@ -106,11 +106,12 @@ moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
  *                                    exact ties to the lower expert index
  *  gates    [T,k] fp32 out           combine weights (renormalised, times gate_scale)
  *  counts   [E] int32 out            tokens per expert
- *  ws       workspace (moe_workspace_size) or NULL.  For E > 32 it holds the bf16 split of
- *           W_r that the tensor-core projection reads, and the error word its bounded
- *           waits report to (MOE_ERR_TIMEOUT, read by moe_read_device_error).  With
- *           NULL the projection of E > 32 runs as an FP32 GEMM on the CUDA cores instead
- *           (slower; same selection rule and bounds).  E <= 32 does not use it. */
+ *  ws       workspace (moe_workspace_size) or NULL.  It holds the bf16 split of W_r that
+ *           the tensor-core projection reads, the partial sums of its K splits, and the
+ *           error word its bounded waits report to (MOE_ERR_TIMEOUT, read by
+ *           moe_read_device_error).  With NULL the projection runs on the CUDA cores
+ *           instead (FP32 FMA; one fused launch for E <= 32; same selection rule and
+ *           bounds). */
 moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float* W_r,
                            const float* logit_bias, const float* sel_bias, float* logits, float* scores,
                            int32_t* topk_idx, float* gates, int32_t* counts, void* ws, void* stream);

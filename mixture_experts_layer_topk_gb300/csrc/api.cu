@@ -198,15 +198,16 @@ moe_status moe_router_topk(const moe_config* cfg, const moe_bf16* X, const float
   if (!aligned16(X) || !aligned16(W_r) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  uint16_t* wsplit = nullptr;
-  int* err = nullptr;
-  if (ws && cfg->E > 32) {  // the tensor-core logits: W_r's bf16 split and the error word
+  RouterFwdScratch w{};
+  if (ws) {  // the tensor-core logits: W_r's bf16 split, K-split partials, the error word
     const WsLayout L = ws_layout(*cfg);
-    wsplit = ws_ptr<uint16_t>(ws, L.wb);
-    err = ws_ptr<int>(ws, L.err);
+    w.wsplit = ws_ptr<uint16_t>(ws, L.wb);
+    w.part = ws_ptr<float>(ws, L.rlog);
+    w.max_splits = L.rlog_splits;
+    w.err = ws_ptr<int>(ws, L.err);
   }
   return cuda_status(launch_router_topk(*cfg, X, W_r, logit_bias, sel_bias, logits, scores, topk_idx, gates, counts,
-                                        (cudaStream_t)stream, nsm, nullptr, wsplit, err));
+                                        (cudaStream_t)stream, nsm, nullptr, ws ? &w : nullptr));
 }
 
 moe_status moe_router_replay(const moe_config* cfg, const moe_bf16* X, const float* W_r, const float* logit_bias,
@@ -220,15 +221,16 @@ moe_status moe_router_replay(const moe_config* cfg, const moe_bf16* X, const flo
   if (!aligned16(X) || !aligned16(W_r) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  uint16_t* wsplit = nullptr;
-  int* err = nullptr;
-  if (ws && cfg->E > 32) {  // the tensor-core logits: W_r's bf16 split and the error word
+  RouterFwdScratch w{};
+  if (ws) {  // the tensor-core logits: W_r's bf16 split, K-split partials, the error word
     const WsLayout L = ws_layout(*cfg);
-    wsplit = ws_ptr<uint16_t>(ws, L.wb);
-    err = ws_ptr<int>(ws, L.err);
+    w.wsplit = ws_ptr<uint16_t>(ws, L.wb);
+    w.part = ws_ptr<float>(ws, L.rlog);
+    w.max_splits = L.rlog_splits;
+    w.err = ws_ptr<int>(ws, L.err);
   }
   return cuda_status(launch_router_topk(*cfg, X, W_r, logit_bias, nullptr, logits, scores, topk_idx, gates, counts,
-                                        (cudaStream_t)stream, nsm, topk_in, wsplit, err));
+                                        (cudaStream_t)stream, nsm, topk_in, ws ? &w : nullptr));
 }
 
 moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* topk_idx, const int32_t* counts,

@@ -21,8 +21,10 @@ struct WsLayout {
   size_t dlogits;       // float[T * E]
   size_t rbwd_part;     // E <= 32: float[splits * E * H] token-split partials of dW_r
   int rbwd_splits;
-  // E > 32 (router GEMMs on the tensor cores, exact three-term bf16 splits):
-  size_t wb;            // bf16[3Ep * H]    W_r row blocks: hi, mid, lo (router forward) or hi, mid, hi (dX_router)
+  // router GEMMs on the tensor cores (exact three-term bf16 splits):
+  size_t wb;            // bf16[3Ep * H]    W_r row blocks: hi, mid, lo (router forward) or hi, mid, hi (dX_router, E > 32)
+  size_t rlog;          // float[(router_max_splits - 1) * T * E]  K-split partial logits of the router forward
+  int rlog_splits;
   size_t dl_rows;       // bf16[3Tp * Ep]   dlogits row blocks hi, mid, lo (dW_r)
   size_t dl_cols;       // bf16[T * 3Ep]    dlogits column blocks hi, hi, mid (dX_router)
   int Tp, Ep;
@@ -54,6 +56,17 @@ inline int router_bwd_splits(const moe_config& c) {
   return s < kmax ? s : kmax;
 }
 
+// Router forward on the tensor cores: a tile is 128 tokens x router_tile_n(E) experts;
+// small problems split K (at most 8 ways) so that the tiles fill the GPU's SMs (sized for
+// up to 160 SMs); the partial sums are added in a fixed order by the routing pass.
+inline int router_tile_n(int E) { return E <= 32 ? 32 : (E <= 64 ? 64 : 128); }
+inline int router_max_splits(const moe_config& c) {
+  const int bn = router_tile_n(c.E);
+  const int tiles = ((c.T + 127) / 128) * ((c.E + bn - 1) / bn);
+  int s = tiles > 0 ? 160 / tiles : 1;
+  return s < 1 ? 1 : (s > 8 ? 8 : s);
+}
+
 inline WsLayout ws_layout(const moe_config& c) {
   WsLayout L;
   const size_t nch = (size_t)(c.T + kChunk - 1) / kChunk;
@@ -73,7 +86,10 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.Ep = (c.E + 31) / 32 * 32;
   const bool tc = c.E > 32;
   L.wb = o;
-  if (tc) o = align256(o + (size_t)3 * L.Ep * c.H * 2);
+  o = align256(o + (size_t)3 * L.Ep * c.H * 2);
+  L.rlog_splits = router_max_splits(c);
+  L.rlog = o;
+  o = align256(o + (size_t)(L.rlog_splits - 1) * c.T * c.E * sizeof(float));
   L.dl_rows = o;
   if (tc) o = align256(o + (size_t)3 * L.Tp * L.Ep * 2);
   L.dl_cols = o;

@@ -1228,7 +1228,8 @@ cudaError_t launch_router_dwr_tc(int T, int Tp, int H, int E, int Ep, const uint
 }
 
 // dX_r[T,H] (fp32) = dlA[T,3Ep] . WB[3Ep,H]: the products hi.hi + hi.mid + mid.hi of the bf16
-// splits of dlogits and W_r (relative error ~2^-16; dX_r is added into a bf16 dX).
+// splits of dlogits and W_r (relative error ~2^-16; dX_r is added into a bf16 dX).  K runs to
+// the next multiple of 64; the maps read zeros past 3*Ep.
 cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const uint16_t* WB, float* dXr, int* err,
                                 int nsm, cudaStream_t st) {
   const int bn = H % 256 == 0 ? 256 : 128;
@@ -1237,7 +1238,7 @@ cudaError_t launch_router_dx_tc(int T, int H, int Ep, const uint16_t* dlA, const
       !map_out_f32(&md, dXr, H, T, 1))
     return cudaErrorInvalidValue;
   GemmArgs g{};
-  g.E = 1; g.K = 3 * Ep; g.n_tiles = H / bn; g.dense_rows = T; g.err = err;
+  g.E = 1; g.K = (3 * Ep + 63) / 64 * 64; g.n_tiles = H / bn; g.dense_rows = T; g.err = err;
   const int tiles = ((T + 127) / 128) * g.n_tiles;
   return bn == 256 ? launch<MODE_DGRAD, EPI_F32, 256>(ma, mb, md, g, tiles, nsm, st)
                    : launch<MODE_DGRAD, EPI_F32, 128>(ma, mb, md, g, tiles, nsm, st);

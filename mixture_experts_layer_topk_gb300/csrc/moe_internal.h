@@ -26,6 +26,14 @@ struct Fp8Op {
   const uint8_t* sc;
 };
 
+// Workspace pieces of the router forward on the tensor cores.
+struct RouterFwdScratch {
+  uint16_t* wsplit;  // [3*Ep, H] bf16 split of W_r (row blocks hi, mid, lo)
+  float* part;       // [max_splits-1, T, E] K-split partial logits
+  int max_splits;
+  int* err;          // device error word
+};
+
 // Workspace pieces of the router backward.
 struct RouterBwdScratch {
   float* dl;          // [T,E] fp32 dlogits
@@ -40,13 +48,13 @@ struct RouterBwdScratch {
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
                                int32_t* counts, cudaStream_t st, int nsm, const int32_t* given = nullptr,
-                               uint16_t* wsplit = nullptr, int* err = nullptr);
-// E > 32: P = X W_r^T on the tensor cores from wsplit = [3*Ep,H] bf16 (row blocks hi,
-// mid, lo of W_r).  With router_tc_ksplits(T,E,nsm) == 2 the two K halves go to P0 and
-// P1 (to be added), else the whole product to P0.
-int router_tc_ksplits(int T, int E, int nsm);
+                               const RouterFwdScratch* w = nullptr);
+// P = X W_r^T on the tensor cores from wsplit = [3*Ep,H] bf16 (row blocks hi, mid, lo of
+// W_r), split over K: split 0 into P0, split s > 0 into Pn + (s-1)*T*E; the routing pass
+// adds them in that order.  router_tc_splits: how many splits (1..max_splits).
+int router_tc_splits(int T, int H, int E, int nsm, int max_splits);
 cudaError_t launch_router_logits_tc(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0,
-                                    float* P1, int* err, int nsm, cudaStream_t st);
+                                    float* Pn, int splits, int* err, cudaStream_t st);
 cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const float* Wr, const float* logits,
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
                               float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,

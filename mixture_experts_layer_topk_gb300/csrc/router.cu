@@ -40,7 +40,9 @@ struct RouteArgs {
   float gate_scale;
   int n_group, topk_group, group_score;
   const int32_t* given;  // router replay: the selection to use instead of top-k (nullable)
-  int halves;            // k_route_rows: the product is split in two K halves (logits + scores)
+  // k_route_rows: the product is logits + the nmore partial [T,E] sums at more (fixed order)
+  const float* more;
+  int nmore;
 };
 
 // Order-preserving map of an fp32 key to uint32: a < b as floats iff ord_key(a) <
@@ -409,10 +411,10 @@ __global__ void __launch_bounds__(256) k_route_rows(RouteArgs a) {
   __syncthreads();
   const int E = a.E;
   for (int t = blockIdx.x * 8 + warp; t < a.T; t += gridDim.x * 8) {
-    // the product (or its first K half) is in logits, the second half (if any) in scores
+    // the product is split over K: logits holds the first part, `more` the others
     for (int e = lane; e < E; e += 32) {
       float p = a.logits[(size_t)t * E + e];
-      if (a.halves == 2) p += a.scores[(size_t)t * E + e];
+      for (int s = 0; s < a.nmore; ++s) p += a.more[((size_t)s * a.T + t) * E + e];
       lrows[warp][e] = p + (a.logit_bias ? a.logit_bias[e] : 0.f);
     }
     __syncwarp();
@@ -439,7 +441,8 @@ cudaError_t launch_two_pass(RouteArgs a, cudaStream_t st, int nsm) {
   k_router_gemm<BE><<<g1, 256, 0, st>>>(a.X, a.Wr, a.T, a.H, a.E, a.logits, a.scores);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  a.halves = 2;
+  a.more = a.scores;  // the second K half; each warp reads its token's row before overwriting it
+  a.nmore = 1;
   return launch_route_rows<V>(a, st, nsm);
 }
 
@@ -720,32 +723,38 @@ struct Bf16In {
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
                                const float* sel_bias, float* logits, float* scores, int32_t* topk_idx, float* gates,
                                int32_t* counts, cudaStream_t st, int nsm, const int32_t* given,
-                               uint16_t* wsplit, int* err) {
+                               const RouterFwdScratch* w) {
   RouteArgs a{X,       Wr,    logit_bias, sel_bias, logits, scores,  topk_idx,     gates,         counts,
               c.T,     c.H,   c.E,        c.k,      c.score_fn, c.renorm, c.gate_scale, c.n_group, c.topk_group,
-              c.group_score, given, 1};
+              c.group_score, given, nullptr, 0};
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
   if (e != cudaSuccess) return e;
   if (c.T == 0) return cudaSuccess;
-  if (c.E <= 8) return launch_small<8, 2, 1024>(a, st, nsm);
-  if (c.E <= 16) return launch_small<16, 2, 512>(a, st, nsm);
-  if (c.E <= 32) return launch_small<32, 1, 256>(a, st, nsm);
-  // E > 32 with a workspace: the logits on the tensor cores from the exact bf16 split of
-  // W_r, block sums promoted to FP32 registers every 64 columns of K (router_tc.cu),
-  // then one warp per token routes.
-  if (wsplit) {
+  // With a workspace: the logits on the tensor cores from the exact bf16 split of W_r,
+  // block sums promoted to FP32 registers every 64 columns of K, the K splits' partial
+  // sums added by the routing pass (one warp per token).
+  if (w) {
     const int Ep = (c.E + 31) / 32 * 32;
     int blocks = (int)(((int64_t)Ep * c.H + 255) / 256);
     blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
-    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, Ep, wsplit, nullptr);
+    k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, Ep, w->wsplit, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_router_logits_tc(c.T, c.H, c.E, Ep, X, wsplit, logits, scores, err, nsm, st)) != cudaSuccess)
+    const int splits = router_tc_splits(c.T, c.H, c.E, nsm, w->max_splits);
+    if ((e = launch_router_logits_tc(c.T, c.H, c.E, Ep, X, w->wsplit, logits, w->part, splits, w->err, st)) !=
+        cudaSuccess)
       return e;
-    a.halves = router_tc_ksplits(c.T, c.E, nsm);
+    a.more = w->part;
+    a.nmore = splits - 1;
+    if (c.E <= 32) return launch_route_rows<1>(a, st, nsm);
     if (c.E <= 64) return launch_route_rows<2>(a, st, nsm);
     if (c.E <= 128) return launch_route_rows<4>(a, st, nsm);
     return launch_route_rows<8>(a, st, nsm);
   }
+  // Without a workspace: E <= 32 in one fused launch (the projection on the CUDA cores,
+  // W_r staged through shared memory); larger E as below.
+  if (c.E <= 8) return launch_small<8, 2, 1024>(a, st, nsm);
+  if (c.E <= 16) return launch_small<16, 2, 512>(a, st, nsm);
+  if (c.E <= 32) return launch_small<32, 1, 256>(a, st, nsm);
   // Without a workspace: an FP32 register-tiled GEMM on the CUDA cores, then the
   // routing pass.
   if (c.E <= 64) return launch_two_pass<64, 2>(a, st, nsm);

@@ -1,4 +1,4 @@
-// Router logits on the tensor cores, for E > 32.
+// Router logits on the tensor cores (every E, when the call has a workspace).
 //
 // "Scalable Training of Mixture-of-Experts Models with Megatron Core" (summary
 // page, "Method"): the router projection is kept in FP32.  Here P = X W_r^T is
@@ -14,13 +14,14 @@
 // in-MMA error is then that of a 64-term partial, and the running sum is an
 // ordinary FP32 sum over H/64 blocks.
 //
-// One CTA per 128-token x 128-expert tile (optionally one of two K halves when
-// the tiles alone would fill less than half the GPU), 6 warps: warp 0 issues
-// the TMA loads of X and the three W_r splits into a 3-stage ring, warp 1
-// allocates tensor memory (two 128-column block accumulators) and issues the
-// MMAs from one thread, warps 2-5 drain the block sums, one token row per
-// thread.  Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT
-// in the device error word and the CTA unwinds.
+// One CTA per 128-token x BN-expert tile (BN = 32, 64 or 128 by E) and K split (up
+// to 8 splits when the tiles alone would leave SMs idle; split s writes its own
+// partial [T,E] sum, added in a fixed order by the routing pass), 6 warps: warp 0
+// issues the TMA loads of X and the three W_r splits into a ring of stages, warp 1
+// allocates tensor memory (two BN-column block accumulators) and issues the MMAs
+// from one thread, warps 2-5 drain the block sums, one token row per thread.
+// Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT in the device
+// error word and the CTA unwinds.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -31,27 +32,34 @@ namespace moe {
 namespace {
 
 constexpr int kRtBM = 128;                  // tokens per tile (MMA M, tensor-memory lanes)
-constexpr int kRtBN = 128;                  // experts per tile (MMA N)
 constexpr int kRtBK = 64;                   // X columns per stage: 128 bytes of bf16
-constexpr int kRtST = 3;                    // stages
 constexpr int kRtA = kRtBM * 128;           // X tile bytes
-constexpr int kRtB = kRtBN * 128;           // bytes of one split's W tile
-constexpr int kRtStage = kRtA + 3 * kRtB;   // 64 KB
 constexpr int kRtThreads = 192;
-constexpr size_t kRtSmem = 1024 + (size_t)kRtST * kRtStage + 256;
+
+// BN experts per tile (MMA N); a stage holds the X tile and the three splits' W tiles
+template <int BN>
+struct RtGeo {
+  static constexpr int B = BN * 128;                    // bytes of one split's W tile
+  static constexpr int STAGE = kRtA + 3 * B;            // 28, 40 or 64 KB
+  static constexpr int ST = BN == 128 ? 3 : (BN == 64 ? 4 : 6);
+  static constexpr size_t SMEM = 1024 + (size_t)ST * STAGE + 256;
+};
 
 struct RouterTcArgs {
   int T, E, Ep;
   int nkb;      // 64-column blocks of X in all of K
   int kb_per;   // blocks per K split
   float* P0;    // split 0 (or the whole product): [T,E]
-  float* P1;    // split 1: [T,E]
+  float* Pn;    // splits 1..: [splits-1][T,E]
   int* err;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_logits_tc(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                        const RouterTcArgs a) {
+  using G = RtGeo<BN>;
+  constexpr int kRtBN = BN, kRtST = G::ST, kRtB = G::B, kRtStage = G::STAGE;
   constexpr uint32_t IDESC = idesc_bf16(kRtBM, kRtBN, 0, 0);
   constexpr uint32_t TMEM_COLS = 2 * kRtBN;
   extern __shared__ uint8_t smem_raw[];
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     const int t = m0 + r;
     if (ok && t < a.T) {
-      float* P = (blockIdx.z ? a.P1 : a.P0) + (size_t)t * a.E;
+      float* P = (blockIdx.z ? a.Pn + (size_t)(blockIdx.z - 1) * a.T * a.E : a.P0) + (size_t)t * a.E;
       if ((a.E & 3) == 0) {
 #pragma unroll
         for (int c = 0; c < kRtBN; c += 4)
@@ -207,8 +215,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 }
 
 // 2D bf16 tensor map over a row-major [rows, cols] matrix, boxes of 64 columns x
-// 128 rows in the 128-byte swizzle layout the MMA descriptors expect.
-bool map_rows_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// box_rows rows in the 128-byte swizzle layout the MMA descriptors expect.
+bool map_rows_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void* p = nullptr;
@@ -220,40 +228,56 @@ bool map_rows_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t row
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   cuuint64_t gd[2] = {cols, rows}, gs[1] = {cols * 2};
-  cuuint32_t bd[2] = {(cuuint32_t)kRtBK, (cuuint32_t)kRtBM}, es[2] = {1, 1};
+  cuuint32_t bd[2] = {(cuuint32_t)kRtBK, box_rows}, es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs, bd, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-int router_tc_ksplits(int T, int E, int nsm) {
-  const int tiles = ((T + kRtBM - 1) / kRtBM) * ((E + kRtBN - 1) / kRtBN);
-  return 2 * tiles <= nsm ? 2 : 1;
-}
-
-cudaError_t launch_router_logits_tc(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0,
-                                    float* P1, int* err, int nsm, cudaStream_t st) {
+template <int BN>
+cudaError_t launch_bn(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0, float* Pn,
+                      int splits, int* err, cudaStream_t st) {
+  using G = RtGeo<BN>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kRtSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_router_logits_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)G::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   CUtensorMap mx, mw;
-  if (!map_rows_bf16(&mx, X, H, T) || !map_rows_bf16(&mw, wsplit, H, 3 * (uint64_t)Ep))
+  if (!map_rows_bf16(&mx, X, H, T, kRtBM) || !map_rows_bf16(&mw, wsplit, H, 3 * (uint64_t)Ep, BN))
     return cudaErrorInvalidValue;
   RouterTcArgs a{};
   a.T = T; a.E = E; a.Ep = Ep;
   a.nkb = (H + kRtBK - 1) / kRtBK;
-  const int splits = router_tc_ksplits(T, E, nsm);
   a.kb_per = (a.nkb + splits - 1) / splits;
-  a.P0 = P0; a.P1 = P1; a.err = err;
-  dim3 grid((T + kRtBM - 1) / kRtBM, (E + kRtBN - 1) / kRtBN, splits);
-  k_router_logits_tc<<<grid, kRtThreads, kRtSmem, st>>>(mx, mw, a);
+  a.P0 = P0; a.Pn = Pn; a.err = err;
+  dim3 grid((T + kRtBM - 1) / kRtBM, (E + BN - 1) / BN, splits);
+  k_router_logits_tc<BN><<<grid, kRtThreads, G::SMEM, st>>>(mx, mw, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int router_tc_splits(int T, int H, int E, int nsm, int max_splits) {
+  const int bn = E <= 32 ? 32 : (E <= 64 ? 64 : 128);
+  const int tiles = ((T + kRtBM - 1) / kRtBM) * ((E + bn - 1) / bn);
+  int s = tiles > 0 ? nsm / tiles : 1;
+  const int nkb = (H + kRtBK - 1) / kRtBK;
+  s = s < max_splits ? s : max_splits;
+  s = s < nkb ? s : nkb;
+  s = s < 1 ? 1 : s;
+  // every split gets at least one block: ceil(nkb / s) * (s - 1) < nkb
+  while (s > 1 && ((nkb + s - 1) / s) * (s - 1) >= nkb) --s;
+  return s;
+}
+
+cudaError_t launch_router_logits_tc(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0,
+                                    float* Pn, int splits, int* err, cudaStream_t st) {
+  if (E <= 32) return launch_bn<32>(T, H, E, Ep, X, wsplit, P0, Pn, splits, err, st);
+  if (E <= 64) return launch_bn<64>(T, H, E, Ep, X, wsplit, P0, Pn, splits, err, st);
+  return launch_bn<128>(T, H, E, Ep, X, wsplit, P0, Pn, splits, err, st);
 }
 
 }  // namespace moe

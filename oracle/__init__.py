@@ -172,6 +172,17 @@ def expert_wgrad(c: OraCfg, inp: dict, topk_idx, gates_, expert: int, kept=None)
     return dW13, dW2
 
 
+def router_dlogits(c: OraCfg, logits, topk_idx, gates_, dgates):
+    """dlogits [T,E] (float64): the gates' exact gradient w.r.t. the logits for the given
+    selection, applied to dgates [T,k]."""
+    dl = np.empty((c.T, c.E), np.float64)
+    _load().ora_router_dlogits(ctypes.byref(c), _p(np.ascontiguousarray(logits, np.float64)),
+                               _p(np.ascontiguousarray(topk_idx, np.int32)),
+                               _p(np.ascontiguousarray(gates_, np.float64)),
+                               _p(np.ascontiguousarray(dgates, np.float64)), _p(dl))
+    return dl
+
+
 def router_wgrad(c: OraCfg, X, dlogits):
     """dW_r [E,H] and dlogit_bias [E] (float64) from the dlogits of all T tokens."""
     dWr = np.empty((c.E, c.H), np.float64)

@@ -723,6 +723,18 @@ void ora_expert_wgrad_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t*
   }
 }
 
+// Router logit gradients for given gate gradients (summary page, "Method": the router
+// is differentiated through its gates): per token, the exact gradient of the gates with
+// respect to the logits for the given selection (token_dlogits), applied to dgates.
+// logits [T,E], gates [T,k], dgates [T,k], dlogits [T,E] (double); topk_idx [T,k].
+void ora_router_dlogits(const ora_cfg* cp, const double* logits, const int32_t* topk_idx, const double* gates,
+                        const double* dgates, double* dlogits) {
+  const ora_cfg c = *cp;
+  for (int64_t t = 0; t < c.T; ++t)
+    token_dlogits(c, logits + (size_t)t * c.E, topk_idx + (size_t)t * c.k, gates + (size_t)t * c.k,
+                  dgates + (size_t)t * c.k, dlogits + (size_t)t * c.E);
+}
+
 // Router weight gradients from the double dlogits of all T tokens:
 // dW_r[e,h] = sum_t dl[t,e] x[t,h];  dlogit_bias[e] = sum_t dl[t,e].
 void ora_router_wgrad(const ora_cfg* cp, const uint16_t* X, const double* dlogits, double* dWr,

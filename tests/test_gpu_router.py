@@ -1,10 +1,11 @@
-"""Router projection for E > 32: the tensor-core path (taken when the call has a
-workspace) and the FP32 CUDA-core path (no workspace), each against the oracle's
-double logits, on shapes that cover both K-split settings of the tensor-core
-launch (two K halves when the tiles fill less than half the GPU, else one),
-ragged token counts, expert counts that are not a multiple of the 128-expert
-tile, and more than one expert tile.  Selections are bit-exact against the
-oracle's float32 selection on each path's own logits and scores.
+"""Router projection: the tensor-core path (taken when the call has a workspace)
+and the CUDA-core path (no workspace: one fused launch for E <= 32, an FP32 GEMM
+for larger E), each against the oracle's double logits, on shapes that cover
+one to eight K splits of the tensor-core launch (partial sums added in a fixed
+order), the 32-, 64- and 128-expert tiles, ragged token counts, expert counts
+that are not a multiple of the tile, and more than one expert tile.  Selections
+are bit-exact against the oracle's float32 selection on each path's own logits
+and scores.
 """
 import numpy as np
 import pytest
@@ -33,6 +34,18 @@ CASES = {
                              sel_bias=True),
     # skewed logit bias (bias enters the logits)
     "e64-skew": S.Workload("e64-skew", T=2000, H=1024, E=64, k=4, F=128, skew=True),
+    # the Mixtral-style router shape: 32 token tiles of 8 experts, several K splits
+    "e8-mixtral-shape": S.Workload("e8-mixtral-shape", T=4096, H=4096, E=8, k=2, F=128),
+    # few tiles, up to eight K splits; sigmoid with groups
+    "e16-groups-splits": S.Workload("e16-groups-splits", T=300, H=1024, E=16, k=3, F=128, score_fn=1, renorm=0,
+                                    n_group=4, topk_group=2),
+    # one expert, one token tile, two K blocks
+    "e1-k1": S.Workload("e1-k1", T=200, H=128, E=1, k=1, F=128),
+    # 96 experts: three 32-row blocks per split, K of the dX_router product (3 x 96) not a
+    # multiple of 64
+    "e96": S.Workload("e96", T=700, H=512, E=96, k=6, F=128),
+    # 32 experts (a full 32-expert tile), ragged tokens
+    "e32-ragged": S.Workload("e32-ragged", T=1000, H=768, E=32, k=4, F=128),
 }
 
 
@@ -87,7 +100,7 @@ def test_router_tensor_path_promotes_block_sums():
     assert logit_rel_err(r["logits"], logits) < 2e-6
 
 
-@pytest.mark.parametrize("name", ["e128-longk", "e64-skew"])
+@pytest.mark.parametrize("name", ["e128-longk", "e64-skew", "e96"])
 def test_router_backward_products(name):
     """dX_router = dlogits W_r and dW_r = dlogits^T X of the layer's backward (tensor-core
     products from bf16 splits for E > 32) against the oracle's dlogits, each on its own.
@@ -108,3 +121,42 @@ def test_router_backward_products(name):
     assert slice_rel_err(layer.dX_router.cpu().numpy(), dxr) < 2e-2
     dWr, _ = O.router_wgrad(c, inp["X"], tk["dlogits"])
     assert slice_rel_err(layer.dW_r.cpu().numpy(), dWr) < 2e-2
+
+
+@pytest.mark.parametrize("name", ["e8-mixtral-shape", "e40-ragged", "e64-skew", "e96", "e128-longk", "e256-groups"])
+def test_router_backward_exact(name):
+    """moe_router_topk_bwd on its own, with seeded gate gradients: dX_router = dlogits W_r,
+    dW_r = dlogits^T X and dlogit_bias = sum_t dlogits against the oracle's double dlogits
+    (its exact gate Jacobian on its own logits and the GPU's selection).  Bounds: dX_router
+    2e-4 (three bf16 split products, ~2^-16 each), dW_r 1e-3 (tensor-core FP32 accumulation
+    over the token splits), dlogit_bias 1e-5."""
+    import mixture_experts_layer_topk_gb300 as M
+    w = CASES[name]
+    inp = S.host_inputs(w, weights=False)
+    cfg = M.config_from(w)
+    T, E, k, H = w.T, w.E, w.k, w.H
+    X, W_r = to_dev(inp["X"]), to_dev(inp["W_r"])
+    lb, sb = to_dev(inp.get("logit_bias")), to_dev(inp.get("sel_bias"))
+    ws = torch.zeros(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    f32, i32 = torch.float32, torch.int32
+    new = lambda *s, dt=f32: torch.full(s, 7, dtype=dt, device="cuda")
+    logits, scores, idx, gates, counts = new(T, E), new(T, E), new(T, k, dt=i32), new(T, k), new(E, dt=i32)
+    M.moe_router_topk(cfg, X, W_r, lb, sb, logits, scores, idx, gates, counts, ws)
+    dgates_h = S.normal_f32(T * k, 1, 99, 1.0).reshape(T, k)
+    dW_r, dlb, dXr = new(E, H), new(E), new(T, H)
+    M.moe_router_topk_bwd(cfg, X, W_r, logits, scores, idx, gates, to_dev(dgates_h), dW_r,
+                          dlb if lb is not None else None, dXr, ws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_error(ws) == 0
+    c = O.cfg(w)
+    lg, sc = logits.cpu().numpy(), scores.cpu().numpy()
+    sel = idx.cpu().numpy()
+    assert np.array_equal(sel, O.select(c, lg, sc, inp.get("sel_bias")))
+    lo, _ = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
+    dl = O.router_dlogits(c, lo, sel, O.gates(c, lo, sel), dgates_h.astype(np.float64))
+    dxr = dl @ np.asarray(inp["W_r"], np.float64)
+    assert slice_rel_err(dXr.cpu().numpy(), dxr) < 2e-4
+    dWr, dlb_o = O.router_wgrad(c, inp["X"], dl)
+    assert slice_rel_err(dW_r.cpu().numpy(), dWr) < 1e-3
+    if lb is not None:
+        assert slice_rel_err(dlb.cpu().numpy(), dlb_o, 1) < 1e-5

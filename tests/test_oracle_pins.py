@@ -172,6 +172,27 @@ def test_gates_closed_form(score_fn, renorm, scale):
             assert abs(g[t].sum() - scale) < 1e-12
 
 
+@pytest.mark.parametrize("score_fn,renorm,scale", [(0, 1, 1.0), (0, 0, 1.0), (1, 1, 2.5), (1, 0, 1.0)])
+def test_router_dlogits_finite_differences(score_fn, renorm, scale):
+    """router_dlogits is the gradient of <dgates, gates(logits)> for a fixed selection:
+    central differences of the (closed-form pinned) gates, one logit column at a time."""
+    w = small(T=6, E=8, k=3, score_fn=score_fn, renorm=renorm, gate_scale=scale)
+    inp = inputs(w)
+    c = O.cfg(w)
+    logits, scores = O.router(c, inp["X"], inp["W_r"])
+    idx = O.select(c, logits, scores)
+    g = O.gates(c, logits, idx)
+    dg = np.random.default_rng(3).standard_normal((w.T, w.k))
+    dl = O.router_dlogits(c, logits, idx, g, dg)
+    h = 1e-6
+    for e in range(w.E):
+        lp, lm = logits.copy(), logits.copy()
+        lp[:, e] += h
+        lm[:, e] -= h
+        fd = ((O.gates(c, lp, idx) - O.gates(c, lm, idx)) * dg).sum(axis=1) / (2 * h)
+        assert np.allclose(dl[:, e], fd, rtol=1e-6, atol=1e-8), (e, dl[:, e], fd)
+
+
 def test_router_logit_bias_enters_logits():
     w = small(T=16, E=8, k=2, skew=True)
     inp = inputs(w)
