@@ -3,12 +3,14 @@
 // "Scalable Training of Mixture-of-Experts Models with Megatron Core" (summary
 // page, "Method"): the router is a learned linear projection of the hidden
 // states, kept in FP32, followed by softmax or sigmoid scoring and top-k
-// selection.  The kernels here fuse the projection (an FP32 GEMV / skinny
-// GEMM), the scoring, the optional group limit, the top-k (warp shuffles) and
-// the gate computation into one launch for E <= 32; for larger E the projection
-// runs on the tensor cores (router_tc.cu: exact bf16 split of W_r, block sums
-// promoted to FP32 registers) followed by a routing pass; without a workspace it
-// is a register-tiled split-K FP32 GEMM on the CUDA cores instead.
+// selection.  With a workspace the projection runs on the tensor cores
+// (router_tc.cu: exact bf16 split of W_r, block sums promoted to FP32 registers)
+// and a routing pass (one warp per token: scores, optional group limit, top-k by
+// warp reductions, gates, histogram) follows.  Without one, the projection runs
+// on the CUDA cores: fused with the routing into one launch for E <= 32, a
+// register-tiled split-K FP32 GEMM for larger E.  The backward's products (dW_r,
+// dX_router) run on the tensor cores from bf16 splits for E > 32 (for small E they
+// are HBM-bound either way, and the CUDA-core kernels take fewer launches).
 //
 // Selection rule: key = logit (+ sel_bias) for softmax, sigmoid(logit)
 // (+ sel_bias) for sigmoid, formed in FP32; the k experts are listed in
@@ -772,7 +774,7 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
     if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, sizeof(float) * c.E, st);
     return e;
   }
-  const bool tc = c.E > 32;  // large E: the three router-gradient products on the tensor cores
+  const bool tc = c.E > 32;  // large E: the router-gradient products on the tensor cores
   RouteBwdArgs a{logits, topk_idx, gates, dgates, w.dl, c.T, c.E, c.k, c.score_fn, c.renorm, c.gate_scale,
                  tc ? w.dl_rows : nullptr, tc ? w.dl_cols : nullptr, w.Tp, w.Ep};
   if (tc) {
