@@ -48,8 +48,13 @@ struct Geo {
   static constexpr int KSTEP = FP8 ? 32 : 16;     // K of one MMA instruction
   static constexpr int THREADS = FP8 ? 320 : 192; // + 4 scale-factor warps for FP8
 };
-constexpr int kStagingBytes = 16384;
-constexpr int kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
+constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
+constexpr int kEpiBarrier = 1;  // named barrier of the first epilogue warpgroup (the second uses 2)
+
+// Threads of a launch: 6 warps, plus 4 scale-factor warps (FP8) or a second epilogue
+// warpgroup (NEPI = 2).
+template <bool FP8, int NEPI>
+constexpr int threads_of() { return FP8 || NEPI == 2 ? 320 : 192; }
 
 enum { MODE_FWD = 0, MODE_DGRAD = 1, MODE_WGRAD = 2 };
 enum { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_F32 = 3 };
@@ -223,13 +228,13 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
 }
 
-template <int MODE, int EPI, int BN, int ST, bool FP8, bool PAIR>
-__global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
+template <int MODE, int EPI, int BN, int ST, bool FP8, bool PAIR, int NEPI>
+__global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapD, const GemmArgs g) {
   using G = Geo<FP8>;
   constexpr int BK = G::BKE;
-  constexpr int kThreads = G::THREADS;
+  constexpr int kThreads = threads_of<FP8, NEPI>();
   constexpr int A_BYTES = BM * 128;
   constexpr int BNL = PAIR ? BN / 2 : BN;  // B rows (N) held by this CTA
   constexpr int B_BYTES = BNL * 128;
@@ -240,13 +245,16 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
                                  : idesc_bf16(PAIR ? 2 * BM : BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
   static_assert(!(PAIR && FP8), "CTA pairs are built for the bf16 path only");
   constexpr bool TMA_OUT = EPI != EPI_SWIGLU;  // outputs leave through the staging buffer and TMA stores
+  static_assert(NEPI == 1 || (NEPI == 2 && MODE == MODE_WGRAD && EPI == EPI_STORE && !FP8),
+                "two epilogue warpgroups are built for the bf16 weight gradients");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
-  // two 8 KB halves, each one [128 rows x 32 bf16] box in the 64-byte swizzle layout
+  // per epilogue warpgroup two 8 KB halves, each one [128 rows x 32 bf16] box in the
+  // 64-byte swizzle layout
   uint8_t* staging = smem + ST * STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + NEPI * kStagingBytes);
   uint64_t* empty = full + ST;
   uint64_t* sf_full = empty + ST;  // FP8: this stage's scale factors are in tensor memory
   uint64_t* acc_full = sf_full + ST;
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], PAIR ? 8 : 4);  // pairs: both CTAs' epilogue warps release
+      mbar_init(&acc_empty[b], (PAIR ? 8 : 4) * NEPI);  // pairs: both CTAs' epilogue warps release
     }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -553,18 +561,23 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         umma_commit(done_bar);
       if (!mbar_wait(done_bar, 0)) set_device_error(g.err, MOE_ERR_TIMEOUT, 5);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + 4 * NEPI) {
     // ------------------------------------------------------------ epilogue
+    // NEPI = 2: warps 2-5 drain the even 32-column chunks of an accumulator and warps
+    // 6-9 the odd ones, each group with its own staging buffer, barrier and leader.
+    const int grp = NEPI == 2 && warp >= 6 ? 1 : 0;
+    uint8_t* const stg = staging + grp * kStagingBytes;
+    const int ebar = kEpiBarrier + grp;
     const int q = warp & 3;
     const int r = q * 32 + lane;  // row within the tile = tensor-memory lane
-    const bool leader = warp == 2 && lane == 0;
+    const bool leader = warp == 2 + 4 * grp && lane == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     int half = 0;  // staging half used by the next box
     // Writes this thread's 32 values into staging half h (64-byte swizzle: 16-byte
     // unit j of row r sits at unit j ^ ((r >> 1) & 3)).
     auto stage_row = [&](int h, const float* v) {
-      uint8_t* base = staging + h * 8192 + r * 64;
+      uint8_t* base = stg + h * 8192 + r * 64;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4*>(base + ((j ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * j);
@@ -572,7 +585,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     // fp32 variant: one [128 rows x 32 fp32] box filling the whole staging buffer in
     // the 128-byte swizzle layout (16-byte unit j of row r sits at unit j ^ (r & 7)).
     auto stage_row_f32 = [&](const float* v) {
-      uint8_t* base = staging + r * 128;
+      uint8_t* base = stg + r * 128;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         *reinterpret_cast<float4*>(base + ((j ^ (r & 7)) << 4)) =
@@ -582,9 +595,9 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
     // (nothing is stored for the missing half of a CTA pair's tile).
     auto publish = [&](int nbox, const int* hx, const int* xs, int y, int z, bool store) {
       fence_proxy_async_smem();
-      named_bar_sync(kEpiBarrier, 128);
+      named_bar_sync(ebar, 128);
       if (leader && store) {
-        for (int b = 0; b < nbox; ++b) tma_store_3d(&mapD, staging + hx[b] * 8192, xs[b], y, z);
+        for (int b = 0; b < nbox; ++b) tma_store_3d(&mapD, stg + hx[b] * 8192, xs[b], y, z);
         bulk_commit_group();
       }
     };
@@ -596,7 +609,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         else
           bulk_wait_group_read<1>();
       }
-      named_bar_sync(kEpiBarrier, 128);
+      named_bar_sync(ebar, 128);
     };
     // The accumulator goes back to the MMA issuer: the leader CTA's barrier, which
     // in a pair also counts the peer's epilogue warps.
@@ -629,7 +642,7 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
         float z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0.f;
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = grp; c < BN / 32; c += NEPI) {
           if constexpr (EPI == EPI_F32) {
             reserve(true);
             stage_row_f32(z);
@@ -647,10 +660,10 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
       }
       // one thread waits (bounded) and shares the outcome, so that all four warps
       // take the same path through the named barriers below
-      if (leader) tmem_holder[1] = mbar_wait(&acc_full[acc], acc_phase) ? 1u : 0u;
-      named_bar_sync(kEpiBarrier, 128);
-      const bool acc_ready = tmem_holder[1] != 0u;
-      named_bar_sync(kEpiBarrier, 128);  // everyone has read the flag before it is reused
+      if (leader) tmem_holder[1 + grp] = mbar_wait(&acc_full[acc], acc_phase) ? 1u : 0u;
+      named_bar_sync(ebar, 128);
+      const bool acc_ready = tmem_holder[1 + grp] != 0u;
+      named_bar_sync(ebar, 128);  // everyone has read the flag before it is reused
       if (!acc_ready) {
         if (leader) set_device_error(g.err, MOE_ERR_TIMEOUT, 6);
         break;
@@ -745,11 +758,16 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
           nch = left < nch ? (left > 1 ? left : 1) : nch;
         }
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
+        if (grp >= nch) {  // no chunk for this group: hand the accumulator back at once
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) release(acc);
+        }
+        for (int c = grp; c < nch; c += NEPI) {
           uint32_t vr[32];
           tmem_ld32(tbase + c * 32, vr);
           tmem_ld_wait();
-          if (c == nch - 1) {
+          if (c + NEPI >= nch) {  // this group's last read of the accumulator
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release(acc);
@@ -845,12 +863,14 @@ __global__ void __launch_bounds__(Geo<FP8>::THREADS, 1)
   }
 }
 
-template <int MODE, int EPI, int BN, bool FP8, bool PAIR = false>
+template <int MODE, int EPI, int BN, bool FP8, bool PAIR = false, int NEPI = 1>
 struct Kern {
   static constexpr int BNL = PAIR ? BN / 2 : BN;
   static constexpr int STAGE = (BM + BNL) * 128;
-  static constexpr int ST = STAGE <= 32768 ? 6 : 4;
-  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + kStagingBytes + (3 * ST + 5) * 8 + 16 + 4 * 260 * 4;
+  // a second epilogue warpgroup's staging buffer takes the room of one operand stage
+  static constexpr int ST = NEPI == 2 ? 5 : (STAGE <= 32768 ? 6 : 4);
+  static constexpr size_t smem =
+      1024 + (size_t)ST * STAGE + NEPI * kStagingBytes + (3 * ST + 5) * 8 + 16 + 4 * 260 * 4;
 };
 
 // ---------------------------------------------------------------- host side
@@ -919,12 +939,12 @@ bool map_out_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid,
   return make_map(m, base, 3, dims, st, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
-template <int MODE, int EPI, int BN, bool FP8 = false, bool PAIR = false>
+template <int MODE, int EPI, int BN, bool FP8 = false, bool PAIR = false, int NEPI = 1>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const GemmArgs& g, int max_tiles,
                    int nsm, cudaStream_t st) {
-  using K = Kern<MODE, EPI, BN, FP8, PAIR>;
+  using K = Kern<MODE, EPI, BN, FP8, PAIR, NEPI>;
   static bool attr = false;
-  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8, PAIR>;
+  auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8, PAIR, NEPI>;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
     if (e != cudaSuccess) return e;
@@ -936,7 +956,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
     const int pairs = max_tiles < nsm / 2 ? max_tiles : nsm / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(Geo<FP8>::THREADS);
+    cfg.blockDim = dim3(threads_of<FP8, NEPI>());
     cfg.dynamicSmemBytes = K::smem;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
@@ -949,7 +969,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
     return cudaLaunchKernelEx(&cfg, kern, a, b, d, g);
   } else {
     const int grid = max_tiles < nsm ? max_tiles : nsm;
-    kern<<<grid, Geo<FP8>::THREADS, K::smem, st>>>(a, b, d, g);
+    kern<<<grid, threads_of<FP8, NEPI>(), K::smem, st>>>(a, b, d, g);
     return cudaGetLastError();
   }
 }
@@ -966,6 +986,14 @@ constexpr bool use_pairs() { return true; }
 // operand is shared by the concurrent tiles, so each byte of the larger one is read
 // from DRAM once.
 inline int wgrad_n_fast(int m, int n) { return m > n ? 1 : 0; }
+
+// Weight gradients whose experts hold few rows (K of a few 64-row blocks per tile) are
+// bound by their epilogue, which writes a 256x256 tile per handful of MMAs: they run
+// with a second epilogue warpgroup (and one operand stage fewer).  Long-K ones keep six
+// operand stages.
+inline bool wgrad_two_epilogues(const GemmShape& s) {
+  return s.dense_rows <= 0 && s.E > 0 && s.rows / s.E < 512;
+}
 
 // pair tiles of a ragged launch: sum over experts of ceil(m tiles / 2) <= max_mtiles / 2 + E
 inline int pair_tiles(const GemmShape& s, int n_tiles) {
@@ -1078,9 +1106,12 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
   g.D = dW2; g.ldd = s.F; g.d_estride = (int64_t)s.H * s.F; g.err = err;
   g.n_fast = wgrad_n_fast(s.H, s.F);
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
-  if (bn == 256 && use_pairs())
-    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(
-        ma, mb, md, g, (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles, s.nsm, st);
+  if (bn == 256 && use_pairs()) {
+    const int pair_tiles = (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles;
+    if (wgrad_two_epilogues(s))
+      return launch<MODE_WGRAD, EPI_STORE, 256, false, true, 2>(ma, mb, md, g, pair_tiles, s.nsm, st);
+    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(ma, mb, md, g, pair_tiles, s.nsm, st);
+  }
   return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
                    : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }
@@ -1107,9 +1138,12 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
     g.gather_rows = s.rows;
   }
   const int tiles = (s.dense_rows > 0 ? 1 : s.E) * g.m_tiles * g.n_tiles;
-  if (bn == 256 && use_pairs())
-    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(
-        ma, mb, md, g, (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles, s.nsm, st);
+  if (bn == 256 && use_pairs()) {
+    const int pair_tiles = (s.dense_rows > 0 ? 1 : s.E) * ((g.m_tiles + 1) / 2) * g.n_tiles;
+    if (wgrad_two_epilogues(s))
+      return launch<MODE_WGRAD, EPI_STORE, 256, false, true, 2>(ma, mb, md, g, pair_tiles, s.nsm, st);
+    return launch<MODE_WGRAD, EPI_STORE, 256, false, true>(ma, mb, md, g, pair_tiles, s.nsm, st);
+  }
   return bn == 256 ? launch<MODE_WGRAD, EPI_STORE, 256>(ma, mb, md, g, tiles, s.nsm, st)
                    : launch<MODE_WGRAD, EPI_STORE, 128>(ma, mb, md, g, tiles, s.nsm, st);
 }
