@@ -145,18 +145,17 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
 // assignments (token-major) are split into 8 contiguous runs, one per warp; a
 // per-warp histogram and a scan over the warps give each run its starting slot per
 // expert, then each warp ranks its run with match_any, so token order is kept.
-// Padding CTAs (blockIdx >= nch): kPadSplit CTAs per expert zero its padding rows.
+// Padding CTAs (blockIdx >= nch): kPadSplit CTAs per expert mark its padding rows in
+// slot_src (-1); k_copy_rows zeroes their rows of Xperm.
 constexpr int kPadSplit = 8;
-__global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx,
+__global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ topk_idx,
                                                  const int32_t* __restrict__ chunk_base,
                                                  const int32_t* __restrict__ counts,
-                                                 const int32_t* __restrict__ offsets, int T, int H, int E, int k,
+                                                 const int32_t* __restrict__ offsets, int T, int E, int k,
                                                  int nch, int cap, int32_t* __restrict__ row_id_map,
-                                                 int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm,
-                                                 int32_t* __restrict__ drop_order,
+                                                 int32_t* __restrict__ slot_src, int32_t* __restrict__ drop_order,
                                                  const int32_t* __restrict__ drop_start) {
   __shared__ int cursor[8][256];
-  const int nvec = H / 8;
   if ((int)blockIdx.x >= nch) {
     const int p = blockIdx.x - nch;
     const int e = p / kPadSplit, part = p % kPadSplit;
@@ -164,11 +163,7 @@ __global__ void __launch_bounds__(256) k_scatter(const uint16_t* __restrict__ X,
     const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
     const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
     const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
-    for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    if (Xperm)
-      for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
-        reinterpret_cast<uint4*>(Xperm)[i] = z;
+    for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;  // (k_copy_rows zeroes their Xperm rows)
     return;
   }
   const int c = blockIdx.x;
@@ -329,10 +324,27 @@ __global__ void __launch_bounds__(1024) k_drop_select(const float* __restrict__ 
 
 // Xperm[row_id_map[t,j]] = X[t]: one warp per token, its k destination rows read once;
 // each lane loads U 16-byte vectors of the row before storing them to every kept row.
+// CTAs past the token range zero the padding rows, kPadSplit CTAs per expert, in the
+// same launch (their writes stream alongside the copy).
 __global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ X,
-                                                   const int32_t* __restrict__ row_id_map, int T, int H, int k,
-                                                   uint16_t* __restrict__ Xperm) {
+                                                   const int32_t* __restrict__ row_id_map,
+                                                   const int32_t* __restrict__ offsets,
+                                                   const int32_t* __restrict__ counts, int T, int H, int k,
+                                                   int tok_blocks, uint16_t* __restrict__ Xperm) {
   constexpr int U = kGatherUnroll;
+  if ((int)blockIdx.x >= tok_blocks) {
+    const int64_t nvec = H / 8;
+    const int p = blockIdx.x - tok_blocks;
+    const int e = p / kPadSplit, part = p % kPadSplit;
+    const int r1e = offsets[e + 1];
+    const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
+    const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
+    const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
+      reinterpret_cast<uint4*>(Xperm)[i] = z;
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -594,17 +606,18 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
                                      chunk_base, drop_start, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the padding CTAs size each segment's tail from the kept counts
-  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(X, topk_idx, chunk_base, kept ? kept : counts, offsets, c.T, c.H,
-                                                   c.E, c.k, nch, cap, row_id_map, slot_src, Xperm, drop_order,
-                                                   drop_start);
+  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(topk_idx, chunk_base, kept ? kept : counts, offsets, c.T, c.E,
+                                                   c.k, nch, cap, row_id_map, slot_src, drop_order, drop_start);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (priority) {
     k_drop_select<<<c.E, 1024, 0, st>>>(priority, drop_order, drop_start, offsets, kept, cap, row_id_map, slot_src,
                                         err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (c.T > 0 && Xperm) {  // no Xperm: the maps only (the grouped GEMM gathers the rows)
-    k_copy_rows<<<(c.T + 7) / 8, 256, 0, st>>>(X, row_id_map, c.T, c.H, c.k, Xperm);
+  if (Xperm) {  // no Xperm: the maps only (the grouped GEMM gathers the rows)
+    const int tb = (c.T + 7) / 8;
+    k_copy_rows<<<tb + c.E * kPadSplit, 256, 0, st>>>(X, row_id_map, offsets, kept ? kept : counts, c.T, c.H, c.k,
+                                                      tb, Xperm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
