@@ -509,27 +509,53 @@ __global__ void __launch_bounds__(256) k_permute_bwd(const uint16_t* __restrict_
   const int my_slot = lane < k ? row_id_map[(size_t)t * k + lane] : 0;
   const int nvec = H / 8;
   for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    // the router and shared-expert terms are loaded first, so that they are in flight
+    // with the expert rows (two rows per step); the sum keeps the order rows, router, shared
+    float4 ra[U], rb[U];
+    uint4 sx[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u + lane;
+      const bool in = v < nvec;
+      if (dXr && in) {
+        const float4* rr = reinterpret_cast<const float4*>(dXr + (size_t)t * H) + 2 * v;
+        ra[u] = __ldg(rr);
+        rb[u] = __ldg(rr + 1);
+      } else {
+        ra[u] = rb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      sx[u] = dXs && in ? __ldg(reinterpret_cast<const uint4*>(dXs + (size_t)t * H) + v) : make_uint4(0, 0, 0, 0);
+    }
     float acc[U][8];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      if (slot < 0) continue;
-      const uint4* src = reinterpret_cast<const uint4*>(dXperm + (size_t)slot * H);
-      uint4 x[U];
+    for (int j = 0; j < k; j += 2) {
+      const int s0 = __shfl_sync(0xffffffffu, my_slot, j);
+      const int s1 = j + 1 < k ? __shfl_sync(0xffffffffu, my_slot, j + 1) : -1;
+      uint4 x0[U], x1[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + 32 * u + lane;
-        x[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        x0[u] = s0 >= 0 && v < nvec ? __ldg(reinterpret_cast<const uint4*>(dXperm + (size_t)s0 * H) + v)
+                                    : make_uint4(0, 0, 0, 0);
+        x1[u] = s1 >= 0 && v < nvec ? __ldg(reinterpret_cast<const uint4*>(dXperm + (size_t)s1 * H) + v)
+                                    : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float f[8];
-        unpack8(x[u], f);
+        if (s0 >= 0) {  // a dropped assignment (capacity) adds nothing
+          unpack8(x0[u], f);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+          for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+        }
+        if (s1 >= 0) {
+          unpack8(x1[u], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
+        }
       }
     }
 #pragma unroll
@@ -537,14 +563,12 @@ __global__ void __launch_bounds__(256) k_permute_bwd(const uint16_t* __restrict_
       const int v = v0 + 32 * u + lane;
       if (v >= nvec) continue;
       if (dXr) {
-        const float4* rr = reinterpret_cast<const float4*>(dXr + (size_t)t * H) + 2 * v;
-        const float4 a = __ldg(rr), b = __ldg(rr + 1);
-        acc[u][0] += a.x; acc[u][1] += a.y; acc[u][2] += a.z; acc[u][3] += a.w;
-        acc[u][4] += b.x; acc[u][5] += b.y; acc[u][6] += b.z; acc[u][7] += b.w;
+        acc[u][0] += ra[u].x; acc[u][1] += ra[u].y; acc[u][2] += ra[u].z; acc[u][3] += ra[u].w;
+        acc[u][4] += rb[u].x; acc[u][5] += rb[u].y; acc[u][6] += rb[u].z; acc[u][7] += rb[u].w;
       }
       if (dXs) {
         float f[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(dXs + (size_t)t * H) + v), f);
+        unpack8(sx[u], f);
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[u][q] += f[q];
       }
