@@ -1,0 +1,51 @@
+"""Host-side logic of the benchmark (no GPU): the recorded DRAM traffic is reported only
+while the grouped GEMM's sources match the ones it was captured on, and the launch counts
+and algorithmic HBM bytes cover every stage the benchmark times."""
+import json
+
+import pytest
+
+import bench
+import moe_synth as S
+
+
+def _write_traffic(tmp_path, digest, nbytes):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"k_grouped_gemm:mixtral": {"source_digest": digest, "bytes_per_step": nbytes, "launches": 6}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+
+
+def test_traffic_record_requires_the_current_kernel_source(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_digest", lambda files=None: "abc")
+    _write_traffic(tmp_path, "abc", 123)
+    assert bench.traffic_record("k_grouped_gemm", "mixtral") == 123
+    assert bench.traffic_record("k_grouped_gemm", "qwen3") is None  # no capture for that workload
+    monkeypatch.setattr(bench, "kernel_digest", lambda files=None: "changed")
+    assert bench.traffic_record("k_grouped_gemm", "mixtral") is None  # the kernel changed since
+
+
+def test_traffic_record_absent_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("k_grouped_gemm", "mixtral") is None
+
+
+def test_kernel_digest_tracks_the_gemm_sources():
+    d = bench.kernel_digest()
+    assert isinstance(d, str) and len(d) == 16
+    assert bench.kernel_digest(("grouped_gemm.cu",)) != d  # common.cuh is part of it
+
+
+@pytest.mark.parametrize("name", sorted(S.WORKLOADS))
+def test_stage_accounting_covers_every_workload(name):
+    w = S.WORKLOADS[name]
+    n = bench.launches_per_step(w)
+    assert isinstance(n, int) and n > 10
+    hb = bench.hbm_bytes(w)
+    for stage in ("permute", "combine", "combine_bwd", "permute_bwd", "router"):
+        assert hb[stage] > 0 and stage in bench.STAGES
+    assert ("quant_w" in hb) == w.fp8
+    # the permute moves X once and writes it k times; the combine backward reads dY once
+    assert hb["permute"] == w.T * w.H * 2 * (1 + w.k)
+    assert hb["combine_bwd"] == w.T * w.H * 2 * (1 + 2 * w.k)
