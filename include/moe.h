@@ -82,8 +82,9 @@ const char* moe_status_string(moe_status s);
 moe_status moe_max_rows(const moe_config* cfg, int64_t* R);
 
 /* Bytes of device workspace all calls of this configuration need.  The
- * workspace holds the device error word, per-chunk routing histograms and the
- * router-gradient scratch.  Initialise it once with moe_workspace_init(). */
+ * workspace holds the device error word, per-chunk routing histograms, the router
+ * forward's bf16 split of W_r and K-split partial logits, and the router-gradient
+ * scratch.  Initialise it once with moe_workspace_init(). */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Zeroes the workspace (including the error word), asynchronously on stream. */
