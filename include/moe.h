@@ -352,11 +352,14 @@ moe_status moe_grouped_swiglu_mlp_bwd_fp8(const moe_config* cfg, const moe_bf16*
  * running inside a memory arena sized once at start-up, a plugin that is handed
  * only its inputs and outputs, or a caller in the middle of recording a CUDA
  * graph (where cudaMalloc is not allowed).
- * Same arguments, outputs and results as moe_permute, minus `ws`.  The scratch
- * it needs lives in a static device array built into the library (512 KiB +
- * 256 B, held by every GPU that loads the library until the process exits),
- * which limits it to ceil(T/128) * E <= 65536 (for example T = 32768 with
- * E = 256); larger configurations return MOE_ERR_WORKSPACE and launch nothing.
+ * Same arguments, outputs and results as moe_permute, minus `ws` (Xperm NULL
+ * writes the maps only, as there).  The scratch it needs lives in a static
+ * device array built into the library (512 KiB + 1.25 KiB, held by every GPU
+ * that loads the library until the process exits), which limits it to
+ * ceil(T/128) * E <= 65536 (for example T = 32768 with E = 256); larger
+ * configurations return MOE_ERR_WORKSPACE and launch nothing.  Each call clears
+ * the part of the array that must start at zero (the error word); the rest is
+ * fully rewritten before it is read.
  * The first call on each device looks up the array's device address with
  * that device current, so make the first call on a device before any stream
  * capture.  Every call shares the one array: calls whose kernels can overlap

@@ -12,16 +12,16 @@ using namespace moe;
 namespace {
 
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // per device; 0 = not looked up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev < 0 || dev >= 64) return 0;
-  if (!cache[dev]) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -247,8 +247,8 @@ moe_status moe_permute(const moe_config* cfg, const moe_bf16* X, const int32_t* 
   const WsLayout L = ws_layout(*cfg);
   const int nsm = num_sms();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  return cuda_status(launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, nullptr, offsets, tile_offsets,
-                                    row_id_map, slot_src, Xperm, ws_ptr<int32_t>(ws, L.chunk_counts),
+  return cuda_status(launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, ws_ptr<int32_t>(ws, L.seg_rows),
+                                    offsets, tile_offsets, row_id_map, slot_src, Xperm, ws_ptr<int32_t>(ws, L.chunk_counts),
                                     ws_ptr<int32_t>(ws, L.chunk_base), nullptr, nullptr, ws_ptr<int>(ws, L.err), nsm,
                                     (cudaStream_t)stream));
 }

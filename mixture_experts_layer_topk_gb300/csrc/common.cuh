@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -18,6 +20,7 @@ struct WsLayout {
   size_t err;           // int32[64]: [0] error code, [1] detail
   size_t chunk_counts;  // int32[nchunks * E]
   size_t chunk_base;    // int32[nchunks * E]
+  size_t seg_rows;      // int32[E]: rows each expert keeps, as the dispatch scan counted them
   size_t dlogits;       // float[T * E]
   size_t rbwd_part;     // E <= 32: float[splits * E * H] token-split partials of dW_r
   int rbwd_splits;
@@ -77,6 +80,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + nch * c.E * sizeof(int32_t));
   L.chunk_base = o;
   o = align256(o + nch * c.E * sizeof(int32_t));
+  L.seg_rows = o;
+  o = align256(o + (size_t)c.E * sizeof(int32_t));
   L.dlogits = o;
   o = align256(o + (size_t)c.T * c.E * sizeof(float));
   L.rbwd_splits = router_bwd_splits(c);
@@ -102,6 +107,22 @@ inline WsLayout ws_layout(const moe_config& c) {
   o = align256(o + ((size_t)c.T * c.k + (size_t)c.E * (c.align - 1)) * (size_t)(c.F / 128) * sizeof(float));
   L.total = o;
   return L;
+}
+
+// cudaFuncSetAttribute acts on the current device only, so the raised dynamic
+// shared-memory limit of a kernel is remembered per device (bit d of `done` for device
+// d < 64).  Two threads may both set it the first time; that is harmless.
+template <typename Kernel>
+inline cudaError_t raise_smem_limit(std::atomic<uint64_t>& done, Kernel kern, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 template <typename T>

@@ -943,13 +943,9 @@ template <int MODE, int EPI, int BN, bool FP8 = false, bool PAIR = false, int NE
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const GemmArgs& g, int max_tiles,
                    int nsm, cudaStream_t st) {
   using K = Kern<MODE, EPI, BN, FP8, PAIR, NEPI>;
-  static bool attr = false;
+  static std::atomic<uint64_t> attr{0};
   auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8, PAIR, NEPI>;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  if (cudaError_t e = raise_smem_limit(attr, kern, K::smem); e != cudaSuccess) return e;
   if (max_tiles <= 0) return cudaSuccess;
   if constexpr (PAIR) {
     // max_tiles counts 256-row pair tiles here; two CTAs (one cluster) per pair tile

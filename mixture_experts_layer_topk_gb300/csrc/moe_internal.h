@@ -59,9 +59,10 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
                               const int32_t* topk_idx, const float* gates, const float* dgates, float* dW_r,
                               float* dlogit_bias, float* dX_router, const RouterBwdScratch& w, int* err, int nsm,
                               cudaStream_t st);
-// cap: per-expert capacity (INT_MAX = dropless); priority [T,k] (nullable): drop
-// the lowest-priority assignments instead of the last ones in token order, which
-// needs kept, drop_order [T*k] and drop_start [E+1].
+// cap: per-expert capacity (INT_MAX = dropless); kept [E] (required) receives the rows
+// each expert keeps, min(histogram total, cap), and sizes the padding; priority [T,k]
+// (nullable): drop the lowest-priority assignments instead of the last ones in token
+// order, which needs drop_order [T*k] and drop_start [E+1].
 cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t* topk_idx, const int32_t* counts,
                            int cap, const float* priority, int32_t* kept, int32_t* offsets, int32_t* tile_offsets,
                            int32_t* row_id_map, int32_t* slot_src, uint16_t* Xperm, int32_t* chunk_counts,

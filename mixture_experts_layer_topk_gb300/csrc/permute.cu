@@ -53,7 +53,10 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const int32_t* __restrict__ 
   for (int e = threadIdx.x; e < E; e += 256) chunk_counts[(size_t)c * E + e] = hist[e];
 }
 
-// One CTA: offsets (aligned segments), tile_offsets, and the per-chunk bases.
+// One CTA: offsets (aligned segments), tile_offsets, the per-chunk bases, and kept[e], the
+// rows expert e keeps (min of its histogram total and the capacity).  The later launches
+// size each segment's padding from kept, so they agree with the slots handed out even when
+// the caller's counts do not match topk_idx (which the scan flags in the error word).
 // G threads per expert each own a contiguous range of chunks.  The chunk histogram
 // is first copied into shared memory with coalesced loads when it fits
 // (kScanStage entries); the per-expert prefix sums run on warp 0 (each lane a run
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
       const int tot = tot_s[x], kt = min(tot, cap);
       if (drop_start) drop_start[x] = od;
       od += tot;
-      if (kept) kept[x] = kt;
+      kept[x] = kt;
       seg_start[x] = oa;
       oa += (kt + align - 1) / align * align;
       ob += (kt + 127) / 128;
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ count
 constexpr int kPadSplit = 8;
 __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ topk_idx,
                                                  const int32_t* __restrict__ chunk_base,
-                                                 const int32_t* __restrict__ counts,
+                                                 const int32_t* __restrict__ kept,
                                                  const int32_t* __restrict__ offsets, int T, int E, int k,
                                                  int nch, int cap, int32_t* __restrict__ row_id_map,
                                                  int32_t* __restrict__ slot_src, int32_t* __restrict__ drop_order,
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
     const int p = blockIdx.x - nch;
     const int e = p / kPadSplit, part = p % kPadSplit;
     const int r1e = offsets[e + 1];
-    const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
+    const int r0e = min(max(offsets[e] + kept[e], offsets[e]), r1e);
     const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
     const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
     for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;  // (k_copy_rows zeroes their Xperm rows)
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(1024) k_drop_select(const float* __restrict__ 
 __global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ X,
                                                    const int32_t* __restrict__ row_id_map,
                                                    const int32_t* __restrict__ offsets,
-                                                   const int32_t* __restrict__ counts, int T, int H, int k,
+                                                   const int32_t* __restrict__ kept, int T, int H, int k,
                                                    int tok_blocks, uint16_t* __restrict__ Xperm) {
   constexpr int U = kGatherUnroll;
   if ((int)blockIdx.x >= tok_blocks) {
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(256) k_copy_rows(const uint16_t* __restrict__ 
     const int p = blockIdx.x - tok_blocks;
     const int e = p / kPadSplit, part = p % kPadSplit;
     const int r1e = offsets[e + 1];
-    const int r0e = min(max(offsets[e] + counts[e], offsets[e]), r1e);
+    const int r0e = min(max(offsets[e] + kept[e], offsets[e]), r1e);
     const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
     const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -608,7 +611,7 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
                            int32_t* row_id_map, int32_t* slot_src, uint16_t* Xperm, int32_t* chunk_counts,
                            int32_t* chunk_base, int32_t* drop_order, int32_t* drop_start, int* err, int nsm,
                            cudaStream_t st) {
-  if (priority && (!kept || !drop_order || !drop_start)) return cudaErrorInvalidValue;
+  if (!kept || (priority && (!drop_order || !drop_start))) return cudaErrorInvalidValue;
   if (!priority) drop_order = drop_start = nullptr;
   const int nch = (c.T + kChunk - 1) / kChunk;
   cudaError_t e;
@@ -618,20 +621,15 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   }
   const size_t scan_smem = nch * c.E <= kScanStage ? sizeof(int) * (size_t)nch * c.E : 0;
   if (scan_smem > 48 * 1024) {
-    static bool attr = false;
-    if (!attr) {
-      if ((e = cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(sizeof(int) * kScanStage))) !=
-          cudaSuccess)
-        return e;
-      attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    if ((e = raise_smem_limit(attr, k_scan, sizeof(int) * kScanStage)) != cudaSuccess) return e;
   }
   k_scan<<<1, 1024, scan_smem, st>>>(counts, chunk_counts, nch, c.E, c.align, cap, kept, offsets, tile_offsets,
                                      chunk_base, drop_start, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // the padding CTAs size each segment's tail from the kept counts
-  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(topk_idx, chunk_base, kept ? kept : counts, offsets, c.T, c.E,
-                                                   c.k, nch, cap, row_id_map, slot_src, drop_order, drop_start);
+  // the padding CTAs size each segment's tail from the kept rows the scan counted
+  k_scatter<<<nch + c.E * kPadSplit, 256, 0, st>>>(topk_idx, chunk_base, kept, offsets, c.T, c.E, c.k, nch, cap,
+                                                   row_id_map, slot_src, drop_order, drop_start);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (priority) {
     k_drop_select<<<c.E, 1024, 0, st>>>(priority, drop_order, drop_start, offsets, kept, cap, row_id_map, slot_src,
@@ -640,8 +638,7 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   }
   if (Xperm) {  // no Xperm: the maps only (the grouped GEMM gathers the rows)
     const int tb = (c.T + 7) / 8;
-    k_copy_rows<<<tb + c.E * kPadSplit, 256, 0, st>>>(X, row_id_map, offsets, kept ? kept : counts, c.T, c.H, c.k,
-                                                      tb, Xperm);
+    k_copy_rows<<<tb + c.E * kPadSplit, 256, 0, st>>>(X, row_id_map, offsets, kept, c.T, c.H, c.k, tb, Xperm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

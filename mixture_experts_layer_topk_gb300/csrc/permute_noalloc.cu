@@ -10,7 +10,7 @@
 // keeps that scratch in a file-scope __device__ array instead, so the call
 // itself allocates nothing.
 //
-// The scratch array (kNoAllocScratchInts 32-bit words, 512 KiB + 256 B) is
+// The scratch array (kNoAllocScratchInts 32-bit words, 512 KiB + 1.25 KiB) is
 // part of the library image: every GPU that loads the library holds it until
 // the process exits.  All calls share it, so calls whose kernels overlap on the
 // GPU (different streams without ordering between them) race on it.
@@ -21,8 +21,10 @@
 
 namespace {
 
-// Layout: [0, 64) error word and detail; then chunk_counts[nch*E]; then chunk_base[nch*E].
-constexpr int64_t kNoAllocScratchInts = 64 + 2 * 65536;
+// Layout: [0, 64) error word and detail; [64, 320) the rows each expert keeps (E <= 256);
+// then chunk_counts[nch*E]; then chunk_base[nch*E], nch*E <= 65536.
+constexpr int64_t kNoAllocMaxChunkExperts = 65536;
+constexpr int64_t kNoAllocScratchInts = 64 + 256 + 2 * kNoAllocMaxChunkExperts;
 
 __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
@@ -59,22 +61,24 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const moe_bf16*
   const moe_status s = moe_max_rows(cfg, &R);  // validates the configuration
   if (s != MOE_OK) return s;
   const bool empty = cfg->T == 0;
-  if ((!X && !empty) || (!topk_idx && !empty) || !counts || !offsets || !tile_offsets || (!row_id_map && !empty) ||
-      !slot_src || !Xperm)
+  // Xperm NULL: the dispatch maps only (X is then not read), as in moe_permute
+  if ((Xperm && !X && !empty) || (!topk_idx && !empty) || !counts || !offsets || !tile_offsets ||
+      (!row_id_map && !empty) || !slot_src)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(Xperm)) return MOE_ERR_INVALID_ARG;
+  if (Xperm && (!aligned16(X) || !aligned16(Xperm))) return MOE_ERR_INVALID_ARG;
   const int64_t nch = ((int64_t)cfg->T + moe::kChunk - 1) / moe::kChunk;
-  if (64 + 2 * nch * cfg->E > kNoAllocScratchInts) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
+  if (nch * cfg->E > kNoAllocMaxChunkExperts) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
   int nsm = 0;
   int32_t* scratch = scratch_on_current_device(&nsm);
   if (!scratch) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the error word must start at zero; the histogram and base arrays are fully rewritten
   if (cudaMemsetAsync(scratch, 0, 64 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  int32_t* chunk_counts = scratch + 64;
+  int32_t* kept = scratch + 64;
+  int32_t* chunk_counts = kept + 256;
   int32_t* chunk_base = chunk_counts + nch * cfg->E;
   const cudaError_t e =
-      moe::launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, nullptr, offsets, tile_offsets, row_id_map,
+      moe::launch_permute(*cfg, X, topk_idx, counts, INT_MAX, nullptr, kept, offsets, tile_offsets, row_id_map,
                           slot_src, Xperm, chunk_counts, chunk_base, nullptr, nullptr, scratch, nsm, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

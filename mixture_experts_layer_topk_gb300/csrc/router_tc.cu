@@ -238,13 +238,8 @@ template <int BN>
 cudaError_t launch_bn(int T, int H, int E, int Ep, const uint16_t* X, const uint16_t* wsplit, float* P0, float* Pn,
                       int splits, int* err, cudaStream_t st) {
   using G = RtGeo<BN>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_logits_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)G::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (cudaError_t e = raise_smem_limit(attr, k_router_logits_tc<BN>, G::SMEM); e != cudaSuccess) return e;
   CUtensorMap mx, mw;
   if (!map_rows_bf16(&mx, X, H, T, kRtBM) || !map_rows_bf16(&mw, wsplit, H, 3 * (uint64_t)Ep, BN))
     return cudaErrorInvalidValue;

@@ -7,7 +7,8 @@ allocation-free variant keeps its scratch in a static array inside the
 library.  This test calls it through the C ABI twice in a row (different
 routings, so the second call runs on scratch the first one left behind) and
 checks that every output is bit-identical to moe_permute's.  It also checks
-that a configuration beyond the built-in scratch is rejected before launch.
+that a configuration beyond the built-in scratch is rejected before launch, and
+that the maps-only form (no Xperm, as the gathered-rows GEMM uses) matches too.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
@@ -69,6 +70,14 @@ def _check_against_workspace_call(w, seed):
     a = got["Xperm"][:n_used].view(torch.int16)
     b = ref["Xperm"][:n_used].view(torch.int16)
     assert torch.equal(a, b)
+    # the maps only: Xperm (and X) NULL
+    maps = _outputs(cfg, w.T, w.H, w.E, w.k)
+    M.moe_permute_noalloc(cfg, None, topk, counts, maps["offsets"], maps["tile_offsets"], maps["row_id_map"],
+                          maps["slot_src"], None)
+    torch.cuda.synchronize()
+    for name in ["offsets", "tile_offsets", "row_id_map"]:
+        assert torch.equal(maps[name], ref[name]), name
+    assert torch.equal(maps["slot_src"][:n_used], ref["slot_src"][:n_used])
     return ref["row_id_map"].clone()
 
 
