@@ -172,6 +172,23 @@ def expert_wgrad(c: OraCfg, inp: dict, topk_idx, gates_, expert: int, kept=None)
     return dW13, dW2
 
 
+def expert_wgrad_cols(c: OraCfg, inp: dict, topk_idx, gates_, expert: int, cols, kept=None):
+    """The weight gradients of one expert at a few FFN indices f in `cols`, equal to the
+    corresponding entries of expert_wgrad at a fraction of its cost: dW13 rows f and F+f
+    ([2*len(cols), H]: gate rows, then up rows) and dW2 columns f ([H, len(cols)])."""
+    cols = np.ascontiguousarray(cols, np.int32)
+    nc = len(cols)
+    dW13r = np.empty((2 * nc, c.H), np.float64)
+    dW2c = np.empty((c.H, nc), np.float64)
+    kp = None if kept is None else np.ascontiguousarray(kept, np.int32)
+    _load().ora_expert_wgrad_cols(ctypes.byref(c), _p(_u16(inp["X"])), _p(_u16(inp["W13"])), _p(_u16(inp["W2"])),
+                                  _p(_u16(inp.get("W13_s"))), _p(_u16(inp.get("W2_s"))),
+                                  _p(np.ascontiguousarray(topk_idx, np.int32)),
+                                  _p(np.ascontiguousarray(gates_, np.float64)), _p(_u16(inp["dY"])),
+                                  ctypes.c_int32(expert), ctypes.c_int32(nc), _p(cols), _p(dW13r), _p(dW2c), _p(kp))
+    return dW13r, dW2c
+
+
 def router_dlogits(c: OraCfg, logits, topk_idx, gates_, dgates):
     """dlogits [T,E] (float64): the gates' exact gradient w.r.t. the logits for the given
     selection, applied to dgates [T,k]."""

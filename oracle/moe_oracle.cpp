@@ -723,6 +723,120 @@ void ora_expert_wgrad_kept(const ora_cfg* cp, const uint16_t* X, const uint16_t*
   }
 }
 
+// The weight gradients of one expert restricted to a few FFN indices f = cols[0..ncols):
+// rows f and F+f of dW13 (dW13_rows [2*ncols, H]: the gate rows of cols, then their up
+// rows) and column f of dW2 (dW2_cols [H, ncols]).  Each entry is formed by the same
+// operations, roundings and summation order as in ora_expert_wgrad_kept (the token rows of
+// the expert in token order, the same 128-token FP8 column blocks), so it equals that
+// function's value; this form costs O(rows * ncols * H) instead of O(rows * F * H), which
+// makes experts with thousands of rows of a 7168-wide layer checkable.
+void ora_expert_wgrad_cols(const ora_cfg* cp, const uint16_t* X, const uint16_t* W13, const uint16_t* W2,
+                           const uint16_t* W13s, const uint16_t* W2s, const int32_t* topk_idx, const double* gates,
+                           const uint16_t* dY, int32_t expert, int32_t ncols, const int32_t* cols,
+                           double* dW13_rows, double* dW2_cols, const int32_t* c_kept) {
+  const ora_cfg c = *cp;
+  const int H = c.H, k = c.k, nc = ncols;
+  const int F = expert < 0 ? c.F_shared : c.F;
+  const uint16_t* w13 = expert < 0 ? W13s : W13 + (size_t)expert * 2 * F * H;
+  const uint16_t* w2 = expert < 0 ? W2s : W2 + (size_t)expert * H * F;
+  std::vector<int64_t> toks;
+  std::vector<double> gsel;
+  for (int64_t t = 0; t < c.T; ++t) {
+    if (expert < 0) {
+      toks.push_back(t);
+      gsel.push_back(1.0);
+      continue;
+    }
+    for (int j = 0; j < k; ++j)
+      if (topk_idx[t * k + j] == expert && (!c_kept || c_kept[t * k + j])) {
+        toks.push_back(t);
+        gsel.push_back(gates[t * k + j]);
+      }
+  }
+  std::fill(dW13_rows, dW13_rows + (size_t)2 * nc * H, 0.0);
+  std::fill(dW2_cols, dW2_cols + (size_t)H * nc, 0.0);
+  const int64_t n = (int64_t)toks.size();
+  const int64_t chunk = 512;
+  // per chunk: x and the expert-output gradient of every row (all H), the activation and
+  // dG, dU of the sampled indices only
+  std::vector<double> xs, dyps, as, dGs, dUs;
+  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+    const int64_t m = std::min(chunk, n - c0);
+    xs.assign((size_t)m * H, 0.0);
+    dyps.assign((size_t)m * H, 0.0);
+    as.assign((size_t)m * nc, 0.0);
+    dGs.assign((size_t)m * nc, 0.0);
+    dUs.assign((size_t)m * nc, 0.0);
+    parallel_for(m, nthreads_of(c), [&](int64_t i) {
+      const int64_t t = toks[c0 + i];
+      const double gj = gsel[c0 + i];
+      const bool gated = c.gated && expert >= 0;
+      double* x = &xs[(size_t)i * H];
+      double* dyp = &dyps[(size_t)i * H];
+      for (int h = 0; h < H; ++h) x[h] = bf(X[(size_t)t * H + h]);
+      std::vector<double> xq, dq;
+      const double* xin = x;
+      if (c.fp8) {  // FC1 reads the token row as 1x128 blocks along H
+        xq.resize(H);
+        qdq_blocks(x, xq.data(), H, 128);
+        xin = xq.data();
+      }
+      for (int h = 0; h < H; ++h) dyp[h] = gated ? bf(dY[(size_t)t * H + h]) : maybe_r(c, gj * bf(dY[(size_t)t * H + h]));
+      const double* din = dyp;
+      if (c.fp8) {  // FC2 dgrad reads the output gradient as 1x128 blocks along H
+        dq.resize(H);
+        qdq_blocks(dyp, dq.data(), H, 128);
+        din = dq.data();
+      }
+      for (int q = 0; q < nc; ++q) {
+        const int f = cols[q];
+        double g = 0, u = 0;
+        const uint16_t* wg = w13 + (size_t)f * H;
+        const uint16_t* wu = w13 + (size_t)(F + f) * H;
+        for (int h = 0; h < H; ++h) {
+          g += bf(wg[h]) * xin[h];
+          u += bf(wu[h]) * xin[h];
+        }
+        const double gr = maybe_r(c, g), ur = maybe_r(c, u);
+        as[(size_t)i * nc + q] = gated ? maybe_r(c, gj * (silu(gr) * ur)) : maybe_r(c, 1.0 * (silu(g) * u));
+        double dA = 0;
+        for (int h = 0; h < H; ++h) dA += bf(w2[(size_t)h * F + f]) * din[h];
+        if (gated) dA *= gj;
+        dGs[(size_t)i * nc + q] = maybe_r(c, dA * ur * dsilu(gr));
+        dUs[(size_t)i * nc + q] = maybe_r(c, dA * silu(gr));
+      }
+    });
+    if (c.fp8) {  // wgrad operands: 128x1 blocks along the expert's tokens
+      qdq_columns(dyps.data(), m, H);
+      qdq_columns(as.data(), m, nc);
+      qdq_columns(xs.data(), m, H);
+      qdq_columns(dGs.data(), m, nc);
+      qdq_columns(dUs.data(), m, nc);
+    }
+    parallel_for(H, nthreads_of(c), [&](int64_t h) {
+      double* row = dW2_cols + (size_t)h * nc;
+      for (int64_t i = 0; i < m; ++i) {
+        const double d = dyps[(size_t)i * H + h];
+        for (int q = 0; q < nc; ++q) row[q] += d * as[(size_t)i * nc + q];
+      }
+    });
+    parallel_for(2 * (int64_t)nc, nthreads_of(c), [&](int64_t r) {
+      double* row = dW13_rows + (size_t)r * H;
+      const bool up = r >= nc;
+      const int q = (int)(up ? r - nc : r);
+      for (int64_t i = 0; i < m; ++i) {
+        const double d = up ? dUs[(size_t)i * nc + q] : dGs[(size_t)i * nc + q];
+        const double* x = &xs[(size_t)i * H];
+        for (int h = 0; h < H; ++h) row[h] += d * x[h];
+      }
+    });
+  }
+  if (c.mirror) {
+    for (size_t i = 0; i < (size_t)2 * nc * H; ++i) dW13_rows[i] = rbf(dW13_rows[i]);
+    for (size_t i = 0; i < (size_t)H * nc; ++i) dW2_cols[i] = rbf(dW2_cols[i]);
+  }
+}
+
 // Router logit gradients for given gate gradients (summary page, "Method": the router
 // is differentiated through its gates): per token, the exact gradient of the gates with
 // respect to the logits for the given selection (token_dlogits), applied to dgates.

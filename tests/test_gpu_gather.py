@@ -1,14 +1,15 @@
 """Gathered-rows expert MLP (no permuted copy of the tokens): FC1 reads the token rows
 of X through the dispatch map with TMA four-row gathers, in the forward and in FC1's
 weight gradient.  The GEMMs see exactly the operands of the plain path, so every
-output must be bit-identical to it (the plain path is held to the oracle in
-test_gpu_parity.py)."""
+output must be bit-identical to it; the gathered path is also held to the oracle
+directly, element by element."""
 import numpy as np
 import pytest
 import torch
 
 import moe_synth as S
-from helpers import make_layer, to_dev
+import oracle as O
+from helpers import host_f64, logit_rel_err, make_layer, slice_rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -72,3 +73,38 @@ def test_gathered_rows_without_tokens():
     got = _run(w, inp, gather_rows=True)
     assert int(got.counts.sum().item()) == 0
     assert not got.dW13.any() and not got.dW2.any()
+
+
+@pytest.mark.parametrize("name", ["ragged-softmax", "dsv3-mini"])
+def test_gathered_rows_match_the_oracle(name):
+    """The gathered path against the oracle: routing and maps bit-exact (the oracle's
+    float32 selection on the GPU's own scores), every value within the bf16 bound."""
+    w = GATHER_CASES[name]
+    inp = S.host_inputs(w)
+    layer = _run(w, inp, gather_rows=True)
+    c = O.cfg(w)
+    lg, sc = layer.logits.cpu().numpy(), layer.scores.cpu().numpy()
+    logits, _ = O.router(c, inp["X"], inp["W_r"], inp.get("logit_bias"))
+    assert logit_rel_err(lg, logits) < 1e-5
+    idx = layer.topk_idx.cpu().numpy()
+    assert np.array_equal(idx, O.select(c, lg, sc, inp.get("sel_bias")))
+    g = O.gates(c, logits, idx)
+    d = O.dispatch(c, idx, R=layer.R)
+    n_used = int(d["offsets"][-1])
+    for k in ["counts", "offsets", "tile_offsets", "row_id_map"]:
+        assert np.array_equal(getattr(layer, k).cpu().numpy(), d[k]), k
+    assert np.array_equal(layer.slot_src.cpu().numpy()[:n_used], d["slot_src"][:n_used])
+    tk = O.tokens(c, inp, idx, logits, g)
+    assert slice_rel_err(host_f64(layer.Y), tk["Y"]) < 2e-2
+    assert slice_rel_err(layer.dgates.cpu().numpy(), tk["dgates"]) < 2e-2
+    assert slice_rel_err(host_f64(layer.dX), tk["dX"]) < 2e-2
+    for e in range(w.E):
+        dW13, dW2 = O.expert_wgrad(c, inp, idx, g, e)
+        assert slice_rel_err(host_f64(layer.dW13[e]), dW13, 2) < 2e-2, e
+        assert slice_rel_err(host_f64(layer.dW2[e]), dW2, 2) < 2e-2, e
+    if w.F_shared:
+        dW13s, dW2s = O.expert_wgrad(c, inp, idx, g, -1)
+        assert slice_rel_err(host_f64(layer.dW13_s), dW13s, 2) < 2e-2
+        assert slice_rel_err(host_f64(layer.dW2_s), dW2s, 2) < 2e-2
+    dWr, _ = O.router_wgrad(c, inp["X"], tk["dlogits"])
+    assert slice_rel_err(layer.dW_r.cpu().numpy(), dWr) < 2e-2

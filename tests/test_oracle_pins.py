@@ -730,3 +730,34 @@ def test_gated_form_is_the_same_function(wname):
     for key in ["Y", "dX", "dW13", "dW2"]:
         err = np.abs(am[key] - bm[key]).max() / np.abs(am[key]).max()
         assert 0 < err < 2e-2, (key, err)
+
+
+# ---------------------------------------------------------------- sampled weight gradients
+@pytest.mark.parametrize("mode", ["mirror", "pure", "fp8", "gated", "kept"])
+def test_expert_wgrad_cols_equals_the_full_gradient(mode):
+    """The column-sampled expert weight gradient (used where the full one is out of reach)
+    reproduces the entries of the full expert_wgrad bit for bit: the same roundings, the
+    same 128-token FP8 blocks (the expert holds more than one 512-token chunk here) and the
+    same summation order, for routed experts and the shared one."""
+    w = small("wc", T=700, H=256, E=2, k=2, F=256, F_shared=128, score_fn=1, gate_scale=2.5,
+              fp8=mode == "fp8")
+    inp = inputs(w)
+    if mode == "fp8":
+        inp = O.fp8_inputs(inp)
+    c = O.cfg(w, mirror=mode != "pure", gated=mode == "gated")
+    logits, scores = O.router(c, inp["X"], inp["W_r"])
+    idx = O.select(c, logits, scores)
+    g = O.gates(c, logits, idx)
+    kept = None
+    if mode == "kept":
+        kept = (np.arange(w.T * w.k).reshape(w.T, w.k) % 3 != 0).astype(np.int32)
+    counts = np.bincount(idx.ravel(), minlength=w.E)
+    assert counts.max() > 512  # more than one chunk
+    for e, F in [(int(np.argmax(counts)), w.F), (-1, w.F_shared)]:
+        cols = np.array([0, 5, 77, F - 1], np.int32)
+        full13, full2 = O.expert_wgrad(c, inp, idx, g, e, kept=kept)
+        r13, c2 = O.expert_wgrad_cols(c, inp, idx, g, e, cols, kept=kept)
+        assert np.array_equal(r13[:len(cols)], full13[cols])
+        assert np.array_equal(r13[len(cols):], full13[F + cols])
+        assert np.array_equal(c2, full2[:, cols])
+        assert np.abs(c2).max() > 0
