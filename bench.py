@@ -1,16 +1,22 @@
 """Benchmark: one MoE layer forward+backward step on GB300, tokens/s.
 
-Workload (default): the Mixtral-style layer, T=4096 tokens, H=4096, E=8 experts,
-top-2 softmax router with renormalised gates, SwiGLU FFN=14336, BF16 tokens and
-expert weights, FP32 router; seeded synthetic inputs.  A step is one pass of
-the whole layer: route, permute, grouped SwiGLU MLP, combine, and their
-backwards (dX, grouped dgrad and wgrad, router gradient).
+Workload (default): the DeepSeek-V3-style layer, the largest that fits one GPU:
+T=8192 tokens, H=7168, 256 routed experts with top-8 and one always-on shared
+expert, sigmoid router with a selection-only bias, group-limited routing (8
+groups, top-4 groups), gates renormalised and scaled by 2.5, SwiGLU FFN=2048,
+BF16 tokens and expert weights, FP32 router; seeded synthetic inputs.  The other
+workloads (Mixtral-, Qwen3-style, skewed, FP8) are selectable with --workload.
+A step is one pass of the whole layer: route, permute, grouped SwiGLU MLP,
+combine, and their backwards (dX, grouped dgrad and wgrad, router gradient).
 
-Prints one JSON line.  `value` is tokens/s with inputs resident in HBM; `e2e`
-is the same metric through the C ABI with the step's inputs copied in from
-pinned host memory and its outputs (Y, dX) copied back inside the timed region.
-The grouped GEMM is the dominant kernel; its roofline is reported against the
-measured dense BF16 peak.  --impl reference times the CPU oracle instead.
+Prints one JSON line.  `value` is tokens/s with inputs resident in HBM: T over
+the median time of one replay of the step captured as a CUDA graph (K replays
+after W warm-up replays, CUDA events between replays).  A second pass runs K
+eager steps with CUDA events between the stages (and NVTX ranges around them)
+for the per-stage times, the grouped GEMM's roofline and the HBM stages'
+bandwidths.  `e2e` is the same metric through the C ABI with the step's inputs
+copied in from pinned host memory and its outputs (Y, dX) copied back inside
+the timed region.  --impl reference times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -160,16 +166,29 @@ STAGES = ["router", "permute", "quant_w", "gemm_fwd", "combine", "combine_bwd", 
 
 
 def run_step(layer, X, dY, ev=None):
-    """One forward+backward through the C ABI; ev: list of len(STAGES)+1 events."""
+    """One forward+backward through the C ABI; ev: list of len(STAGES)+1 events (eager
+    runs only: the events then bracket every stage, with an NVTX range around each)."""
+    import torch
     import mixture_experts_layer_topk_gb300 as M
     c, w = layer.cfg, layer.w
-    rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+    nvtx = torch.cuda.nvtx
+
+    def rec(i):
+        if ev is None:
+            return
+        if i > 0:
+            nvtx.range_pop()
+        ev[i].record()
+        if i < len(STAGES):
+            nvtx.range_push(STAGES[i])
+
     rec(0)
     M.moe_router_topk(c, X, w.W_r, w.logit_bias, w.sel_bias, layer.logits, layer.scores, layer.topk_idx,
                       layer.gates, layer.counts, layer.ws)
     rec(1)
-    M.moe_permute(c, X, layer.topk_idx, layer.counts, layer.offsets, layer.tile_offsets, layer.row_id_map,
-                  layer.slot_src, layer.Xperm, layer.ws)
+    # gathered rows: the dispatch writes the maps only and FC1 reads X through them
+    M.moe_permute(c, None if layer.gather_rows else X, layer.topk_idx, layer.counts, layer.offsets,
+                  layer.tile_offsets, layer.row_id_map, layer.slot_src, layer.Xperm, layer.ws)
     rec(2)
     if layer.fp8:
         # the step re-quantizes the weights (as after every optimizer update) inside the timed region
@@ -180,6 +199,10 @@ def run_step(layer, X, dY, ev=None):
                                      layer.W2q, layer.W2sc, layer.GU, layer.A, layer.Yperm,
                                      X if c.F_shared else None, layer.W13q_s, layer.W13sc_s, layer.W2q_s,
                                      layer.W2sc_s, layer.GU_s, layer.A_s, layer.Yshared, layer.fp8_ws, layer.ws)
+    elif layer.gather_rows:
+        M.moe_grouped_swiglu_mlp_gather(c, X, layer.slot_src, layer.offsets, layer.tile_offsets, w.W13, w.W2,
+                                        layer.GU, layer.A, layer.Yperm, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
+                                        layer.Yshared, layer.ws)
     else:
         M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
                                  layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
@@ -191,7 +214,13 @@ def run_step(layer, X, dY, ev=None):
                                 layer.dYperm, layer.dgates)
     rec(6)
     sh = c.F_shared > 0
-    if layer.fp8:
+    if layer.gather_rows:
+        M.moe_grouped_swiglu_mlp_bwd_gather(c, X, layer.slot_src, layer.offsets, layer.tile_offsets, layer.counts,
+                                            w.W13, w.W2, layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm,
+                                            layer.dW13, layer.dW2, dY if sh else None, w.W13_s, w.W2_s, layer.GU_s,
+                                            layer.A_s, layer.dGU_s, layer.dX_shared, layer.dW13_s, layer.dW2_s,
+                                            layer.ws)
+    elif layer.fp8:
         M.moe_grouped_swiglu_mlp_bwd_fp8(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts, layer.W13q,
                                          layer.W13sc, layer.W2q, layer.W2sc, layer.GU, layer.A, layer.dYperm,
                                          layer.dGU, layer.dXperm, layer.dW13, layer.dW2, X if sh else None,
@@ -212,11 +241,11 @@ def run_step(layer, X, dY, ev=None):
     rec(9)
 
 
-def launches_per_step(w):
+def launches_per_step(w, gather=False):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
     n = 3                                  # router: W_r split, tensor-core logits, routing
-    n += 4                                 # chunk histogram, scan, scatter, row copy
+    n += 3 if gather else 4                # chunk histogram, scan, scatter, (row copy)
     n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
     n += 2                                 # combine, combine backward
     n += 4 * (1 + sh)                      # FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad
@@ -231,8 +260,9 @@ def launches_per_step(w):
     return n
 
 
-def hbm_bytes(w):
-    """Algorithmic bytes of the HBM-bound stages (index maps excluded)."""
+def hbm_bytes(w, gather=False):
+    """Algorithmic bytes of the HBM-bound stages (index maps excluded; with gathered rows
+    the dispatch writes the maps only and is not an HBM stage)."""
     T, H, S_ = w.T, w.H, w.T * w.k
     sh = w.F_shared > 0
     d = {
@@ -246,6 +276,8 @@ def hbm_bytes(w):
     if w.fp8:  # bf16 weights read, E4M3 weights written (scales < 0.01%)
         wel = 3 * w.E * w.F * w.H + 3 * w.F_shared * w.H
         d["quant_w"] = wel * 2 + wel
+    if gather:
+        del d["permute"]
     return d
 
 
@@ -296,7 +328,8 @@ def cpu_baseline(w, seed, budget_s=15.0):
     t = one(n)
     return {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"full layer forward+backward (router, dispatch, all {w.E} experts' dgrad and wgrad) of the "
-                      f"first {n} of {w.T} tokens, double accumulation, {t:.1f} s wall"}
+                      f"first {n} of {w.T} tokens, double accumulation, {t:.1f} s wall",
+            "extrapolated_full_layer_s": round(w.T * t / n, 1)}
 
 
 def bench_ours(args, w):
@@ -310,7 +343,7 @@ def bench_ours(args, w):
     dev = torch.device("cuda", local)
     weights, X, dY = device_inputs(w, args.seed, dev)
     cfg = M.config_from(w)
-    layer = M.MoELayer(cfg, weights, device=dev, fp8=w.fp8)
+    layer = M.MoELayer(cfg, weights, device=dev, fp8=w.fp8, gather_rows=args.gather)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -319,30 +352,53 @@ def bench_ours(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
+    # eager warm-up (sets the kernels' attributes), then the step captured as one CUDA graph
+    for _ in range(2):
         run_step(layer, X, dY)
     barrier()
     if layer.device_error() != 0:
         raise RuntimeError("device error during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(device=dev)
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        run_step(layer, X, dY)  # one eager step on the capture stream before capturing
+        with torch.cuda.graph(graph, stream=cs):
+            run_step(layer, X, dY)
+    stream.wait_stream(cs)
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    if layer.device_error() != 0:
+        raise RuntimeError("device error during the warm-up replays")
 
-    # timed region: K steps, events around every stage on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
+    # timed region: K replays, an event between consecutive replays
     sampler = ClockSampler(gpu_id_for_smi(torch, local))
     time.sleep(0.3)
     barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
     for i in range(args.steps):
-        run_step(layer, X, dY, evs[i])
-    t_end.record(stream)
+        graph.replay()
+        evs[i + 1].record(stream)
+    barrier()
+    replay_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if layer.device_error() != 0:
+        raise RuntimeError("device error during the timed replays")
+
+    # stage pass: K eager steps, events around every stage on the launching stream
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        run_step(layer, X, dY, sevs[i])
     barrier()
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    stage_ms = {s: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+    stage_ms = {s: sum(sevs[i][j].elapsed_time(sevs[i][j + 1]) for i in range(args.steps)) / args.steps
                 for j, s in enumerate(STAGES)}
+    eager_ms = sum(sevs[i][0].elapsed_time(sevs[i][-1]) for i in range(args.steps)) / args.steps
     if layer.device_error() != 0:
-        raise RuntimeError("device error during the timed steps")
+        raise RuntimeError("device error during the stage pass")
 
     # end to end through the C ABI with host buffers: every step copies its inputs (X, dY)
     # up from pinned host memory and its results (Y, dX) back.  A copy stream moves the
@@ -358,7 +414,6 @@ def bench_ours(args, w):
     dYd = [torch.empty_like(dY) for _ in range(2)]
     Yd = [layer.Y, torch.empty_like(layer.Y)]
     dXd = [layer.dX, torch.empty_like(layer.dX)]
-    cs = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b are on the device
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b has finished
     ev_out = [torch.cuda.Event() for _ in range(2)]   # results of buffer b are on the host
@@ -400,52 +455,63 @@ def bench_ours(args, w):
     e2e_ms = e0.elapsed_time(e1)
     layer.Y, layer.dX = Yd[0], dXd[0]
 
-    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device=dev)
+    med_ms = statistics.median(replay_ms)
+    med_ms, total_ms, e2e_ms = max_over_ranks([med_ms, total_ms, e2e_ms], device=dev)
     if rank != 0:
         return None
 
-    ms_per_step = total_ms / args.steps
     tokens = w.T * ws_
-    value = tokens / (ms_per_step / 1e3)
+    value = tokens / (med_ms / 1e3)
     pk, pk_kind = peaks()
     gemm_flop = M.gemm_flops(cfg)
     gemm_ms = stage_ms["gemm_fwd"] + stage_ms["gemm_bwd"]
     gemm_tflops = gemm_flop / (gemm_ms / 1e3) / 1e12
+    # the GEMMs are timed inside a step of several milliseconds: the sustained peak
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     peak_kind = f"{pk_kind} bf16 sustained"
     if w.fp8:  # dense FP8 runs at twice the BF16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s)
         peak_t *= 2.0
         peak_kind = f"{pk_kind} bf16 sustained x 2 (FP8:BF16 nominal ratio)"
-    traffic = traffic_record("k_grouped_gemm", w.name)
-    hb = hbm_bytes(w)
+    traffic = traffic_record("k_grouped_gemm", w.name + ("-gather" if args.gather else ""))
+    hb = hbm_bytes(w, gather=args.gather)
     hbm = {}
     for s, b in hb.items():
         gbs = b / (stage_ms[s] / 1e3) / 1e9
         hbm[s] = {"achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 3),
                   "ms": round(stage_ms[s], 4)}
+    wbytes = (w.E * 3 * w.F * w.H + 3 * w.F_shared * w.H) * 2
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if w.fp8 else "bf16", "data": "synthetic (seeded normal inputs)",
+        "warmup": args.warmup, "ms_per_step": round(med_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if w.fp8 else "bf16",
+        "data": "synthetic (seeded normal inputs)",
+        "timing": {"value_from": "median of K CUDA-graph replays of the whole step",
+                   "ms_per_step_mean": round(total_ms / args.steps, 4),
+                   "ms_per_step_min": round(min(replay_ms), 4), "ms_per_step_max": round(max(replay_ms), 4),
+                   "eager_ms_per_step": round(eager_ms, 4)},
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared,
-                   "router": ("softmax" if w.score_fn == 0 else "sigmoid") + (", renorm" if w.renorm else ""),
-                   "l2": "inputs larger than L2 (expert weights %.2f GB re-read every step)" %
-                         (w.E * 3 * w.F * w.H * 2 / 1e9),
+                   "router": ("softmax" if w.score_fn == 0 else "sigmoid") + (", renorm" if w.renorm else "")
+                             + (f", {w.n_group} groups / top-{w.topk_group}" if w.n_group > 1 else "")
+                             + (", selection bias" if w.sel_bias else "")
+                             + (f", x{w.gate_scale:g}" if w.gate_scale != 1.0 else ""),
+                   "dispatch": "gathered rows (no permuted copy)" if args.gather else "permuted copy",
+                   "l2": "inputs larger than L2 (expert weights %.2f GB re-read every step)" % (wbytes / 1e9),
                    "parallelism": "replicas" if ws_ > 1 else "single GPU"},
         "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_peak": round(gemm_tflops / peak_t, 3),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "roofline": {"kernel": "k_grouped_gemm (FC1+SwiGLU, FC2, FC2 dgrad+dSwiGLU, FC2 wgrad, FC1 dgrad, FC1 wgrad)",
                      "bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peak_t, 3), "peak_source": peak_kind,
+                     "frac_of_burst": round(gemm_tflops / (pk["bf16_tflops"] * (2.0 if w.fp8 else 1.0)), 3),
                      "traffic": traffic},
         "hbm_stages": hbm,
         "clocks": clocks,
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": launches_per_step(w, gather=args.gather) * args.steps,
         "e2e": {"value": round(tokens / (e2e_ms / args.steps / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * X.numel() * 2, "d2h_bytes_per_step": 2 * X.numel() * 2},
     }
     if ws_ == 1 and not args.no_cpu_baseline:
-        del layer, weights, X, dY
+        del graph, layer, weights, X, dY
         torch.cuda.empty_cache()
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
     return line
@@ -492,16 +558,20 @@ def bench_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mixtral", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--workload", default="dsv3", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--gather", action="store_true",
+                    help="gathered-rows dispatch: FC1 reads X through the maps, no permuted copy (bf16 only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = S.WORKLOADS[args.workload]
+    if args.gather and w.fp8:
+        ap.error("--gather is built for the bf16 expert GEMMs")
     line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

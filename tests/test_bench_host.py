@@ -49,3 +49,10 @@ def test_stage_accounting_covers_every_workload(name):
     # the permute moves X once and writes it k times; the combine backward reads dY once
     assert hb["permute"] == w.T * w.H * 2 * (1 + w.k)
     assert hb["combine_bwd"] == w.T * w.H * 2 * (1 + 2 * w.k)
+
+
+def test_gathered_rows_accounting():
+    """With gathered rows the dispatch copies nothing: one launch fewer, no permute HBM stage."""
+    w = S.WORKLOADS["dsv3"]
+    assert bench.launches_per_step(w, gather=True) == bench.launches_per_step(w) - 1
+    assert "permute" not in bench.hbm_bytes(w, gather=True)
