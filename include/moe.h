@@ -94,6 +94,22 @@ moe_status moe_workspace_init(const moe_config* cfg, void* ws, void* stream);
  * moe_status value) and clears it.  Not for use inside a graph capture. */
 moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
 
+/* Limit of every pipeline wait inside the tensor-core kernels (grouped GEMMs, router
+ * projection), in nanoseconds; library-wide, read when each kernel is launched (a
+ * captured graph keeps the value of its capture).  Default 4e9 (4 s).  The pages have
+ * no counterpart: this is the library's failure detection.  A wait on another part of
+ * the kernel's pipeline (a TMA copy landing, the MMAs of a tile, the epilogue freeing an
+ * accumulator) that runs out of time sets MOE_ERR_TIMEOUT in the device error word
+ * (moe_read_device_error) and the kernel unwinds: each CTA waits, with a fixed 4 s
+ * bound, for the copies and MMAs it already issued (the two CTAs of a pair settle the
+ * loads each of them issued), frees its tensor memory and exits, so the context stays
+ * usable and the next call runs normally.  A limit of 0 makes every pipeline wait a
+ * single non-blocking test, so that nearly every launch runs out: meant for testing the
+ * unwind path, the outputs of such a launch are undefined.  Not thread-safe against
+ * concurrent launches that expect another value. */
+void moe_set_wait_limit_ns(uint64_t ns);
+uint64_t moe_get_wait_limit_ns(void);
+
 /* Route.  ("Method": the router is a learned linear projection, optionally kept
  * in FP32, followed by softmax or sigmoid scoring and top-k selection.)
  *  X        [T,H] bf16 (device)      tokens

@@ -23,7 +23,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from"] + [
+__all__ = ["MoeConfig", "MoeError", "load", "MoELayer", "config_from", "moe_set_wait_limit_ns",
+           "moe_get_wait_limit_ns"] + [
     "moe_router_topk", "moe_permute", "moe_grouped_swiglu_mlp", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_mlp_bwd", "moe_router_topk_bwd", "moe_permute_bwd",
     "moe_workspace_size", "moe_workspace_init", "moe_read_device_error", "moe_max_rows", "moe_permute_noalloc", "moe_permute_capacity",
@@ -36,7 +37,8 @@ EXPORTED = ["moe_status_string", "moe_max_rows", "moe_workspace_size", "moe_work
             "moe_router_topk_bwd", "moe_permute_bwd", "moe_permute_noalloc", "moe_fp8_workspace_size",
             "moe_quantize_weights_fp8", "moe_grouped_swiglu_mlp_fp8", "moe_grouped_swiglu_mlp_bwd_fp8",
             "moe_router_replay", "moe_permute_capacity", "moe_grouped_swiglu_mlp_gated",
-            "moe_grouped_swiglu_mlp_bwd_gated", "moe_grouped_swiglu_mlp_gather", "moe_grouped_swiglu_mlp_bwd_gather"]
+            "moe_grouped_swiglu_mlp_bwd_gated", "moe_grouped_swiglu_mlp_gather", "moe_grouped_swiglu_mlp_bwd_gather",
+            "moe_set_wait_limit_ns", "moe_get_wait_limit_ns"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -97,6 +99,10 @@ def load(build: bool = True):
                 f.restype = ctypes.c_int
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
+            lib.moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.moe_set_wait_limit_ns.restype = None
+            lib.moe_get_wait_limit_ns.argtypes = []
+            lib.moe_get_wait_limit_ns.restype = ctypes.c_uint64
             _lib = lib
     return _lib
 
@@ -141,6 +147,16 @@ def config_from(w, align: int = 128, group_score: int = 0) -> MoeConfig:
     return MoeConfig(w.T, w.H, w.E, w.k, w.F, getattr(w, "F_shared", 0), getattr(w, "score_fn", 0),
                      getattr(w, "renorm", 1), float(getattr(w, "gate_scale", 1.0)), getattr(w, "n_group", 1),
                      getattr(w, "topk_group", 1), group_score, align, 0)
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    """Limit of every pipeline wait inside the tensor-core kernels (default 4e9 ns); a wait
+    that runs out sets MOE_ERR_TIMEOUT and the kernel unwinds.  0: one test per wait."""
+    load().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_get_wait_limit_ns() -> int:
+    return int(load().moe_get_wait_limit_ns())
 
 
 def moe_max_rows(cfg: MoeConfig) -> int:

@@ -134,9 +134,17 @@ Fp8Layout fp8_layout(const moe_config& c, void* base) {
     if (_e != cudaSuccess) return MOE_ERR_CUDA;     \
   } while (0)
 
+std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};
+
 }  // namespace
 
+uint64_t moe::pipeline_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 extern "C" {
+
+void moe_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+
+uint64_t moe_get_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {

@@ -104,6 +104,7 @@ struct GemmArgs {
   int sfb_r, sfb_c;
   int64_t sfb_ld;
   int* err;
+  uint64_t wait_ns;  // limit of each pipeline wait (0: one non-blocking test)
 };
 
 struct Tile {
@@ -222,10 +223,95 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   return r;
 }
 
+// Weight-gradient epilogue without staging: stores one 32-row x 32-column chunk of bf16
+// outputs held one row per lane (acc: the lane's 32 fp32 accumulator values, from
+// tcgen05.ld 32x32b).  A 4x4 transpose of 16-byte units inside each group of four lanes
+// (two butterfly exchanges, over lane bits 0 and 1) leaves lane 4j+l holding unit l of
+// rows 4j..4j+3, so each of the four store instructions writes 8 rows x 64 contiguous
+// bytes (whole 32-byte sectors) with no shared memory, proxy fence or barrier.
+// row0: this warp's first output row at the chunk's first column; ldd: row pitch.
+__device__ __forceinline__ void store_chunk_direct(uint16_t* row0, int64_t ldd, int lane, const uint32_t* acc) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+  const bool l0 = lane & 1, l1 = lane & 2;
+  // lanes l and l^1 swap the units whose index bit 0 differs from the lane's bit 0
+#pragma unroll
+  for (int s1 = 0; s1 < 2; ++s1)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = 8 * s1 + q, b = 8 * s1 + 4 + q;  // units (s1, 0) and (s1, 1)
+      const uint32_t y = __shfl_xor_sync(0xffffffffu, l0 ? w[a] : w[b], 1);
+      if (l0)
+        w[a] = y;
+      else
+        w[b] = y;
+    }
+  // lanes l and l^2 swap the units whose index bit 1 differs from the lane's bit 1
+#pragma unroll
+  for (int s0 = 0; s0 < 2; ++s0)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = 4 * s0 + q, b = 8 + 4 * s0 + q;  // units (0, s0) and (1, s0)
+      const uint32_t y = __shfl_xor_sync(0xffffffffu, l1 ? w[a] : w[b], 2);
+      if (l1)
+        w[a] = y;
+      else
+        w[b] = y;
+    }
+  const int j = lane >> 2, l = lane & 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<uint4*>(row0 + (int64_t)(4 * j + u) * ldd + 8 * l) =
+        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+}
+
 __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
+}
+
+// Exit path of a producer: every TMA load this CTA issued has landed before the CTA may
+// leave.  `issued` counts the producer's stage loads (issue i went to stage i % ST with
+// phase parity (i / ST) & 1); only the producer's thread calls this.
+//
+// One CTA: wait for the last issue of every stage.  CTA pairs: the loads of both CTAs
+// complete on the leader's barriers, which the leader arms for both halves, and after a
+// timeout the two producers may have stopped after different numbers of issues (one
+// passed a wait the other gave up on).  The peer therefore sends its count to the
+// leader (a store into the leader's shared memory, then a release-arrive on peer_done);
+// the leader arms the issues only the peer made for the peer's half alone (once the
+// stage's previous phase has completed, so the arrival counts in the right phase),
+// counts the missing half of the issues only it made as arrived (mbarrier.complete_tx),
+// and then waits for the last issue of every stage.  Either count exceeds the other by
+// at most ST: an issue needs the MMA to have consumed the stage's previous issue, which
+// needs both halves of it.  The peer stays alive until the closing cluster barrier,
+// which the leader reaches only after this.
+template <int ST, bool PAIR>
+__device__ __forceinline__ void drain_loads(uint64_t* full, int issued, int rank, uint32_t* peer_issued,
+                                            uint64_t* peer_done, uint32_t half_bytes, int* err) {
+  int n = issued;
+  if constexpr (PAIR) {
+    if (rank != 0) {
+      st_shared_cluster(mapa_shared(smem_u32(peer_issued), 0), (uint32_t)issued);
+      mbar_arrive_cluster(mapa_shared(smem_u32(peer_done), 0));
+      return;
+    }
+    int np = issued;
+    if (mbar_wait_cluster(peer_done, 0))
+      np = (int)*peer_issued;
+    else
+      set_device_error(err, MOE_ERR_TIMEOUT, 8);
+    for (int i = issued; i < np; ++i) {  // issued by the peer alone
+      if (i >= ST && !mbar_wait(&full[i % ST], ((i - ST) / ST) & 1)) set_device_error(err, MOE_ERR_TIMEOUT, 9);
+      mbar_arrive_expect_tx(&full[i % ST], half_bytes);
+    }
+    for (int i = np; i < issued; ++i) mbar_complete_tx(&full[i % ST], half_bytes);  // issued by the leader alone
+    n = np > issued ? np : issued;
+  }
+  for (int i = n > ST ? n - ST : 0; i < n; ++i)
+    if (!mbar_wait(&full[i % ST], (i / ST) & 1)) set_device_error(err, MOE_ERR_TIMEOUT, 2);
 }
 
 template <int MODE, int EPI, int BN, int ST, bool FP8, bool PAIR, int NEPI>
@@ -244,7 +330,11 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
   constexpr uint32_t IDESC = FP8 ? idesc_mxf8(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD)
                                  : idesc_bf16(PAIR ? 2 * BM : BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD);
   static_assert(!(PAIR && FP8), "CTA pairs are built for the bf16 path only");
-  constexpr bool TMA_OUT = EPI != EPI_SWIGLU;  // outputs leave through the staging buffer and TMA stores
+  // bf16 weight gradients leave straight from registers (store_chunk_direct); the other
+  // stored outputs through the staging buffer and TMA stores
+  constexpr bool DIRECT = MODE == MODE_WGRAD && EPI == EPI_STORE;
+  constexpr bool TMA_OUT = EPI != EPI_SWIGLU && !DIRECT;
+  constexpr int STAGING = DIRECT ? 0 : NEPI * kStagingBytes;
   static_assert(NEPI == 1 || (NEPI == 2 && MODE == MODE_WGRAD && EPI == EPI_STORE && !FP8),
                 "two epilogue warpgroups are built for the bf16 weight gradients");
 
@@ -254,13 +344,15 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
   // per epilogue warpgroup two 8 KB halves, each one [128 rows x 32 bf16] box in the
   // 64-byte swizzle layout
   uint8_t* staging = smem + ST * STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + NEPI * kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING);
   uint64_t* empty = full + ST;
   uint64_t* sf_full = empty + ST;  // FP8: this stage's scale factors are in tensor memory
   uint64_t* acc_full = sf_full + ST;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* peer_done = done_bar + 1;  // CTA pairs: the peer's producer has stopped (leader's copy)
+  // [0] tensor-memory base, [1]/[2] epilogue flags of warpgroups 0/1, [3] the peer's issue count
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(peer_done + 1);
   int* s_seg = reinterpret_cast<int*>(tmem_holder + 4);
   int* s_tile = s_seg + 260;
   int* s_cnt = s_tile + 260;
@@ -301,6 +393,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       mbar_init(&acc_empty[b], (PAIR ? 8 : 4) * NEPI);  // pairs: both CTAs' epilogue warps release
     }
     mbar_init(done_bar, 1);
+    mbar_init(peer_done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
@@ -353,8 +446,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) idx[i] = src_row(base + i);
     };
-    int stage = 0;
-    uint32_t phase = 0, used = 0, last_par = 0;
+    int stage = 0, issued = 0;
+    uint32_t phase = 0;
     bool ok = true;
     int t = t_first;
     Tile tl;
@@ -369,7 +462,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     next_work();
     while (t < total && ok) {
       for (int kb = 0; kb < tl.kb; ++kb) {
-        const int w_ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(&empty[stage], phase ^ 1) : 0, 0);
+        const int w_ok =
+            __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : 0, 0);
         if (!w_ok) {
           if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
           ok = false;
@@ -398,10 +492,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           tma_gather4_pair(sb + j * 8192 + q * 512, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, idx[0], idx[1],
                            idx[2], idx[3]);
         }
-        if (lane == 0) {
-          used |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-        }
+        ++issued;
         if (++stage == ST) {
           stage = 0;
           phase ^= 1;
@@ -412,20 +503,17 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       t += t_step;
       next_work();
     }
-    if (lane == 0 && rank == 0)
-      for (int s2 = 0; s2 < ST; ++s2)
-        if (used >> s2 & 1)
-          if (!mbar_wait(&full[s2], last_par >> s2 & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
+    if (lane == 0) drain_loads<ST, PAIR>(full, issued, rank, tmem_holder + 3, peer_done, STAGE, g.err);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, used = 0, last_par = 0;
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
       bool ok = true;
       for (int t = t_first; t < total && ok; t += t_step) {
         const Tile tl = decode(t);
         for (int kb = 0; kb < tl.kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, g.wait_ns)) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
             ok = false;
             break;
@@ -481,21 +569,15 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
             }
           }
           }
-          used |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          ++issued;
           if (++stage == ST) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      // nothing may still be landing in shared memory when the CTA exits (for pairs the
-      // leader's barriers count both CTAs' copies, and the closing cluster barrier
-      // keeps the peer alive until the leader has seen them land)
-      if (!PAIR || rank == 0)
-        for (int s = 0; s < ST; ++s)
-          if (used >> s & 1)
-            if (!mbar_wait(&full[s], last_par >> s & 1)) set_device_error(g.err, MOE_ERR_TIMEOUT, 2);
+      // nothing may still be landing in shared memory when the CTA exits
+      drain_loads<ST, PAIR>(full, issued, rank, tmem_holder + 3, peer_done, STAGE, g.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the leader CTA of a pair)
@@ -506,14 +588,14 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       for (int t = t_first; t < total && ok; t += t_step) {
         const Tile tl = decode(t);
         if (tl.kb == 0) continue;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, g.wait_ns)) {
           set_device_error(g.err, MOE_ERR_TIMEOUT, 3);
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
         for (int kb = 0; kb < tl.kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase) || (FP8 && !mbar_wait(&sf_full[stage], phase))) {
+          if (!mbar_wait(&full[stage], phase, g.wait_ns) || (FP8 && !mbar_wait(&sf_full[stage], phase, g.wait_ns))) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 4);
             ok = false;
             break;
@@ -625,6 +707,55 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     };
     for (int t = t_first; t < total; t += t_step) {
       const Tile tl = decode(t);
+      if constexpr (DIRECT) {
+        // each warp: its 32 rows of the tile; group grp: the chunks grp, grp + NEPI, ...
+        uint16_t* const dwarp = g.D + (int64_t)tl.e * g.d_estride + (int64_t)(tl.m0 + q * 32) * g.ldd + tl.n0;
+        if (tl.kb == 0) {
+          // an expert without rows: its weight gradient is zero, written as whole rows
+          // (this group's BN/NEPI columns of a row by LPR lanes, 16 bytes each)
+          if (tl.valid) {
+            constexpr int LPR = BN * 2 / NEPI / 16, RPI = 32 / LPR;
+            uint16_t* const z0 = dwarp + grp * (BN / NEPI) + 8 * (lane % LPR);
+#pragma unroll 4
+            for (int r0 = 0; r0 < 32; r0 += RPI)
+              *reinterpret_cast<uint4*>(z0 + (int64_t)(r0 + lane / LPR) * g.ldd) = make_uint4(0, 0, 0, 0);
+          }
+          continue;
+        }
+        const uint32_t w_ok = lane == 0 ? (mbar_wait(&acc_full[acc], acc_phase, g.wait_ns) ? 1u : 0u) : 0u;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 6);
+          break;
+        }
+        mbar_wait(&acc_full[acc], acc_phase);  // already complete: acquires the accumulator for this thread
+        tc_fence_after();
+        if (tl.valid) {
+          // two register buffers: the next chunk's tensor-memory load is in flight while
+          // the current one is converted and stored
+          constexpr int NC = BN / 32 / NEPI;
+          const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + 32 * grp;
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tb, ra);
+#pragma unroll
+          for (int i = 0; i < NC; i += 2) {
+            tmem_ld_wait();
+            if (i + 1 < NC) tmem_ld32(tb + 32 * NEPI * (i + 1), rb);
+            store_chunk_direct(dwarp + 32 * (grp + NEPI * i), g.ldd, lane, ra);
+            if (i + 1 < NC) {
+              tmem_ld_wait();
+              if (i + 2 < NC) tmem_ld32(tb + 32 * NEPI * (i + 2), ra);
+              store_chunk_direct(dwarp + 32 * (grp + NEPI * (i + 1)), g.ldd, lane, rb);
+            }
+          }
+        }
+        // every tensor-memory read of this thread has completed (the last wait above)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release(acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        continue;
+      }
       const int64_t row = tl.m0 + r;
       if constexpr (EPI == EPI_DSWIGLU) {
         // pull this row's saved pre-activations into L2 while the accumulator fills
@@ -660,7 +791,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       }
       // one thread waits (bounded) and shares the outcome, so that all four warps
       // take the same path through the named barriers below
-      if (leader) tmem_holder[1 + grp] = mbar_wait(&acc_full[acc], acc_phase) ? 1u : 0u;
+      if (leader) tmem_holder[1 + grp] = mbar_wait(&acc_full[acc], acc_phase, g.wait_ns) ? 1u : 0u;
       named_bar_sync(ebar, 128);
       const bool acc_ready = tmem_holder[1 + grp] != 0u;
       named_bar_sync(ebar, 128);  // everyone has read the flag before it is reused
@@ -806,7 +937,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     for (int t = t_first; t < total && ok; t += t_step) {
       const Tile tl = decode(t);
       for (int kb = 0; kb < tl.kb; ++kb) {
-        const bool w_ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1) : false, 0);
+        const bool w_ok =
+            __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : false, 0);
         if (!w_ok) {
           if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 7);
           ok = false;
@@ -867,10 +999,12 @@ template <int MODE, int EPI, int BN, bool FP8, bool PAIR = false, int NEPI = 1>
 struct Kern {
   static constexpr int BNL = PAIR ? BN / 2 : BN;
   static constexpr int STAGE = (BM + BNL) * 128;
+  // bf16 weight gradients store from registers and need no staging buffer
+  static constexpr bool DIRECT = MODE == MODE_WGRAD && EPI == EPI_STORE;
+  static constexpr int STAGING = DIRECT ? 0 : NEPI * kStagingBytes;
   // a second epilogue warpgroup's staging buffer takes the room of one operand stage
-  static constexpr int ST = NEPI == 2 ? 5 : (STAGE <= 32768 ? 6 : 4);
-  static constexpr size_t smem =
-      1024 + (size_t)ST * STAGE + NEPI * kStagingBytes + (3 * ST + 5) * 8 + 16 + 4 * 260 * 4;
+  static constexpr int ST = STAGE > 32768 ? 4 : (NEPI == 2 && !DIRECT ? 5 : 6);
+  static constexpr size_t smem = 1024 + (size_t)ST * STAGE + STAGING + (3 * ST + 6) * 8 + 16 + 4 * 260 * 4;
 };
 
 // ---------------------------------------------------------------- host side
@@ -947,6 +1081,8 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
   auto kern = k_grouped_gemm<MODE, EPI, BN, K::ST, FP8, PAIR, NEPI>;
   if (cudaError_t e = raise_smem_limit(attr, kern, K::smem); e != cudaSuccess) return e;
   if (max_tiles <= 0) return cudaSuccess;
+  GemmArgs ga = g;
+  ga.wait_ns = pipeline_wait_ns();
   if constexpr (PAIR) {
     // max_tiles counts 256-row pair tiles here; two CTAs (one cluster) per pair tile
     const int pairs = max_tiles < nsm / 2 ? max_tiles : nsm / 2;
@@ -962,10 +1098,10 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, b, d, g);
+    return cudaLaunchKernelEx(&cfg, kern, a, b, d, ga);
   } else {
     const int grid = max_tiles < nsm ? max_tiles : nsm;
-    kern<<<grid, threads_of<FP8, NEPI>(), K::smem, st>>>(a, b, d, g);
+    kern<<<grid, threads_of<FP8, NEPI>(), K::smem, st>>>(a, b, d, ga);
     return cudaGetLastError();
   }
 }

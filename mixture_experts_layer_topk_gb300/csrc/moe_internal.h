@@ -8,6 +8,10 @@
 
 namespace moe {
 
+// Limit of each pipeline wait inside the tensor-core kernels, in nanoseconds (the
+// library-wide setting of moe_set_wait_limit_ns; read at every launch).
+uint64_t pipeline_wait_ns();
+
 // Sizes of one grouped GEMM launch.
 struct GemmShape {
   int E, H, F;                  // F: expert FFN size (Fs for the shared expert)

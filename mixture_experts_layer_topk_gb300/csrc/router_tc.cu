@@ -52,6 +52,7 @@ struct RouterTcArgs {
   float* P0;    // split 0 (or the whole product): [T,E]
   float* Pn;    // splits 1..: [splits-1][T,E]
   int* err;
+  uint64_t wait_ns;  // limit of each pipeline wait (0: one non-blocking test)
 };
 
 template <int BN>
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       int stage = 0;
       uint32_t phase = 0, used = 0, last_par = 0;
       for (int i = 0; i < nk; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1)) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, a.wait_ns)) {
           set_device_error(a.err, MOE_ERR_TIMEOUT, 11);
           break;
         }
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       uint32_t phase = 0;
       for (int i = 0; i < nk; ++i) {
         const int b = i & 1;
-        if (!mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1) || !mbar_wait(&full[stage], phase)) {
+        if (!mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1, a.wait_ns) || !mbar_wait(&full[stage], phase, a.wait_ns)) {
           set_device_error(a.err, MOE_ERR_TIMEOUT, 13);
           break;
         }
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     bool ok = true;
     for (int i = 0; i < nk; ++i) {
       const int b = i & 1;
-      if (!mbar_wait(&acc_full[b], (i >> 1) & 1)) {
+      if (!mbar_wait(&acc_full[b], (i >> 1) & 1, a.wait_ns)) {
         set_device_error(a.err, MOE_ERR_TIMEOUT, 15);
         ok = false;
         break;
@@ -248,6 +249,7 @@ cudaError_t launch_bn(int T, int H, int E, int Ep, const uint16_t* X, const uint
   a.nkb = (H + kRtBK - 1) / kRtBK;
   a.kb_per = (a.nkb + splits - 1) / splits;
   a.P0 = P0; a.Pn = Pn; a.err = err;
+  a.wait_ns = pipeline_wait_ns();
   dim3 grid((T + kRtBM - 1) / kRtBM, (E + BN - 1) / BN, splits);
   k_router_logits_tc<BN><<<grid, kRtThreads, G::SMEM, st>>>(mx, mw, a);
   return cudaGetLastError();
