@@ -203,18 +203,33 @@ def run_step(layer, X, dY, ev=None):
         M.moe_grouped_swiglu_mlp_gather(c, X, layer.slot_src, layer.offsets, layer.tile_offsets, w.W13, w.W2,
                                         layer.GU, layer.A, layer.Yperm, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
                                         layer.Yshared, layer.ws)
+    elif layer.memory_efficient:
+        # gates applied before FC2 (gated rows), so the combine is a plain sum
+        M.moe_grouped_swiglu_mlp_gated(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.slot_src,
+                                       layer.gates, w.W13, w.W2, layer.GU, layer.A, layer.Yperm,
+                                       X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
+                                       layer.Yshared, layer.ws)
     else:
         M.moe_grouped_swiglu_mlp(c, layer.Xperm, layer.offsets, layer.tile_offsets, w.W13, w.W2, layer.GU, layer.A,
                                  layer.Yperm, X if c.F_shared else None, w.W13_s, w.W2_s, layer.GU_s, layer.A_s,
                                  layer.Yshared, layer.ws)
     rec(4)
-    M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, layer.gates, layer.Yshared, layer.Y)
+    me = layer.memory_efficient
+    M.moe_unpermute_combine(c, layer.Yperm, layer.row_id_map, None if me else layer.gates, layer.Yshared, layer.Y)
     rec(5)
-    M.moe_unpermute_combine_bwd(c, dY, layer.Yperm, layer.row_id_map, layer.gates, layer.offsets, layer.counts,
-                                layer.dYperm, layer.dgates)
+    # memory-efficient form: dYperm is a copy of dY's rows, the gate gradient comes from FC2's dgrad
+    M.moe_unpermute_combine_bwd(c, dY, None if me else layer.Yperm, layer.row_id_map, None if me else layer.gates,
+                                layer.offsets, layer.counts, layer.dYperm, None if me else layer.dgates)
     rec(6)
     sh = c.F_shared > 0
-    if layer.gather_rows:
+    if me:
+        M.moe_grouped_swiglu_mlp_bwd_gated(c, layer.Xperm, layer.offsets, layer.tile_offsets, layer.counts,
+                                           layer.slot_src, layer.row_id_map, layer.gates, w.W13, w.W2, layer.GU,
+                                           layer.dYperm, layer.dGU, layer.dXperm, layer.A, layer.dW13, layer.dW2,
+                                           layer.dgates, X if sh else None, dY if sh else None, w.W13_s, w.W2_s,
+                                           layer.GU_s, layer.A_s, layer.dGU_s, layer.dX_shared, layer.dW13_s,
+                                           layer.dW2_s, layer.ws)
+    elif layer.gather_rows:
         M.moe_grouped_swiglu_mlp_bwd_gather(c, X, layer.slot_src, layer.offsets, layer.tile_offsets, layer.counts,
                                             w.W13, w.W2, layer.GU, layer.A, layer.dYperm, layer.dGU, layer.dXperm,
                                             layer.dW13, layer.dW2, dY if sh else None, w.W13_s, w.W2_s, layer.GU_s,
@@ -241,11 +256,12 @@ def run_step(layer, X, dY, ev=None):
     rec(9)
 
 
-def launches_per_step(w, gather=False):
+def launches_per_step(w, gather=False, memory_efficient=False):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
     n = 3                                  # router: W_r split, tensor-core logits, routing
     n += 3 if gather else 4                # chunk histogram, scan, scatter, (row copy)
+    n += 1 if memory_efficient else 0      # fixed-order sum of the gate-gradient partials
     n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
     n += 2                                 # combine, combine backward
     n += 4 * (1 + sh)                      # FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad
@@ -260,9 +276,10 @@ def launches_per_step(w, gather=False):
     return n
 
 
-def hbm_bytes(w, gather=False):
+def hbm_bytes(w, gather=False, memory_efficient=False):
     """Algorithmic bytes of the HBM-bound stages (index maps excluded; with gathered rows
-    the dispatch writes the maps only and is not an HBM stage)."""
+    the dispatch writes the maps only and is not an HBM stage; in the memory-efficient
+    form the combine backward copies dY's rows and reads no Yperm)."""
     T, H, S_ = w.T, w.H, w.T * w.k
     sh = w.F_shared > 0
     d = {
@@ -278,6 +295,8 @@ def hbm_bytes(w, gather=False):
         d["quant_w"] = wel * 2 + wel
     if gather:
         del d["permute"]
+    if memory_efficient:
+        d["combine_bwd"] = T * H * 2 + S_ * H * 2
     return d
 
 
@@ -343,7 +362,8 @@ def bench_ours(args, w):
     dev = torch.device("cuda", local)
     weights, X, dY = device_inputs(w, args.seed, dev)
     cfg = M.config_from(w)
-    layer = M.MoELayer(cfg, weights, device=dev, fp8=w.fp8, gather_rows=args.gather)
+    layer = M.MoELayer(cfg, weights, device=dev, fp8=w.fp8, gather_rows=args.gather,
+                       memory_efficient=args.memory_efficient)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -472,8 +492,9 @@ def bench_ours(args, w):
     if w.fp8:  # dense FP8 runs at twice the BF16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s)
         peak_t *= 2.0
         peak_kind = f"{pk_kind} bf16 sustained x 2 (FP8:BF16 nominal ratio)"
-    traffic = traffic_record("k_grouped_gemm", w.name + ("-gather" if args.gather else ""))
-    hb = hbm_bytes(w, gather=args.gather)
+    variant = "-gather" if args.gather else ("-memeff" if args.memory_efficient else "")
+    traffic = traffic_record("k_grouped_gemm", w.name + variant)
+    hb = hbm_bytes(w, gather=args.gather, memory_efficient=args.memory_efficient)
     hbm = {}
     for s, b in hb.items():
         gbs = b / (stage_ms[s] / 1e3) / 1e9
@@ -495,6 +516,8 @@ def bench_ours(args, w):
                              + (", selection bias" if w.sel_bias else "")
                              + (f", x{w.gate_scale:g}" if w.gate_scale != 1.0 else ""),
                    "dispatch": "gathered rows (no permuted copy)" if args.gather else "permuted copy",
+                   "combine": ("gates applied before FC2, unit-weight sum (memory-efficient form)"
+                               if args.memory_efficient else "gate-weighted sum"),
                    "l2": "inputs larger than L2 (expert weights %.2f GB re-read every step)" % (wbytes / 1e9),
                    "parallelism": "replicas" if ws_ > 1 else "single GPU"},
         "gemm_tflops": round(gemm_tflops, 1), "gemm_frac_of_peak": round(gemm_tflops / peak_t, 3),
@@ -506,7 +529,7 @@ def bench_ours(args, w):
                      "traffic": traffic},
         "hbm_stages": hbm,
         "clocks": clocks,
-        "gpu_launches": launches_per_step(w, gather=args.gather) * args.steps,
+        "gpu_launches": launches_per_step(w, gather=args.gather, memory_efficient=args.memory_efficient) * args.steps,
         "e2e": {"value": round(tokens / (e2e_ms / args.steps / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * X.numel() * 2, "d2h_bytes_per_step": 2 * X.numel() * 2},
     }
@@ -564,14 +587,18 @@ def main():
     ap.add_argument("--workload", default="dsv3", choices=sorted(S.WORKLOADS))
     ap.add_argument("--gather", action="store_true",
                     help="gathered-rows dispatch: FC1 reads X through the maps, no permuted copy (bf16 only)")
+    ap.add_argument("--memory-efficient", action="store_true",
+                    help="gates applied before FC2 and activations recomputed in the backward (bf16 only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = S.WORKLOADS[args.workload]
-    if args.gather and w.fp8:
-        ap.error("--gather is built for the bf16 expert GEMMs")
+    if (args.gather or args.memory_efficient) and w.fp8:
+        ap.error("--gather and --memory-efficient are built for the bf16 expert GEMMs")
+    if args.gather and args.memory_efficient:
+        ap.error("--gather and --memory-efficient are separate forms")
     line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

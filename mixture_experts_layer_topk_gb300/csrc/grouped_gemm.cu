@@ -112,6 +112,25 @@ struct Tile {
   bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
 };
 
+// Weight-gradient tile t -> (expert, tile within the expert), `per` tiles per expert.
+// Routed launches interleave the tiles of kWgradWindow consecutive experts: the
+// concurrent CTAs then share a few experts' operands in L2 (a few tens of MB), and the
+// zero tiles of an expert without rows (stores only) run beside other experts' MMAs
+// instead of in a store-only phase of their own.
+constexpr int kWgradWindow = 4;
+__device__ __forceinline__ void wgrad_expert_of(int t, int per, int E, bool routed, int& e, int& local) {
+  if (!routed) {
+    e = t / per;
+    local = t % per;
+    return;
+  }
+  const int e0 = t / (kWgradWindow * per) * kWgradWindow;
+  const int gsz = E - e0 < kWgradWindow ? E - e0 : kWgradWindow;
+  const int u = t - e0 * per;
+  e = e0 + u % gsz;
+  local = u / gsz;
+}
+
 template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                             const int* s_cnt) {
@@ -146,7 +165,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
-    const int e = t / per, local = t % per;
+    int e, local;
+    wgrad_expert_of(t, per, g.E, g.dense_rows <= 0, e, local);
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
@@ -206,7 +226,8 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   } else {
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
-    const int e = t / per, local = t % per;
+    int e, local;
+    wgrad_expert_of(t, per, g.E, g.dense_rows <= 0, e, local);
     const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
@@ -698,11 +719,11 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     auto release = [&](int b) {
       if constexpr (PAIR) {
         if (rank == 0)
-          mbar_arrive(&acc_empty[b]);
+          mbar_arrive_relaxed(&acc_empty[b]);
         else
-          mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
+          mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&acc_empty[b]), 0));
       } else {
-        mbar_arrive(&acc_empty[b]);
+        mbar_arrive_relaxed(&acc_empty[b]);
       }
     };
     for (int t = t_first; t < total; t += t_step) {
@@ -729,6 +750,12 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         }
         mbar_wait(&acc_full[acc], acc_phase);  // already complete: acquires the accumulator for this thread
         tc_fence_after();
+        // the accumulator goes back as soon as this warp's last tensor-memory load has completed
+        auto release_now = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) release(acc);
+        };
         if (tl.valid) {
           // two register buffers: the next chunk's tensor-memory load is in flight while
           // the current one is converted and stored
@@ -739,19 +766,23 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
 #pragma unroll
           for (int i = 0; i < NC; i += 2) {
             tmem_ld_wait();
-            if (i + 1 < NC) tmem_ld32(tb + 32 * NEPI * (i + 1), rb);
+            if (i + 1 < NC)
+              tmem_ld32(tb + 32 * NEPI * (i + 1), rb);
+            else
+              release_now();
             store_chunk_direct(dwarp + 32 * (grp + NEPI * i), g.ldd, lane, ra);
             if (i + 1 < NC) {
               tmem_ld_wait();
-              if (i + 2 < NC) tmem_ld32(tb + 32 * NEPI * (i + 2), ra);
+              if (i + 2 < NC)
+                tmem_ld32(tb + 32 * NEPI * (i + 2), ra);
+              else
+                release_now();
               store_chunk_direct(dwarp + 32 * (grp + NEPI * (i + 1)), g.ldd, lane, rb);
             }
           }
+        } else {
+          release_now();  // the missing half of a pair tile: nothing to read
         }
-        // every tensor-memory read of this thread has completed (the last wait above)
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) release(acc);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         continue;

@@ -221,6 +221,163 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
   }
 }
 
+// Dispatch of a small layer in one launch (dropless, T*k <= kSmallAssign, E <= 32,
+// T*k*E <= kSmallWork): the
+// four launches above are a chain of short dependent steps, which dominates when the
+// layer moves only ~100 MB.  Here every token CTA takes kSmallTok tokens and
+//   1. counts, from all of topk_idx, each expert's assignments before its first token and
+//      in total (warp ballots, one per expert per 32 assignments; lane e keeps expert e),
+//   2. derives the aligned segment starts and the M-tile schedule from the totals,
+//   3. ranks its own assignments in token order (match_any within a warp, running
+//      per-expert cursors across the warp's passes), writes row_id_map and slot_src,
+//   4. copies its tokens' rows into Xperm (the k slots of each token, 16-byte vectors).
+// CTAs past the token range mark and zero the padding rows, kPadSplit CTAs per expert.
+// CTA 0 writes offsets, tile_offsets and kept, and checks the totals against counts.
+// The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
+constexpr int kSmallTok = 32;
+constexpr int kSmallAssign = 16384;
+constexpr int kSmallMaxE = 32;
+constexpr int64_t kSmallWork = 131072;  // T*k*E: at most 64 ballots per 32 assignments of a warp's share
+
+__global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restrict__ topk_idx,
+                                                        const int32_t* __restrict__ counts,
+                                                        const uint16_t* __restrict__ X, int T, int H, int E, int k,
+                                                        int align, int tok_blocks, int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ tile_offsets, int32_t* __restrict__ kept,
+                                                        int32_t* __restrict__ row_id_map,
+                                                        int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm,
+                                                        int* err) {
+  __shared__ int s_cnt[2][8][kSmallMaxE];   // per warp: [0] before this CTA's tokens, [1] in total
+  __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
+  __shared__ int s_tot[kSmallMaxE];
+  __shared__ int s_slot[kSmallTok * 32];   // slots of this CTA's assignments (k <= 32)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = (int64_t)T * k;
+  const bool tok_cta = (int)blockIdx.x < tok_blocks;
+  const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
+  const int64_t a0 = (int64_t)t0 * k;  // this CTA's first assignment
+  int before = 0, total = 0;
+  for (int64_t i0 = (int64_t)warp * 32; i0 < S; i0 += 256) {
+    const int64_t i = i0 + lane;
+    const int e = i < S ? topk_idx[i] : -1;
+    const int64_t nb = a0 - i0;  // lanes of this pass that come before a0
+    const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
+    for (int x = 0; x < E; ++x) {
+      const unsigned m = __ballot_sync(0xffffffffu, e == x);
+      if (lane == x) {
+        total += __popc(m);
+        before += __popc(m & bmask);
+      }
+    }
+  }
+  s_cnt[0][warp][lane] = before;
+  s_cnt[1][warp][lane] = total;
+  __syncthreads();
+  if (warp == 0) {
+    int bsum = 0, tsum = 0;
+    for (int w = 0; w < 8; ++w) {
+      bsum += s_cnt[0][w][lane];
+      tsum += s_cnt[1][w][lane];
+    }
+    if (lane >= E) bsum = tsum = 0;
+    // exclusive scans over the experts (lanes) of the aligned rows and the M tiles
+    const int rows = (tsum + align - 1) / align * align, tiles = (tsum + 127) / 128;
+    int ir = rows, it = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ir, o), b = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) {
+        ir += a;
+        it += b;
+      }
+    }
+    if (lane < E) {
+      s_off[lane + 1] = ir;
+      s_tot[lane] = tsum;
+      s_cnt[0][0][lane] = ir - rows + bsum;  // this CTA's first slot for expert `lane`
+    }
+    if (lane == 0) s_off[0] = 0;
+    if (blockIdx.x == 0) {
+      if (lane < E) {
+        offsets[lane + 1] = ir;
+        tile_offsets[lane + 1] = it;
+        kept[lane] = tsum;
+        if (tsum != counts[lane]) set_device_error(err, MOE_ERR_DEVICE, 1000 + lane);
+      }
+      if (lane == 0) offsets[0] = tile_offsets[0] = 0;
+    }
+  }
+  __syncthreads();
+  if (!tok_cta) {  // padding rows of one expert's segment: slot_src -1, Xperm rows zero
+    const int p = blockIdx.x - tok_blocks;
+    const int e = p / kPadSplit, part = p % kPadSplit;
+    const int r0e = s_off[e] + s_tot[e], r1e = s_off[e + 1];
+    const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
+    const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
+    for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
+    if (Xperm) {
+      const int64_t nvec = H / 8;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
+        reinterpret_cast<uint4*>(Xperm)[i] = z;
+    }
+    return;
+  }
+  const int nt = min(kSmallTok, T - t0);
+  const int n = nt * k;  // this CTA's assignments, a0 .. a0 + n - 1
+  if (warp == 0) {
+    int cursor = lane < E ? s_cnt[0][0][lane] : 0;  // lane e: next slot of expert e
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b = 0; b < n; b += 32) {
+      const int i = b + lane;
+      int e = i < n ? topk_idx[a0 + i] : -1 - lane;
+      const bool ok = i < n && (unsigned)e < (unsigned)E;
+      if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int base = __shfl_sync(0xffffffffu, cursor, ok ? e : 0);
+      const int slot = ok ? base + __popc(peers & lt) : -1;
+      if (i < n) {
+        row_id_map[a0 + i] = slot;
+        s_slot[i] = slot;
+        if (ok) slot_src[slot] = (int)(a0 + i);
+      }
+      // each expert's cursor advances by its assignments in this pass
+      for (int x = 0; x < E; ++x) {
+        const unsigned m = __ballot_sync(0xffffffffu, ok && e == x);
+        if (lane == x) cursor += __popc(m);
+      }
+    }
+  }
+  if (!Xperm) return;
+  __syncthreads();
+  // rows: warp w copies tokens w, w + 8, ... of this CTA, U vectors per lane in flight
+  constexpr int U = kGatherUnroll;
+  const int nvec = H / 8;
+  for (int tt = warp; tt < nt; tt += 8) {
+    const int t = t0 + tt;
+    const int my_slot = lane < k ? s_slot[tt * k + lane] : -1;
+    const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)t * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint4 xv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        xv[u] = v < nvec ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+        if (slot < 0) continue;
+        uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + 32 * u + lane;
+          if (v < nvec) out[v] = xv[u];
+        }
+      }
+    }
+  }
+}
+
 // Order-preserving key of a priority: a larger float gives a larger key; -0 and +0
 // give the same key.
 __device__ __forceinline__ uint32_t priority_key(float f) {
@@ -615,6 +772,16 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   if (!priority) drop_order = drop_start = nullptr;
   const int nch = (c.T + kChunk - 1) / kChunk;
   cudaError_t e;
+  // (every CTA counts all assignments with E ballots per 32 of them: bounded by kSmallWork)
+  if (cap == INT_MAX && c.T > 0 && (int64_t)c.T * c.k <= kSmallAssign && c.E <= kSmallMaxE &&
+      (int64_t)c.T * c.k * c.E <= kSmallWork) {
+    // a small dropless layer: the whole dispatch in one launch
+    const int tb = (c.T + kSmallTok - 1) / kSmallTok;
+    k_dispatch_small<<<tb + c.E * kPadSplit, 256, 0, st>>>(topk_idx, counts, X, c.T, c.H, c.E, c.k, c.align, tb,
+                                                           offsets, tile_offsets, kept, row_id_map, slot_src, Xperm,
+                                                           err);
+    return cudaGetLastError();
+  }
   if (nch > 0) {
     k_chunk_hist<<<nch, 256, 0, st>>>(topk_idx, c.T, c.E, c.k, chunk_counts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

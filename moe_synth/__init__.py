@@ -129,6 +129,12 @@ WORKLOADS = {
     # profiling stand-in with the Qwen3-style layer's router (X of 134 MB, 128 experts,
     # top-8) and a narrow FFN, so that the whole layer holds a few GB
     "qwen3-small": Workload("qwen3-small", T=16384, H=4096, E=128, k=8, F=128),
+    # profiling stand-in with the DeepSeek-V3-style layer's routing (the router weight's
+    # spread scaled so the logits keep their spread at the narrower H) and therefore its
+    # per-expert row counts, with a narrower H and FFN: 1.6 GB of expert weights
+    "dsv3-mid": Workload("dsv3-mid", T=8192, H=2048, E=256, k=8, F=512, F_shared=512, score_fn=1,
+                         renorm=1, gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True,
+                         wr_std=0.02 * math.sqrt(7168 / 2048)),
     # profiling stand-in with DeepSeek-V3-style routing and small expert segments
     # (about 64 rows per expert): 2.8 GB of expert weights, small enough for a full capture
     "dsv3-small": Workload("dsv3-small", T=2048, H=7168, E=256, k=8, F=256, F_shared=256, score_fn=1,
