@@ -112,25 +112,6 @@ struct Tile {
   bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
 };
 
-// Weight-gradient tile t -> (expert, tile within the expert), `per` tiles per expert.
-// Routed launches interleave the tiles of kWgradWindow consecutive experts: the
-// concurrent CTAs then share a few experts' operands in L2 (a few tens of MB), and the
-// zero tiles of an expert without rows (stores only) run beside other experts' MMAs
-// instead of in a store-only phase of their own.
-constexpr int kWgradWindow = 4;
-__device__ __forceinline__ void wgrad_expert_of(int t, int per, int E, bool routed, int& e, int& local) {
-  if (!routed) {
-    e = t / per;
-    local = t % per;
-    return;
-  }
-  const int e0 = t / (kWgradWindow * per) * kWgradWindow;
-  const int gsz = E - e0 < kWgradWindow ? E - e0 : kWgradWindow;
-  const int u = t - e0 * per;
-  e = e0 + u % gsz;
-  local = u / gsz;
-}
-
 template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                             const int* s_cnt) {
@@ -165,8 +146,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
-    int e, local;
-    wgrad_expert_of(t, per, g.E, g.dense_rows <= 0, e, local);
+    const int e = t / per, local = t % per;
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
@@ -226,8 +206,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   } else {
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
-    int e, local;
-    wgrad_expert_of(t, per, g.E, g.dense_rows <= 0, e, local);
+    const int e = t / per, local = t % per;
     const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
