@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
 constexpr int kSmallTok = 32;
 constexpr int kSmallAssign = 16384;
 constexpr int kSmallMaxE = 32;
-constexpr int64_t kSmallWork = 131072;  // T*k*E: at most 64 ballots per 32 assignments of a warp's share
+constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 512 ballots
 
 __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restrict__ topk_idx,
                                                         const int32_t* __restrict__ counts,
@@ -251,16 +251,28 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
   __shared__ int s_tot[kSmallMaxE];
   __shared__ int s_slot[kSmallTok * 32];   // slots of this CTA's assignments (k <= 32)
+  extern __shared__ int s_idx[];           // all of topk_idx (S <= kSmallAssign ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t S = (int64_t)T * k;
+  const int S = T * k;
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
-  const int64_t a0 = (int64_t)t0 * k;  // this CTA's first assignment
+  const int a0 = t0 * k;  // this CTA's first assignment
+  // topk_idx into shared memory first, every load in flight at once (16-byte loads when
+  // the buffer is 16-byte aligned), so the counting passes below wait on no global load
+  if ((reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0) {
+    const int nv = S / 4;
+    for (int v = threadIdx.x; v < nv; v += 256)
+      reinterpret_cast<int4*>(s_idx)[v] = __ldg(reinterpret_cast<const int4*>(topk_idx) + v);
+    for (int i = nv * 4 + threadIdx.x; i < S; i += 256) s_idx[i] = __ldg(topk_idx + i);
+  } else {
+    for (int i = threadIdx.x; i < S; i += 256) s_idx[i] = __ldg(topk_idx + i);
+  }
+  __syncthreads();
   int before = 0, total = 0;
-  for (int64_t i0 = (int64_t)warp * 32; i0 < S; i0 += 256) {
-    const int64_t i = i0 + lane;
-    const int e = i < S ? topk_idx[i] : -1;
-    const int64_t nb = a0 - i0;  // lanes of this pass that come before a0
+  for (int i0 = warp * 32; i0 < S; i0 += 256) {
+    const int i = i0 + lane;
+    const int e = i < S ? s_idx[i] : -1;
+    const int nb = a0 - i0;  // lanes of this pass that come before a0
     const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
     for (int x = 0; x < E; ++x) {
       const unsigned m = __ballot_sync(0xffffffffu, e == x);
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
     const unsigned lt = (1u << lane) - 1u;
     for (int b = 0; b < n; b += 32) {
       const int i = b + lane;
-      int e = i < n ? topk_idx[a0 + i] : -1 - lane;
+      int e = i < n ? s_idx[a0 + i] : -1 - lane;
       const bool ok = i < n && (unsigned)e < (unsigned)E;
       if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
       const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -777,9 +789,12 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
       (int64_t)c.T * c.k * c.E <= kSmallWork) {
     // a small dropless layer: the whole dispatch in one launch
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;
-    k_dispatch_small<<<tb + c.E * kPadSplit, 256, 0, st>>>(topk_idx, counts, X, c.T, c.H, c.E, c.k, c.align, tb,
-                                                           offsets, tile_offsets, kept, row_id_map, slot_src, Xperm,
-                                                           err);
+    const size_t smem = sizeof(int) * (size_t)c.T * c.k;  // <= 64 KB
+    static std::atomic<uint64_t> attr{0};
+    if ((e = raise_smem_limit(attr, k_dispatch_small, sizeof(int) * kSmallAssign)) != cudaSuccess) return e;
+    k_dispatch_small<<<tb + c.E * kPadSplit, 256, smem, st>>>(topk_idx, counts, X, c.T, c.H, c.E, c.k, c.align, tb,
+                                                              offsets, tile_offsets, kept, row_id_map, slot_src, Xperm,
+                                                              err);
     return cudaGetLastError();
   }
   if (nch > 0) {
