@@ -112,27 +112,6 @@ struct Tile {
   bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
 };
 
-// Weight-gradient tile t -> (expert, tile within the expert), `per` tiles per expert.
-// Routed launches keep the tiles of experts with rows in expert order (the concurrent
-// CTAs share one expert's operands in L2) and spread the zero tiles of the experts
-// without rows evenly between them: position t is a zero tile when floor((t+1) Z / N)
-// > floor(t Z / N) (Z zero tiles of N in all), so each CTA's zero-tile stores run
-// beside the MMAs of its next tiles instead of in a store-only phase of all CTAs.
-// s_order: the experts with rows in order, then those without; n_rows: how many have rows.
-__device__ __forceinline__ void wgrad_expert_of(int t, int per, int E, const int* s_order, int n_rows, int& e,
-                                                int& local) {
-  const int64_t n_all = (int64_t)E * per, n_zero = (int64_t)(E - n_rows) * per;
-  const int64_t zb = (int64_t)t * n_zero / n_all;  // zero tiles before position t
-  if ((int64_t)(t + 1) * n_zero / n_all > zb) {
-    e = s_order[n_rows + (int)(zb / per)];
-    local = (int)(zb % per);
-  } else {
-    const int64_t u = t - zb;
-    e = s_order[(int)(u / per)];
-    local = (int)(u % per);
-  }
-}
-
 template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                             const int* s_cnt) {
@@ -167,8 +146,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
-    int e = t / per, local = t % per;
-    if (g.dense_rows <= 0) wgrad_expert_of(t, per, g.E, s_tile, s_tile[256], e, local);
+    const int e = t / per, local = t % per;
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
@@ -228,8 +206,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   } else {
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
-    int e = t / per, local = t % per;
-    if (g.dense_rows <= 0) wgrad_expert_of(t, per, g.E, s_tile, s_tile[256], e, local);
+    const int e = t / per, local = t % per;
     const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
@@ -394,19 +371,6 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       if (threadIdx.x == 0) {
         s_ptile[0] = 0;
         for (int e = 0; e < g.E; ++e) s_ptile[e + 1] = s_ptile[e] + (s_tile[e + 1] - s_tile[e] + 1) / 2;
-      }
-    }
-    if (MODE == MODE_WGRAD) {
-      // weight gradients: s_tile holds the expert order of the tile schedule (experts with
-      // rows, then those without) and s_tile[256] how many have rows (wgrad_expert_of)
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int n = 0;
-        for (int e = 0; e < g.E; ++e)
-          if (s_cnt[e] > 0) s_tile[n++] = e;
-        s_tile[256] = n;
-        for (int e = 0; e < g.E; ++e)
-          if (s_cnt[e] <= 0) s_tile[n++] = e;
       }
     }
   }

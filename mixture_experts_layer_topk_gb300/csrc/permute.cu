@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
 // CTAs past the token range mark and zero the padding rows, kPadSplit CTAs per expert.
 // CTA 0 writes offsets, tile_offsets and kept, and checks the totals against counts.
 // The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
-constexpr int kSmallTok = 32;
+constexpr int kSmallTok = 16;
 constexpr int kSmallAssign = 16384;
 constexpr int kSmallMaxE = 32;
 constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 512 ballots
@@ -362,8 +362,9 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   }
   if (!Xperm) return;
   __syncthreads();
-  // rows: warp w copies tokens w, w + 8, ... of this CTA, U vectors per lane in flight
-  constexpr int U = kGatherUnroll;
+  // rows: warp w copies tokens w, w + 8, ... of this CTA; each lane has U = 16 vectors in
+  // flight (a whole 4096-wide row per warp), since these few CTAs carry the whole copy
+  constexpr int U = 16;
   const int nvec = H / 8;
   for (int tt = warp; tt < nt; tt += 8) {
     const int t = t0 + tt;
