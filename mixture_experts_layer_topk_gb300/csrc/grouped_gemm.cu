@@ -49,6 +49,9 @@ struct Geo {
   static constexpr int THREADS = FP8 ? 320 : 192; // + 4 scale-factor warps for FP8
 };
 constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
+// bf16 weight gradients: token rows per stage (both operands MN-major, 128-byte rows of
+// 64 columns); 8 MMAs per stage wait and commit
+constexpr int kWgradRows = 128;
 constexpr int kEpiBarrier = 1;  // named barrier of the first epilogue warpgroup (the second uses 2)
 
 // Threads of a launch: 6 warps, plus 4 scale-factor warps (FP8) or a second epilogue
@@ -319,12 +322,17 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapD, const GemmArgs g) {
   using G = Geo<FP8>;
-  constexpr int BK = G::BKE;
+  // K per stage: 128 bytes of each K-major row, or (bf16 weight gradients) kWgradRows token
+  // rows of the MN-major operands
+  constexpr bool WROWS = MODE == MODE_WGRAD && EPI == EPI_STORE && !FP8;
+  constexpr int BK = WROWS ? kWgradRows : G::BKE;
   constexpr int kThreads = threads_of<FP8, NEPI>();
-  constexpr int A_BYTES = BM * 128;
+  constexpr int ROWB = BK * G::EB;          // bytes per operand row (MN-major: per MN atom row x rows)
+  constexpr int A_BYTES = BM * ROWB;
   constexpr int BNL = PAIR ? BN / 2 : BN;  // B rows (N) held by this CTA
-  constexpr int B_BYTES = BNL * 128;
+  constexpr int B_BYTES = BNL * ROWB;
   constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr int MNB = 128 * BK;            // bytes of one MN-major box: 128-byte rows x BK rows
   constexpr uint32_t TMEM_COLS = FP8 ? 512 : 2 * BN;  // FP8: accumulators + per-stage scale columns
   constexpr uint32_t SFC = 2 * BN;                    // first scale-factor column (FP8): 8 per stage
   constexpr uint32_t IDESC = FP8 ? idesc_mxf8(BM, BN, MODE == MODE_WGRAD, MODE != MODE_FWD)
@@ -439,12 +447,16 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       const int sr = __ldg(g.gather_src + r);
       return sr >= 0 ? sr / g.gather_k : g.gather_oob;
     };
-    int idx[4];
+    constexpr int NH = MODE == MODE_FWD ? 1 : BK / 64;  // WGRAD: 64-row halves of a stage's B rows
+    int idx[NH][4];
     auto rows_of = [&](const Tile& tt, int k_b) {
-      const int64_t base = MODE == MODE_FWD ? (int64_t)tt.m0 + 4 * lane
-                                            : (int64_t)tt.k0 + (int64_t)k_b * BK + 4 * (lane & 15);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) idx[i] = src_row(base + i);
+      for (int h = 0; h < NH; ++h) {
+        const int64_t base = MODE == MODE_FWD ? (int64_t)tt.m0 + 4 * lane
+                                              : (int64_t)tt.k0 + (int64_t)k_b * BK + 64 * h + 4 * (lane & 15);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) idx[h][i] = src_row(base + i);
+      }
     };
     int stage = 0, issued = 0;
     uint32_t phase = 0;
@@ -476,7 +488,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar, 2 * STAGE);
         const uint32_t cbar = mapa_shared(smem_u32(bar), 0);
         if constexpr (MODE == MODE_FWD) {
-          tma_gather4_pair(sa + lane * 512, &mapA, cbar, kc, idx[0], idx[1], idx[2], idx[3]);
+          tma_gather4_pair(sa + lane * 512, &mapA, cbar, kc, idx[0][0], idx[0][1], idx[0][2], idx[0][3]);
           if (lane == 0) {
             const int brow = EPI == EPI_SWIGLU ? (rank ? g.F + tl.n0 : tl.n0) : tl.n0 + rank * BNL;
             tma_load_3d_pair(sb, &mapB, cbar, kc, brow, tl.e);
@@ -485,12 +497,15 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           if (lane == 0) {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d_pair(sa + j * 8192, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
+              tma_load_2d_pair(sa + j * MNB, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
           }
-          // B: two 64-column MN-major boxes of 64 K rows, 16 four-row gathers each
+          // B: two 64-column MN-major boxes of BK rows; each lane gathers four rows of every
+          // 64-row half of its box
           const int j = lane >> 4, q = lane & 15;
-          tma_gather4_pair(sb + j * 8192 + q * 512, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, idx[0], idx[1],
-                           idx[2], idx[3]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            tma_gather4_pair(sb + j * MNB + (64 * h + 4 * q) * 128, &mapB, cbar, tl.n0 + rank * BNL + 64 * j,
+                             idx[h][0], idx[h][1], idx[h][2], idx[h][3]);
         }
         ++issued;
         if (++stage == ST) {
@@ -528,10 +543,10 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
             const uint32_t cbar = mapa_shared(smem_u32(bar), 0);
             if constexpr (MODE == MODE_WGRAD) {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * 8192, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
+              for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MNB, &mapA, cbar, tl.m0 + 64 * j, tl.k0 + kc);
 #pragma unroll
               for (int j = 0; j < BNL / 64; ++j)
-                tma_load_2d_pair(sb + j * 8192, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, tl.k0 + kc);
+                tma_load_2d_pair(sb + j * MNB, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, tl.k0 + kc);
             } else {
               tma_load_2d_pair(sa, &mapA, cbar, kc, tl.m0);
               if constexpr (MODE == MODE_FWD) {
@@ -540,7 +555,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
               } else {
 #pragma unroll
                 for (int j = 0; j < BNL / 64; ++j)
-                  tma_load_3d_pair(sb + j * 8192, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, kc, tl.e);
+                  tma_load_3d_pair(sb + j * MNB, &mapB, cbar, tl.n0 + rank * BNL + 64 * j, kc, tl.e);
               }
             }
           } else {
@@ -548,11 +563,11 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           if constexpr (MODE == MODE_WGRAD) {
 #pragma unroll
             for (int j = 0; j < BM / G::MN_INNER; ++j)
-              tma_load_2d(sa + j * G::MN_BOX, &mapA, bar, tl.m0 + G::MN_INNER * j, tl.k0 + kc);
+              tma_load_2d(sa + j * MNB, &mapA, bar, tl.m0 + G::MN_INNER * j, tl.k0 + kc);
             const int kb_row = g.kwrap > 0 ? (tl.k0 + kc) % g.kwrap : tl.k0 + kc;
 #pragma unroll
             for (int j = 0; j < BN / G::MN_INNER; ++j)
-              tma_load_2d(sb + j * G::MN_BOX, &mapB, bar, tl.n0 + G::MN_INNER * j, kb_row);
+              tma_load_2d(sb + j * MNB, &mapB, bar, tl.n0 + G::MN_INNER * j, kb_row);
           } else {
             tma_load_2d(sa, &mapA, bar, g.kwrap > 0 ? kc % g.kwrap : kc, tl.m0);
             if constexpr (MODE == MODE_FWD) {
@@ -565,7 +580,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
             } else {
 #pragma unroll
               for (int j = 0; j < BN / G::MN_INNER; ++j)
-                tma_load_3d(sb + j * G::MN_BOX, &mapB, bar, tl.n0 + G::MN_INNER * j, kc, tl.e);
+                tma_load_3d(sb + j * MNB, &mapB, bar, tl.n0 + G::MN_INNER * j, kc, tl.e);
             }
           }
           }
@@ -608,10 +623,10 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           constexpr uint32_t MN_STEP = G::KSTEP * 128;
 #pragma unroll
           for (int kk = 0; kk < BK / G::KSTEP; ++kk) {
-            const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * MN_STEP, G::MN_BOX, 1024)
+            const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * MN_STEP, MNB, 1024)
                                                    : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = MODE == MODE_FWD ? smem_desc_sw128(sb + kk * 32, 16, 1024)
-                                                 : smem_desc_sw128(sb + kk * MN_STEP, G::MN_BOX, 1024);
+                                                 : smem_desc_sw128(sb + kk * MN_STEP, MNB, 1024);
             if constexpr (PAIR)
               umma_f16_pair(d, ad, bd, IDESC, (kb | kk) != 0);
             else if constexpr (FP8)
@@ -1008,12 +1023,13 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
 template <int MODE, int EPI, int BN, bool FP8, bool PAIR = false, int NEPI = 1>
 struct Kern {
   static constexpr int BNL = PAIR ? BN / 2 : BN;
-  static constexpr int STAGE = (BM + BNL) * 128;
+  static constexpr bool WROWS = MODE == MODE_WGRAD && EPI == EPI_STORE && !FP8;
+  static constexpr int STAGE = (BM + BNL) * (WROWS ? kWgradRows * 2 : 128);
   // bf16 weight gradients store from registers and need no staging buffer
   static constexpr bool DIRECT = MODE == MODE_WGRAD && EPI == EPI_STORE;
   static constexpr int STAGING = DIRECT ? 0 : NEPI * kStagingBytes;
   // a second epilogue warpgroup's staging buffer takes the room of one operand stage
-  static constexpr int ST = STAGE > 32768 ? 4 : (NEPI == 2 && !DIRECT ? 5 : 6);
+  static constexpr int ST = STAGE > 49152 ? 3 : (STAGE > 32768 ? 4 : (NEPI == 2 && !DIRECT ? 5 : 6));
   static constexpr size_t smem = 1024 + (size_t)ST * STAGE + STAGING + (3 * ST + 6) * 8 + 16 + 4 * 260 * 4;
 };
 
@@ -1239,7 +1255,7 @@ cudaError_t launch_fc2_wgrad(const GemmShape& s, const uint16_t* dYp, const uint
                              cudaStream_t st) {
   const int bn = pick_bn(s.F);
   CUtensorMap ma, mb, md;
-  if (!map2d(&ma, dYp, s.H, s.rows, 64, 64) || !map2d(&mb, Aact, s.F, s.rows, 64, 64) ||
+  if (!map2d(&ma, dYp, s.H, s.rows, 64, kWgradRows) || !map2d(&mb, Aact, s.F, s.rows, 64, kWgradRows) ||
       !map_out(&md, dW2, s.F, s.H, s.dense_rows > 0 ? 1 : s.E))
     return cudaErrorInvalidValue;
   GemmArgs g{};
@@ -1264,8 +1280,9 @@ cudaError_t launch_fc1_wgrad(const GemmShape& s, const uint16_t* dGU, const uint
   const int bn = pick_bn(s.H);
   if (gather && bn != 256) return cudaErrorInvalidValue;  // gathered rows need the CTA-pair kernel
   CUtensorMap ma, mb, md;
-  const bool ok_b = gather ? map2d(&mb, X1, s.H, gather->src_rows, 64, 1) : map2d(&mb, X1, s.H, s.rows, 64, 64);
-  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, 64) || !ok_b ||
+  const bool ok_b =
+      gather ? map2d(&mb, X1, s.H, gather->src_rows, 64, 1) : map2d(&mb, X1, s.H, s.rows, 64, kWgradRows);
+  if (!map2d(&ma, dGU, 2 * (uint64_t)s.F, s.rows, 64, kWgradRows) || !ok_b ||
       !map_out(&md, dW13, s.H, 2 * (uint64_t)s.F, s.dense_rows > 0 ? 1 : s.E))
     return cudaErrorInvalidValue;
   GemmArgs g{};

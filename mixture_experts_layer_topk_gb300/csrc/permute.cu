@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
 // CTAs past the token range mark and zero the padding rows, kPadSplit CTAs per expert.
 // CTA 0 writes offsets, tile_offsets and kept, and checks the totals against counts.
 // The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
-constexpr int kSmallTok = 16;
+constexpr int kSmallTok = 8;  // one token per warp
 constexpr int kSmallAssign = 16384;
 constexpr int kSmallMaxE = 32;
 constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 512 ballots
@@ -257,8 +257,21 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
   const int a0 = t0 * k;  // this CTA's first assignment
-  // topk_idx into shared memory first, every load in flight at once (16-byte loads when
-  // the buffer is 16-byte aligned), so the counting passes below wait on no global load
+  // each warp's token row is loaded first (the first 4096 columns, 16 vectors per lane),
+  // so that its latency passes while the routing is counted; the stores need the slots
+  constexpr int U = 16;
+  const int nvec = H / 8;
+  const int my_t = t0 + warp;
+  const bool copies = Xperm != nullptr && tok_cta && my_t < T;
+  uint4 xv[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int v = 32 * u + lane;
+    xv[u] = copies && v < nvec ? __ldg(reinterpret_cast<const uint4*>(X + (size_t)my_t * H) + v)
+                               : make_uint4(0, 0, 0, 0);
+  }
+  // topk_idx into shared memory, every load in flight at once (16-byte loads when the
+  // buffer is 16-byte aligned), so the counting passes below wait on no global load
   if ((reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0) {
     const int nv = S / 4;
     for (int v = threadIdx.x; v < nv; v += 256)
@@ -360,32 +373,28 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
       }
     }
   }
-  if (!Xperm) return;
-  __syncthreads();
-  // rows: warp w copies tokens w, w + 8, ... of this CTA; each lane has U = 16 vectors in
-  // flight (a whole 4096-wide row per warp), since these few CTAs carry the whole copy
-  constexpr int U = 16;
-  const int nvec = H / 8;
-  for (int tt = warp; tt < nt; tt += 8) {
-    const int t = t0 + tt;
-    const int my_slot = lane < k ? s_slot[tt * k + lane] : -1;
-    const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)t * H);
-    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
-      uint4 xv[U];
+  __syncthreads();  // the slots warp 0 wrote are visible to every warp
+  if (!copies) return;
+  // warp w stores its token's row (preloaded above) to each of the token's k slots;
+  // columns past the first 4096 (H > 4096) are loaded and stored in further rounds
+  const int my_slot = lane < k ? s_slot[warp * k + lane] : -1;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)my_t * H);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    if (v0 > 0) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + 32 * u + lane;
         xv[u] = v < nvec ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
       }
-      for (int j = 0; j < k; ++j) {
-        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-        if (slot < 0) continue;
-        uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      if (slot < 0) continue;
+      uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + 32 * u + lane;
-          if (v < nvec) out[v] = xv[u];
-        }
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < nvec) out[v] = xv[u];
       }
     }
   }
