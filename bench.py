@@ -327,27 +327,87 @@ def traffic_record(kernel, workload):
         return None
 
 
-def cpu_baseline(w, seed, budget_s=15.0):
-    """The CPU oracle's whole-layer forward+backward on the first n tokens of the same workload."""
+def oracle_inputs(w, seed, tokens):
+    """Host inputs for the CPU oracle, for samples drawn from `tokens`.  The routed experts'
+    weights are generated only for the experts those tokens reach (the generator is
+    counter-based, so an expert's slice is the same as in the full tensor; the other
+    experts' pages are never touched); in FP8 mode they are block-quantized once here,
+    outside the timed samples."""
     import oracle as O
-    inp = S.host_inputs(w, seed=seed)
+    inp = S.host_inputs(w, seed=seed, weights=False)
+    T, H, E, F, Fs = w.T, w.H, w.E, w.F, w.F_shared
+    tokens = np.asarray(tokens, np.int64)
+    c = O.cfg(w.replace(T=len(tokens)))
+    logits, scores = O.router(c, np.ascontiguousarray(inp["X"][tokens]), inp["W_r"], inp.get("logit_bias"))
+    used = sorted(set(int(e) for e in O.select(c, logits, scores, inp.get("sel_bias")).ravel()))
+    W13 = np.empty((E, 2 * F, H), np.uint16)
+    W2 = np.empty((E, H, F), np.uint16)
+    for e in used:
+        W13[e] = S.normal_bf16(2 * F * H, seed, S.TID_W13, w.w_std, start=e * 2 * F * H).reshape(2 * F, H)
+        W2[e] = S.normal_bf16(H * F, seed, S.TID_W2, w.w_std, start=e * H * F).reshape(H, F)
+        if w.fp8:
+            W13[e] = O.qdq_weights(W13[e])
+            W2[e] = O.qdq_weights(W2[e])
+    inp["W13"], inp["W2"] = W13, W2
+    if Fs:
+        inp["W13_s"] = S.normal_bf16(2 * Fs * H, seed, S.TID_W13S, w.w_std).reshape(2 * Fs, H)
+        inp["W2_s"] = S.normal_bf16(H * Fs, seed, S.TID_W2S, w.w_std).reshape(H, Fs)
+        if w.fp8:
+            inp["W13_s"] = O.qdq_weights(inp["W13_s"])
+            inp["W2_s"] = O.qdq_weights(inp["W2_s"])
+    return inp
+
+
+def oracle_sample(w, inp, off, n):
+    """The CPU oracle's forward+backward of the layer for the tokens off .. off+n-1: routing
+    (logits, selection, gates), the tokens' outputs, input gradients and gate gradients, the
+    weight gradients of every expert the tokens are routed to and of the shared expert, and
+    the router's weight gradient.  An expert no sampled token reaches has a zero weight
+    gradient; it is not computed.  The independent oracle calls of a sample run side by side
+    on the host's cores."""
+    import oracle as O
+    sub = w.replace(T=n)
+    si = dict(inp)
+    si["X"] = np.ascontiguousarray(inp["X"][off:off + n])
+    si["dY"] = np.ascontiguousarray(inp["dY"][off:off + n])
+    c = O.cfg(sub)
+    logits, scores = O.router(c, si["X"], si["W_r"], si.get("logit_bias"))
+    idx = O.select(c, logits, scores, si.get("sel_bias"))
+    g = O.gates(c, logits, idx)
+    O.dispatch(c, idx)
+    experts = sorted(set(int(x) for x in idx.ravel())) + ([-1] if w.F_shared else [])
+    # the per-expert weight gradients are independent oracle calls: run them side by side
+    # (ctypes releases the GIL) while the tokens' forward+backward runs
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(max_workers=len(experts) + 1) as ex:
+        fut_tk = ex.submit(O.tokens, c, si, idx, logits, g)
+        futs = [ex.submit(O.expert_wgrad, c, si, idx, g, e) for e in experts]
+        tk = fut_tk.result()
+        for f in futs:
+            f.result()
+    O.router_wgrad(c, si["X"], tk["dlogits"])
+
+
+SAMPLE_TEXT = ("forward+backward of the whole layer for the sampled tokens through the CPU oracle (routing, "
+               "outputs, input and gate gradients, the weight gradients of the experts they reach, shared "
+               "expert and router weight gradients), double accumulation")
+
+
+def cpu_baseline(w, seed, budget_s=15.0):
+    """The CPU oracle on the first n tokens of the same workload, n sized for about budget_s."""
+    inp = oracle_inputs(w, seed, np.arange(min(w.T, 256)))
 
     def one(n):
-        sub = w.replace(T=n)
-        si = dict(inp)
-        si["X"] = inp["X"][:n]
-        si["dY"] = inp["dY"][:n]
         t0 = time.perf_counter()
-        O.full_layer(sub, si, mirror=True)
+        oracle_sample(w, inp, 0, n)
         return time.perf_counter() - t0
 
     n0 = 2
     t0 = one(n0)
-    n = max(1, min(w.T, int(n0 * budget_s / max(t0, 1e-3))))
+    n = max(1, min(w.T, 256, int(n0 * budget_s / max(t0, 1e-3))))
     t = one(n)
     return {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"full layer forward+backward (router, dispatch, all {w.E} experts' dgrad and wgrad) of the "
-                      f"first {n} of {w.T} tokens, double accumulation, {t:.1f} s wall",
+            "sample": f"{SAMPLE_TEXT}: the first {n} of {w.T} tokens, {t:.1f} s wall",
             "extrapolated_full_layer_s": round(w.T * t / n, 1)}
 
 
@@ -543,24 +603,23 @@ def bench_ours(args, w):
 def bench_reference(args, w):
     """The CPU oracle as the reference arm: each step is the oracle's whole-layer
     forward+backward on a bounded sample of the workload's tokens."""
-    import oracle as O
     ws_, rank, _ = dist_env()
     if rank != 0:
         return None
-    inp = S.host_inputs(w, seed=args.seed)
+    # each step takes the next n tokens (wrapping); the sample is sized from a 2-token probe
+    # on a small input set, then the inputs of every token the steps will touch are made
+    inp = oracle_inputs(w, args.seed, np.arange(2))
 
     def step(n, off):
-        sub = w.replace(T=n)
-        si = dict(inp)
-        si["X"] = np.ascontiguousarray(inp["X"][off:off + n])
-        si["dY"] = np.ascontiguousarray(inp["dY"][off:off + n])
-        O.full_layer(sub, si, mirror=True)
+        oracle_sample(w, inp, off, n)
 
     t0 = time.perf_counter()
     step(2, 0)
     t_probe = time.perf_counter() - t0
     budget = 150.0 / max(1, args.steps + args.warmup)
     n = max(1, min(w.T, int(2 * budget / max(t_probe, 1e-3))))
+    offs = [(i * n) % max(1, w.T - n) for i in range(args.warmup + args.steps)]
+    inp = oracle_inputs(w, args.seed, np.unique(np.concatenate([np.arange(o, o + n) for o in offs])))
     for i in range(args.warmup):
         step(n, (i * n) % max(1, w.T - n))
     t0 = time.perf_counter()
@@ -574,7 +633,7 @@ def bench_reference(args, w):
             "data": "synthetic (seeded normal inputs)",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared},
             "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{n} of {w.T} tokens per step, whole-layer forward+backward"},
+                             "sample": f"{SAMPLE_TEXT}: {n} of {w.T} tokens per step"},
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
