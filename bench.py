@@ -260,7 +260,11 @@ def launches_per_step(w, gather=False, memory_efficient=False):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
     n = 3                                  # router: W_r split, tensor-core logits, routing
-    n += 3 if gather else 4                # chunk histogram, scan, scatter, (row copy)
+    S_ = w.T * w.k
+    if S_ <= 16384 and w.E <= 32 and S_ * w.E <= 131072:
+        n += 1 if gather else 2            # small layers: dispatch maps in one launch, (row copy)
+    else:
+        n += 3 if gather else 4            # chunk histogram, scan, scatter, (row copy)
     n += 1 if memory_efficient else 0      # fixed-order sum of the gate-gradient partials
     n += 2 * (1 + sh)                      # FC1 (+SwiGLU), FC2
     n += 2                                 # combine, combine backward

@@ -221,55 +221,40 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
   }
 }
 
-// Dispatch of a small layer in one launch (dropless, T*k <= kSmallAssign, E <= 32,
-// T*k*E <= kSmallWork): the
-// four launches above are a chain of short dependent steps, which dominates when the
-// layer moves only ~100 MB.  Here every token CTA takes kSmallTok tokens and
-//   1. counts, from all of topk_idx, each expert's assignments before its first token and
-//      in total (warp ballots, one per expert per 32 assignments; lane e keeps expert e),
+// Dispatch maps of a small layer in one launch (dropless, T*k <= kSmallAssign, E <= 32,
+// T*k*E <= kSmallWork): the chunked path's histogram, scan and scatter are three short
+// dependent launches, which dominate when the layer moves only ~100 MB.  Here every token
+// CTA takes kSmallTok tokens and
+//   1. loads all of topk_idx into shared memory and counts, per expert, the assignments
+//      before its first token and in total (warp ballots, one per expert per 32
+//      assignments; lane e keeps expert e),
 //   2. derives the aligned segment starts and the M-tile schedule from the totals,
-//   3. ranks its own assignments in token order (match_any within a warp, running
-//      per-expert cursors across the warp's passes), writes row_id_map and slot_src,
-//   4. copies its tokens' rows into Xperm (the k slots of each token, 16-byte vectors).
-// CTAs past the token range mark and zero the padding rows, kPadSplit CTAs per expert.
+//   3. ranks its own assignments in token order (match_any within warp 0, running
+//      per-expert cursors across the passes) and writes row_id_map and slot_src.
+// CTAs past the token range mark the padding rows in slot_src, kPadSplit CTAs per expert.
 // CTA 0 writes offsets, tile_offsets and kept, and checks the totals against counts.
-// The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
-constexpr int kSmallTok = 8;  // one token per warp
+// The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}; the
+// row copy (k_copy_rows, which also zeroes the padding rows) follows.
+constexpr int kSmallTok = 128;
 constexpr int kSmallAssign = 16384;
 constexpr int kSmallMaxE = 32;
 constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 512 ballots
 
 __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restrict__ topk_idx,
-                                                        const int32_t* __restrict__ counts,
-                                                        const uint16_t* __restrict__ X, int T, int H, int E, int k,
+                                                        const int32_t* __restrict__ counts, int T, int E, int k,
                                                         int align, int tok_blocks, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ tile_offsets, int32_t* __restrict__ kept,
                                                         int32_t* __restrict__ row_id_map,
-                                                        int32_t* __restrict__ slot_src, uint16_t* __restrict__ Xperm,
-                                                        int* err) {
+                                                        int32_t* __restrict__ slot_src, int* err) {
   __shared__ int s_cnt[2][8][kSmallMaxE];   // per warp: [0] before this CTA's tokens, [1] in total
   __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
   __shared__ int s_tot[kSmallMaxE];
-  __shared__ int s_slot[kSmallTok * 32];   // slots of this CTA's assignments (k <= 32)
   extern __shared__ int s_idx[];           // all of topk_idx (S <= kSmallAssign ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = T * k;
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
   const int a0 = t0 * k;  // this CTA's first assignment
-  // each warp's token row is loaded first (the first 4096 columns, 16 vectors per lane),
-  // so that its latency passes while the routing is counted; the stores need the slots
-  constexpr int U = 16;
-  const int nvec = H / 8;
-  const int my_t = t0 + warp;
-  const bool copies = Xperm != nullptr && tok_cta && my_t < T;
-  uint4 xv[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int v = 32 * u + lane;
-    xv[u] = copies && v < nvec ? __ldg(reinterpret_cast<const uint4*>(X + (size_t)my_t * H) + v)
-                               : make_uint4(0, 0, 0, 0);
-  }
   // topk_idx into shared memory, every load in flight at once (16-byte loads when the
   // buffer is 16-byte aligned), so the counting passes below wait on no global load
   if ((reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0) {
@@ -319,7 +304,6 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
     if (lane < E) {
       s_off[lane + 1] = ir;
       s_tot[lane] = tsum;
-      s_cnt[0][0][lane] = ir - rows + bsum;  // this CTA's first slot for expert `lane`
     }
     if (lane == 0) s_off[0] = 0;
     if (blockIdx.x == 0) {
@@ -331,73 +315,40 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
       }
       if (lane == 0) offsets[0] = tile_offsets[0] = 0;
     }
+    if (tok_cta) {
+      // rank this CTA's assignments; lane e holds the next slot of expert e
+      int cursor = lane < E ? ir - rows + bsum : 0;
+      const int n = min(kSmallTok, T - t0) * k;
+      const unsigned lt = (1u << lane) - 1u;
+      for (int b = 0; b < n; b += 32) {
+        const int i = b + lane;
+        int e = i < n ? s_idx[a0 + i] : -1 - lane;
+        const bool ok = i < n && (unsigned)e < (unsigned)E;
+        if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int base = __shfl_sync(0xffffffffu, cursor, ok ? e : 0);
+        const int slot = ok ? base + __popc(peers & lt) : -1;
+        if (i < n) {
+          row_id_map[a0 + i] = slot;
+          if (ok) slot_src[slot] = a0 + i;
+        }
+        // each expert's cursor advances by its assignments in this pass
+        for (int x = 0; x < E; ++x) {
+          const unsigned m = __ballot_sync(0xffffffffu, ok && e == x);
+          if (lane == x) cursor += __popc(m);
+        }
+      }
+    }
   }
+  if (tok_cta) return;
   __syncthreads();
-  if (!tok_cta) {  // padding rows of one expert's segment: slot_src -1, Xperm rows zero
-    const int p = blockIdx.x - tok_blocks;
-    const int e = p / kPadSplit, part = p % kPadSplit;
-    const int r0e = s_off[e] + s_tot[e], r1e = s_off[e + 1];
-    const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
-    const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
-    for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
-    if (Xperm) {
-      const int64_t nvec = H / 8;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int64_t i = (int64_t)r0 * nvec + threadIdx.x; i < (int64_t)r1 * nvec; i += 256)
-        reinterpret_cast<uint4*>(Xperm)[i] = z;
-    }
-    return;
-  }
-  const int nt = min(kSmallTok, T - t0);
-  const int n = nt * k;  // this CTA's assignments, a0 .. a0 + n - 1
-  if (warp == 0) {
-    int cursor = lane < E ? s_cnt[0][0][lane] : 0;  // lane e: next slot of expert e
-    const unsigned lt = (1u << lane) - 1u;
-    for (int b = 0; b < n; b += 32) {
-      const int i = b + lane;
-      int e = i < n ? s_idx[a0 + i] : -1 - lane;
-      const bool ok = i < n && (unsigned)e < (unsigned)E;
-      if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int base = __shfl_sync(0xffffffffu, cursor, ok ? e : 0);
-      const int slot = ok ? base + __popc(peers & lt) : -1;
-      if (i < n) {
-        row_id_map[a0 + i] = slot;
-        s_slot[i] = slot;
-        if (ok) slot_src[slot] = (int)(a0 + i);
-      }
-      // each expert's cursor advances by its assignments in this pass
-      for (int x = 0; x < E; ++x) {
-        const unsigned m = __ballot_sync(0xffffffffu, ok && e == x);
-        if (lane == x) cursor += __popc(m);
-      }
-    }
-  }
-  __syncthreads();  // the slots warp 0 wrote are visible to every warp
-  if (!copies) return;
-  // warp w stores its token's row (preloaded above) to each of the token's k slots;
-  // columns past the first 4096 (H > 4096) are loaded and stored in further rounds
-  const int my_slot = lane < k ? s_slot[warp * k + lane] : -1;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)my_t * H);
-  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
-    if (v0 > 0) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + 32 * u + lane;
-        xv[u] = v < nvec ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
-      }
-    }
-    for (int j = 0; j < k; ++j) {
-      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      if (slot < 0) continue;
-      uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + 32 * u + lane;
-        if (v < nvec) out[v] = xv[u];
-      }
-    }
-  }
+  // padding rows of one expert's segment: slot_src -1 (k_copy_rows zeroes their Xperm rows)
+  const int p = blockIdx.x - tok_blocks;
+  const int e = p / kPadSplit, part = p % kPadSplit;
+  const int r0e = s_off[e] + s_tot[e], r1e = s_off[e + 1];
+  const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
+  const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
+  for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
 }
 
 // Order-preserving key of a priority: a larger float gives a larger key; -0 and +0
@@ -802,10 +753,15 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
     const size_t smem = sizeof(int) * (size_t)c.T * c.k;  // <= 64 KB
     static std::atomic<uint64_t> attr{0};
     if ((e = raise_smem_limit(attr, k_dispatch_small, sizeof(int) * kSmallAssign)) != cudaSuccess) return e;
-    k_dispatch_small<<<tb + c.E * kPadSplit, 256, smem, st>>>(topk_idx, counts, X, c.T, c.H, c.E, c.k, c.align, tb,
-                                                              offsets, tile_offsets, kept, row_id_map, slot_src, Xperm,
-                                                              err);
-    return cudaGetLastError();
+    k_dispatch_small<<<tb + c.E * kPadSplit, 256, smem, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb, offsets,
+                                                              tile_offsets, kept, row_id_map, slot_src, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (Xperm) {
+      const int cb = (c.T + 7) / 8;
+      k_copy_rows<<<cb + c.E * kPadSplit, 256, 0, st>>>(X, row_id_map, offsets, kept, c.T, c.H, c.k, cb, Xperm);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
   if (nch > 0) {
     k_chunk_hist<<<nch, 256, 0, st>>>(topk_idx, c.T, c.E, c.k, chunk_counts);
