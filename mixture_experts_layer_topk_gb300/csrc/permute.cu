@@ -225,9 +225,9 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
 // T*k*E <= kSmallWork): the chunked path's histogram, scan and scatter are three short
 // dependent launches, which dominate when the layer moves only ~100 MB.  Here every token
 // CTA takes kSmallTok tokens and
-//   1. loads all of topk_idx into shared memory and counts, per expert, the assignments
-//      before its first token and in total (warp ballots, one per expert per 32
-//      assignments; lane e keeps expert e),
+//   1. counts, from all of topk_idx, each expert's assignments before its first token and
+//      in total (warp ballots, one per expert per 32 assignments; lane e keeps expert e;
+//      each warp loads a batch of its ids before counting any),
 //   2. derives the aligned segment starts and the M-tile schedule from the totals,
 //   3. ranks its own assignments in token order (match_any within warp 0, running
 //      per-expert cursors across the passes) and writes row_id_map and slot_src.
@@ -249,34 +249,33 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   __shared__ int s_cnt[2][8][kSmallMaxE];   // per warp: [0] before this CTA's tokens, [1] in total
   __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
   __shared__ int s_tot[kSmallMaxE];
-  extern __shared__ int s_idx[];           // all of topk_idx (S <= kSmallAssign ints)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = T * k;
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
   const int a0 = t0 * k;  // this CTA's first assignment
-  // topk_idx into shared memory, every load in flight at once (16-byte loads when the
-  // buffer is 16-byte aligned), so the counting passes below wait on no global load
-  if ((reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0) {
-    const int nv = S / 4;
-    for (int v = threadIdx.x; v < nv; v += 256)
-      reinterpret_cast<int4*>(s_idx)[v] = __ldg(reinterpret_cast<const int4*>(topk_idx) + v);
-    for (int i = nv * 4 + threadIdx.x; i < S; i += 256) s_idx[i] = __ldg(topk_idx + i);
-  } else {
-    for (int i = threadIdx.x; i < S; i += 256) s_idx[i] = __ldg(topk_idx + i);
-  }
-  __syncthreads();
+  // warp w counts assignments w*32 + 256*p (+ lane); each batch of NB passes
+  // loads all of its ids before counting any, so no pass waits on a load of its own
+  constexpr int NB = kSmallAssign / 256 / 2;  // passes per batch (two batches at most)
   int before = 0, total = 0;
-  for (int i0 = warp * 32; i0 < S; i0 += 256) {
-    const int i = i0 + lane;
-    const int e = i < S ? s_idx[i] : -1;
-    const int nb = a0 - i0;  // lanes of this pass that come before a0
-    const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
-    for (int x = 0; x < E; ++x) {
-      const unsigned m = __ballot_sync(0xffffffffu, e == x);
-      if (lane == x) {
-        total += __popc(m);
-        before += __popc(m & bmask);
+  for (int p0 = 0; p0 * 256 < S; p0 += NB) {
+    int ids[NB];
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int i = (p0 + q) * 256 + warp * 32 + lane;
+      ids[q] = i < S ? __ldg(topk_idx + i) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int i0 = (p0 + q) * 256 + warp * 32;
+      const int nb = a0 - i0;  // lanes of this pass that come before a0
+      const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
+      for (int x = 0; x < E; ++x) {
+        const unsigned m = __ballot_sync(0xffffffffu, ids[q] == x);
+        if (lane == x) {
+          total += __popc(m);
+          before += __popc(m & bmask);
+        }
       }
     }
   }
@@ -322,7 +321,7 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
       const unsigned lt = (1u << lane) - 1u;
       for (int b = 0; b < n; b += 32) {
         const int i = b + lane;
-        int e = i < n ? s_idx[a0 + i] : -1 - lane;
+        int e = i < n ? __ldg(topk_idx + a0 + i) : -1 - lane;
         const bool ok = i < n && (unsigned)e < (unsigned)E;
         if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -750,10 +749,7 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
       (int64_t)c.T * c.k * c.E <= kSmallWork) {
     // a small dropless layer: the whole dispatch in one launch
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;
-    const size_t smem = sizeof(int) * (size_t)c.T * c.k;  // <= 64 KB
-    static std::atomic<uint64_t> attr{0};
-    if ((e = raise_smem_limit(attr, k_dispatch_small, sizeof(int) * kSmallAssign)) != cudaSuccess) return e;
-    k_dispatch_small<<<tb + c.E * kPadSplit, 256, smem, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb, offsets,
+    k_dispatch_small<<<tb + c.E * kPadSplit, 256, 0, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb, offsets,
                                                               tile_offsets, kept, row_id_map, slot_src, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (Xperm) {
