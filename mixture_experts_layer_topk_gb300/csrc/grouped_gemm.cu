@@ -52,10 +52,6 @@ constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
 // bf16 weight gradients: token rows per stage (both operands MN-major, 128-byte rows of
 // 64 columns); 8 MMAs per stage wait and commit
 constexpr int kWgradRows = 128;
-// Routed weight gradients: the CTAs (pairs) split into two groups, one walking the experts
-// from the fewest rows up, the other from the most rows down (section on the schedule in
-// the kernel's prologue)
-constexpr bool kWgradTwoGroups = true;
 constexpr int kEpiBarrier = 1;  // named barrier of the first epilogue warpgroup (the second uses 2)
 
 // Threads of a launch: 6 warps, plus 4 scale-factor warps (FP8) or a second epilogue
@@ -153,7 +149,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
-    const int e = kWgradTwoGroups && g.dense_rows <= 0 ? s_tile[t / per] : t / per, local = t % per;
+    const int e = t / per, local = t % per;
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
@@ -213,7 +209,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   } else {
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
-    const int e = kWgradTwoGroups && g.dense_rows <= 0 ? s_tile[t / per] : t / per, local = t % per;
+    const int e = t / per, local = t % per;
     const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
@@ -385,57 +381,6 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         for (int e = 0; e < g.E; ++e) s_ptile[e + 1] = s_ptile[e] + (s_tile[e + 1] - s_tile[e] + 1) / 2;
       }
     }
-    if (MODE == MODE_WGRAD && kWgradTwoGroups) {
-      // Routed weight gradients: an expert with few rows makes tiles bound by their stores
-      // (a 256x256 output per handful of MMAs; none at all without rows), one with many
-      // rows makes MMA-bound tiles, and all CTAs working on one expert at a time would
-      // alternate between the two.  So the CTAs (pairs) split into two groups: group 0
-      // takes the experts in order of increasing k-blocks, group 1 in order of decreasing
-      // k-blocks, each group on one expert at a time (its operands shared in L2), and the
-      // split point balances a cost of max(8 MMAs per k-block, 18 MMA-times of stores) per
-      // tile against the groups' sizes.  s_tile[0..n) receives this CTA's group's experts in
-      // its order and s_tile[256] their number n; s_ptile is scratch.
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const int npairs = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-        const int pid = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-        const int grp = npairs >= 2 ? (pid & 1) : 0;
-        int* bucket = s_ptile;  // 64 counts, then 64 starts
-        for (int b = 0; b < 64; ++b) bucket[b] = 0;
-        auto kbk = [&](int e) {
-          const int kb = (s_cnt[e] + BK - 1) / BK;
-          return kb < 63 ? kb : 63;
-        };
-        for (int e = 0; e < g.E; ++e) ++bucket[kbk(e)];
-        int acc = 0;
-        for (int b = 0; b < 64; ++b) {
-          bucket[64 + b] = acc;
-          acc += bucket[b];
-        }
-        for (int e = 0; e < g.E; ++e) s_tile[bucket[64 + kbk(e)]++] = e;  // ascending k-blocks
-        auto cost = [&](int e) {
-          const int c = 8 * ((s_cnt[e] + BK - 1) / BK);
-          return c > 18 ? c : 18;
-        };
-        int64_t total_cost = 0;
-        for (int i = 0; i < g.E; ++i) total_cost += cost(s_tile[i]);
-        const int n0 = (npairs + 1) / 2;  // pairs of group 0 (all of them when npairs < 2)
-        int split = g.E;
-        if (npairs >= 2) {
-          int64_t run = 0;
-          split = 0;
-          while (split < g.E && run * npairs < total_cost * n0) run += cost(s_tile[split++]);
-        }
-        if (grp == 0) {
-          s_tile[256] = split;
-        } else {
-          const int n = g.E - split;
-          for (int i = 0; i < n; ++i) s_ptile[i] = s_tile[g.E - 1 - i];  // descending
-          for (int i = 0; i < n; ++i) s_tile[i] = s_ptile[i];
-          s_tile[256] = n;
-        }
-      }
-    }
   }
   // rows of the A tensor map: a coordinate at or past it reads zeros
   const int64_t oob_row = 1LL << 30;
@@ -490,16 +435,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     const int mtl = PAIR ? (g.m_tiles + 1) / 2 : g.m_tiles;
     total = (g.dense_rows > 0 && g.ksplit_rows <= 0 ? 1 : g.E) * mtl * g.n_tiles;
   }
-  int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-  if (MODE == MODE_WGRAD && kWgradTwoGroups && g.dense_rows <= 0) {
-    // this CTA's group (prologue above): its experts' tiles, strided over its pairs
-    const int npairs = t_step, grp = npairs >= 2 ? (t_first & 1) : 0;
-    const int mtl = PAIR ? (g.m_tiles + 1) / 2 : g.m_tiles;
-    total = s_tile[256] * mtl * g.n_tiles;
-    t_step = npairs >= 2 ? (npairs - grp + 1) / 2 : 1;
-    t_first = npairs >= 2 ? t_first >> 1 : t_first;
-  }
+  const int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
 
   if (warp == 0 && PAIR && (MODE == MODE_FWD || MODE == MODE_WGRAD) && g.gather_src) {
     // ------------------------------------------------------------ TMA producer, gathered rows

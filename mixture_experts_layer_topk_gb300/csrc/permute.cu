@@ -249,11 +249,14 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   __shared__ int s_cnt[2][8][kSmallMaxE];   // per warp: [0] before this CTA's tokens, [1] in total
   __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
   __shared__ int s_tot[kSmallMaxE];
+  __shared__ int s_mine[kSmallTok * 32];   // this CTA's assignments (k <= 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = T * k;
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
   const int a0 = t0 * k;  // this CTA's first assignment
+  if (tok_cta)  // this CTA's own assignments, for the ranking below
+    for (int i = threadIdx.x; i < min(kSmallTok, T - t0) * k; i += 256) s_mine[i] = __ldg(topk_idx + a0 + i);
   // warp w counts assignments w*32 + 256*p (+ lane); each batch of NB passes
   // loads all of its ids before counting any, so no pass waits on a load of its own
   constexpr int NB = kSmallAssign / 256 / 2;  // passes per batch (two batches at most)
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
       const unsigned lt = (1u << lane) - 1u;
       for (int b = 0; b < n; b += 32) {
         const int i = b + lane;
-        int e = i < n ? __ldg(topk_idx + a0 + i) : -1 - lane;
+        int e = i < n ? s_mine[i] : -1 - lane;
         const bool ok = i < n && (unsigned)e < (unsigned)E;
         if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
         const unsigned peers = __match_any_sync(0xffffffffu, e);
