@@ -52,36 +52,6 @@ constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
 // bf16 weight gradients: token rows per stage (both operands MN-major, 128-byte rows of
 // 64 columns); 8 MMAs per stage wait and commit
 constexpr int kWgradRows = 128;
-// Routed weight gradients: an expert with at most this many k-blocks makes tiles bound by
-// their stores (k-blocks x 8 MMAs take less time than storing a 256 x 256 bf16 tile)
-constexpr int kLightKb = 2;
-
-// The tiles of one CTA (pair), in order: step s of n gives a tile index.  Tiles are split
-// into a first class [0, n_first) and a second [n_first, total); the CTA takes first,
-// first + step, ... of each class and interleaves its two shares in proportion
-// (Bresenham: a second-class tile whenever the running count of them falls behind).  With
-// an empty second class this is the plain strided walk.  Every role of the kernel runs the
-// same sequence.
-struct TileSeq {
-  int first, step, n_first, hc, lc, n, err, hi, li;
-  __device__ __forceinline__ void init(int first_, int step_, int n_first_, int total) {
-    first = first_;
-    step = step_;
-    n_first = n_first_;
-    hc = n_first > first ? (n_first - first + step - 1) / step : 0;
-    lc = total - n_first > first ? (total - n_first - first + step - 1) / step : 0;
-    n = hc + lc;
-    err = hi = li = 0;
-  }
-  __device__ __forceinline__ int next() {
-    err += lc;
-    if (err >= n && lc > 0) {
-      err -= n;
-      return n_first + first + step * li++;
-    }
-    return first + step * hi++;
-  }
-};
 constexpr int kEpiBarrier = 1;  // named barrier of the first epilogue warpgroup (the second uses 2)
 
 // Threads of a launch: 6 warps, plus 4 scale-factor warps (FP8) or a second epilogue
@@ -179,7 +149,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.valid = true;
   } else {
     const int per = g.m_tiles * g.n_tiles;
-    const int e = g.dense_rows <= 0 ? s_tile[t / per] : t / per, local = t % per;
+    const int e = t / per, local = t % per;
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
@@ -239,7 +209,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
   } else {
     const int mpairs = (g.m_tiles + 1) / 2;
     const int per = mpairs * g.n_tiles;
-    const int e = g.dense_rows <= 0 ? s_tile[t / per] : t / per, local = t % per;
+    const int e = t / per, local = t % per;
     const int m = 2 * (g.n_fast ? local / g.n_tiles : local % mpairs) + rank;
     r.e = e;
     r.valid = m < g.m_tiles;
@@ -411,22 +381,6 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         for (int e = 0; e < g.E; ++e) s_ptile[e + 1] = s_ptile[e] + (s_tile[e + 1] - s_tile[e] + 1) / 2;
       }
     }
-    if (MODE == MODE_WGRAD) {
-      // Routed weight gradients: experts with few rows make store-bound tiles, the others
-      // MMA-bound ones.  s_tile lists the MMA-bound experts in order, then the store-bound
-      // ones (including those without rows) in order, and s_tile[256] counts the former;
-      // tiles index this list, and each CTA interleaves its share of the two classes
-      // (TileSeq) while the CTAs still work through each class one expert at a time.
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int n = 0;
-        for (int e = 0; e < g.E; ++e)
-          if ((s_cnt[e] + BK - 1) / BK > kLightKb) s_tile[n++] = e;
-        s_tile[256] = n;
-        for (int e = 0; e < g.E; ++e)
-          if ((s_cnt[e] + BK - 1) / BK <= kLightKb) s_tile[n++] = e;
-      }
-    }
   }
   // rows of the A tensor map: a coordinate at or past it reads zeros
   const int64_t oob_row = 1LL << 30;
@@ -483,12 +437,6 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
   }
   const int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
   const int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-  TileSeq seq0;
-  {
-    int n_first = total;
-    if (MODE == MODE_WGRAD && g.dense_rows <= 0) n_first = s_tile[256] * (total / (g.E > 0 ? g.E : 1));
-    seq0.init(t_first, t_step, n_first, total);
-  }
 
   if (warp == 0 && PAIR && (MODE == MODE_FWD || MODE == MODE_WGRAD) && g.gather_src) {
     // ------------------------------------------------------------ TMA producer, gathered rows
@@ -513,24 +461,18 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     int stage = 0, issued = 0;
     uint32_t phase = 0;
     bool ok = true;
-    TileSeq sq = seq0;
-    int s_left = sq.n;  // steps not taken yet
-    bool have = false;
+    int t = t_first;
     Tile tl;
     auto next_work = [&]() {  // the next tile with k-blocks, and its first rows
-      have = false;
-      while (s_left > 0) {
-        --s_left;
-        tl = decode(sq.next());
-        if (tl.kb > 0) {
-          have = true;
-          break;
-        }
+      while (t < total) {
+        tl = decode(t);
+        if (tl.kb > 0) break;
+        t += t_step;
       }
-      if (have) rows_of(tl, 0);
+      if (t < total) rows_of(tl, 0);
     };
     next_work();
-    while (have && ok) {
+    while (t < total && ok) {
       for (int kb = 0; kb < tl.kb; ++kb) {
         const int w_ok =
             __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : 0, 0);
@@ -573,6 +515,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         if (MODE == MODE_WGRAD && kb + 1 < tl.kb) rows_of(tl, kb + 1);
       }
       if (!ok) break;
+      t += t_step;
       next_work();
     }
     if (lane == 0) drain_loads<ST, PAIR>(full, issued, rank, tmem_holder + 3, peer_done, STAGE, g.err);
@@ -582,9 +525,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      TileSeq sq = seq0;
-      for (int s = 0; s < sq.n && ok; ++s) {
-        const Tile tl = decode(sq.next());
+      for (int t = t_first; t < total && ok; t += t_step) {
+        const Tile tl = decode(t);
         for (int kb = 0; kb < tl.kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, g.wait_ns)) {
             set_device_error(g.err, MOE_ERR_TIMEOUT, 1);
@@ -658,9 +600,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      TileSeq sq = seq0;
-      for (int s = 0; s < sq.n && ok; ++s) {
-        const Tile tl = decode(sq.next());
+      for (int t = t_first; t < total && ok; t += t_step) {
+        const Tile tl = decode(t);
         if (tl.kb == 0) continue;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, g.wait_ns)) {
           set_device_error(g.err, MOE_ERR_TIMEOUT, 3);
@@ -779,9 +720,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
         mbar_arrive_relaxed(&acc_empty[b]);
       }
     };
-    TileSeq sq = seq0;
-    for (int s = 0; s < sq.n; ++s) {
-      const Tile tl = decode(sq.next());
+    for (int t = t_first; t < total; t += t_step) {
+      const Tile tl = decode(t);
       if constexpr (DIRECT) {
         // each warp: its 32 rows of the tile; group grp: the chunks grp, grp + NEPI, ...
         uint16_t* const dwarp = g.D + (int64_t)tl.e * g.d_estride + (int64_t)(tl.m0 + q * 32) * g.ldd + tl.n0;
@@ -1019,9 +959,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    TileSeq sq = seq0;
-    for (int s = 0; s < sq.n && ok; ++s) {
-      const Tile tl = decode(sq.next());
+    for (int t = t_first; t < total && ok; t += t_step) {
+      const Tile tl = decode(t);
       for (int kb = 0; kb < tl.kb; ++kb) {
         const bool w_ok =
             __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : false, 0);
