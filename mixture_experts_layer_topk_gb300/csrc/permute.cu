@@ -223,62 +223,65 @@ __global__ void __launch_bounds__(256) k_scatter(const int32_t* __restrict__ top
 
 // Dispatch maps of a small layer in one launch (dropless, T*k <= kSmallAssign, E <= 32,
 // T*k*E <= kSmallWork): the chunked path's histogram, scan and scatter are three short
-// dependent launches, which dominate when the layer moves only ~100 MB.  Here every token
-// CTA takes kSmallTok tokens and
+// dependent launches, which dominate when the layer moves only ~100 MB.  Here CTA c takes
+// tokens [c*kSmallTok, (c+1)*kSmallTok) and
 //   1. counts, from all of topk_idx, each expert's assignments before its first token and
 //      in total (warp ballots, one per expert per 32 assignments; lane e keeps expert e;
-//      each warp loads a batch of its ids before counting any),
+//      each warp loads its ids before counting any; 32 warps share the passes),
 //   2. derives the aligned segment starts and the M-tile schedule from the totals,
 //   3. ranks its own assignments in token order (match_any within warp 0, running
-//      per-expert cursors across the passes) and writes row_id_map and slot_src.
-// CTAs past the token range mark the padding rows in slot_src, kPadSplit CTAs per expert.
-// CTA 0 writes offsets, tile_offsets and kept, and checks the totals against counts.
-// The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}; the
-// row copy (k_copy_rows, which also zeroes the padding rows) follows.
+//      per-expert cursors across the passes) and writes row_id_map and slot_src,
+//   4. marks the padding rows of expert c (c < E) in slot_src.
+// The grid has max(token CTAs, E) CTAs.  CTA 0 writes offsets, tile_offsets and kept, and
+// checks the totals against counts.  The slots are those of the chunked path: offsets[e] +
+// #{earlier assignments to e}; the row copy (k_copy_rows, which also zeroes the padding
+// rows) follows.
 constexpr int kSmallTok = 128;
 constexpr int kSmallAssign = 16384;
 constexpr int kSmallMaxE = 32;
-constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 512 ballots
+constexpr int64_t kSmallWork = 131072;  // T*k*E: each warp makes at most 128 ballots
+constexpr int kSmallThreads = 1024;
 
-__global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restrict__ topk_idx,
-                                                        const int32_t* __restrict__ counts, int T, int E, int k,
-                                                        int align, int tok_blocks, int32_t* __restrict__ offsets,
-                                                        int32_t* __restrict__ tile_offsets, int32_t* __restrict__ kept,
-                                                        int32_t* __restrict__ row_id_map,
-                                                        int32_t* __restrict__ slot_src, int* err) {
-  __shared__ int s_cnt[2][8][kSmallMaxE];   // per warp: [0] before this CTA's tokens, [1] in total
-  __shared__ int s_off[kSmallMaxE + 1];    // aligned segment starts
+__global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(const int32_t* __restrict__ topk_idx,
+                                                                  const int32_t* __restrict__ counts, int T, int E,
+                                                                  int k, int align, int tok_blocks,
+                                                                  int32_t* __restrict__ offsets,
+                                                                  int32_t* __restrict__ tile_offsets,
+                                                                  int32_t* __restrict__ kept,
+                                                                  int32_t* __restrict__ row_id_map,
+                                                                  int32_t* __restrict__ slot_src, int* err) {
+  constexpr int NW = kSmallThreads / 32;
+  __shared__ int s_cnt[2][NW][kSmallMaxE];  // per warp: [0] before this CTA's tokens, [1] in total
+  __shared__ int s_off[kSmallMaxE + 1];     // aligned segment starts
   __shared__ int s_tot[kSmallMaxE];
-  __shared__ int s_mine[kSmallTok * 32];   // this CTA's assignments (k <= 32)
+  __shared__ int s_mine[kSmallTok * 32];    // this CTA's assignments (k <= 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = T * k;
   const bool tok_cta = (int)blockIdx.x < tok_blocks;
   const int t0 = tok_cta ? (int)blockIdx.x * kSmallTok : T;
   const int a0 = t0 * k;  // this CTA's first assignment
   if (tok_cta)  // this CTA's own assignments, for the ranking below
-    for (int i = threadIdx.x; i < min(kSmallTok, T - t0) * k; i += 256) s_mine[i] = __ldg(topk_idx + a0 + i);
-  // warp w counts assignments w*32 + 256*p (+ lane); each batch of NB passes
-  // loads all of its ids before counting any, so no pass waits on a load of its own
-  constexpr int NB = kSmallAssign / 256 / 2;  // passes per batch (two batches at most)
+    for (int i = threadIdx.x; i < min(kSmallTok, T - t0) * k; i += kSmallThreads) s_mine[i] = __ldg(topk_idx + a0 + i);
+  // warp w counts assignments w*32 + 32*NW*p (+ lane), loading all of its ids first
+  constexpr int NP = kSmallAssign / (32 * NW);  // passes per warp at most
   int before = 0, total = 0;
-  for (int p0 = 0; p0 * 256 < S; p0 += NB) {
-    int ids[NB];
+  int ids[NP];
 #pragma unroll
-    for (int q = 0; q < NB; ++q) {
-      const int i = (p0 + q) * 256 + warp * 32 + lane;
-      ids[q] = i < S ? __ldg(topk_idx + i) : -1;
-    }
+  for (int q = 0; q < NP; ++q) {
+    const int i = q * 32 * NW + warp * 32 + lane;
+    ids[q] = i < S ? __ldg(topk_idx + i) : -1;
+  }
 #pragma unroll
-    for (int q = 0; q < NB; ++q) {
-      const int i0 = (p0 + q) * 256 + warp * 32;
-      const int nb = a0 - i0;  // lanes of this pass that come before a0
-      const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
-      for (int x = 0; x < E; ++x) {
-        const unsigned m = __ballot_sync(0xffffffffu, ids[q] == x);
-        if (lane == x) {
-          total += __popc(m);
-          before += __popc(m & bmask);
-        }
+  for (int q = 0; q < NP; ++q) {
+    const int i0 = q * 32 * NW + warp * 32;
+    if (i0 >= S) break;
+    const int nb = a0 - i0;  // lanes of this pass that come before a0
+    const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
+    for (int x = 0; x < E; ++x) {
+      const unsigned m = __ballot_sync(0xffffffffu, ids[q] == x);
+      if (lane == x) {
+        total += __popc(m);
+        before += __popc(m & bmask);
       }
     }
   }
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
   __syncthreads();
   if (warp == 0) {
     int bsum = 0, tsum = 0;
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       bsum += s_cnt[0][w][lane];
       tsum += s_cnt[1][w][lane];
     }
@@ -342,15 +345,11 @@ __global__ void __launch_bounds__(256) k_dispatch_small(const int32_t* __restric
       }
     }
   }
-  if (tok_cta) return;
+  const int e = blockIdx.x;
+  if (e >= E) return;
   __syncthreads();
-  // padding rows of one expert's segment: slot_src -1 (k_copy_rows zeroes their Xperm rows)
-  const int p = blockIdx.x - tok_blocks;
-  const int e = p / kPadSplit, part = p % kPadSplit;
-  const int r0e = s_off[e] + s_tot[e], r1e = s_off[e + 1];
-  const int per = (r1e - r0e + kPadSplit - 1) / kPadSplit;
-  const int r0 = r0e + part * per, r1 = min(r1e, r0 + per);
-  for (int r = r0 + threadIdx.x; r < r1; r += 256) slot_src[r] = -1;
+  // the padding rows of expert e: slot_src -1 (k_copy_rows zeroes their Xperm rows)
+  for (int r = s_off[e] + s_tot[e] + threadIdx.x; r < s_off[e + 1]; r += kSmallThreads) slot_src[r] = -1;
 }
 
 // Order-preserving key of a priority: a larger float gives a larger key; -0 and +0
@@ -752,8 +751,9 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
       (int64_t)c.T * c.k * c.E <= kSmallWork) {
     // a small dropless layer: the whole dispatch in one launch
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;
-    k_dispatch_small<<<tb + c.E * kPadSplit, 256, 0, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb, offsets,
-                                                              tile_offsets, kept, row_id_map, slot_src, err);
+    k_dispatch_small<<<tb > c.E ? tb : c.E, kSmallThreads, 0, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb,
+                                                                     offsets, tile_offsets, kept, row_id_map,
+                                                                     slot_src, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (Xperm) {
       const int cb = (c.T + 7) / 8;
