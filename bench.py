@@ -11,10 +11,12 @@ combine, and their backwards (dX, grouped dgrad and wgrad, router gradient).
 
 Prints one JSON line.  `value` is tokens/s with inputs resident in HBM: T over
 the median time of one replay of the step captured as a CUDA graph (K replays
-after W warm-up replays, CUDA events between replays).  A second pass runs K
-eager steps with CUDA events between the stages (and NVTX ranges around them)
-for the per-stage times, the grouped GEMM's roofline and the HBM stages'
-bandwidths.  `e2e` is the same metric through the C ABI with the step's inputs
+after W warm-up replays, CUDA events between replays).  A second pass gives
+the per-stage times, the grouped GEMM's roofline and the HBM stages'
+bandwidths: the step captured again with a CUDA event between the stages (the
+events become nodes of the graph), replayed K times, so that the stage times
+hold no host launch gaps (K eager steps with the same events where the capture
+of events is unavailable).  Every eager step carries an NVTX range per stage.  `e2e` is the same metric through the C ABI with the step's inputs
 copied in from pinned host memory and its outputs (Y, dX) copied back inside
 the timed region.  --impl reference times the CPU oracle instead.
 """
@@ -166,19 +168,19 @@ STAGES = ["router", "permute", "quant_w", "gemm_fwd", "combine", "combine_bwd", 
 
 
 def run_step(layer, X, dY, ev=None):
-    """One forward+backward through the C ABI; ev: list of len(STAGES)+1 events (eager
-    runs only: the events then bracket every stage, with an NVTX range around each)."""
+    """One forward+backward through the C ABI, with an NVTX range around each stage;
+    ev: list of len(STAGES)+1 events recorded between the stages (on the current stream,
+    also while it is being captured)."""
     import torch
     import mixture_experts_layer_topk_gb300 as M
     c, w = layer.cfg, layer.w
     nvtx = torch.cuda.nvtx
 
     def rec(i):
-        if ev is None:
-            return
         if i > 0:
             nvtx.range_pop()
-        ev[i].record()
+        if ev is not None:
+            ev[i].record()
         if i < len(STAGES):
             nvtx.range_push(STAGES[i])
 
@@ -256,13 +258,17 @@ def run_step(layer, X, dY, ev=None):
     rec(9)
 
 
-def launches_per_step(w, gather=False, memory_efficient=False):
+def launches_per_step(w, gather=False, memory_efficient=False, nsm=152):
     """Kernels of ours launched by run_step (memsets are not counted)."""
     sh = 1 if w.F_shared else 0
     n = 3                                  # router: W_r split, tensor-core logits, routing
     S_ = w.T * w.k
     if S_ <= 16384 and w.E <= 32 and S_ * w.E <= 131072:
-        n += 1 if gather else 2            # small layers: dispatch maps in one launch, (row copy)
+        # small layers: maps and row copy in one launch when each CTA's token rows fit its
+        # shared memory (one CTA per SM); otherwise the maps, then (without gather) the copy
+        tpc = -(-w.T // min(nsm, w.T))
+        fused = not gather and tpc * w.H * 2 <= 219 * 1024 and tpc * w.k <= 1024
+        n += 1 if (gather or fused) else 2
     else:
         n += 3 if gather else 4            # chunk histogram, scan, scatter, (row copy)
     n += 1 if memory_efficient else 0      # fixed-order sum of the gate-gradient partials
@@ -471,16 +477,47 @@ def bench_ours(args, w):
     if layer.device_error() != 0:
         raise RuntimeError("device error during the timed replays")
 
-    # stage pass: K eager steps, events around every stage on the launching stream
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
-    barrier()
-    for i in range(args.steps):
-        run_step(layer, X, dY, sevs[i])
+    # stage pass: the step captured with an event between the stages (event nodes of the
+    # graph) and replayed K times, each replay's stage times read after it; K eager steps
+    # with the same events where events cannot be recorded into a graph
+    ns = len(STAGES)
+    stage_sum = [0.0] * ns
+    pass_ms = 0.0
+    stage_timing = "graph"
+    try:
+        sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(ns + 1)]
+        sgraph = torch.cuda.CUDAGraph()
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(sgraph, stream=cs):
+                run_step(layer, X, dY, sev)
+        stream.wait_stream(cs)
+        barrier()
+        for i in range(args.steps):
+            sgraph.replay()
+            torch.cuda.synchronize()
+            for j in range(ns):
+                stage_sum[j] += sev[j].elapsed_time(sev[j + 1])
+            pass_ms += sev[0].elapsed_time(sev[-1])
+        del sgraph
+    except (TypeError, RuntimeError) as exc:
+        stage_timing = "eager (" + type(exc).__name__ + " capturing the stage events)"
+        stage_sum = [0.0] * ns
+        pass_ms = 0.0
+        torch.cuda.synchronize()
+        sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            run_step(layer, X, dY, sevs[i])
+        barrier()
+        for i in range(args.steps):
+            for j in range(ns):
+                stage_sum[j] += sevs[i][j].elapsed_time(sevs[i][j + 1])
+            pass_ms += sevs[i][0].elapsed_time(sevs[i][-1])
     barrier()
     clocks = sampler.stop()
-    stage_ms = {s: sum(sevs[i][j].elapsed_time(sevs[i][j + 1]) for i in range(args.steps)) / args.steps
-                for j, s in enumerate(STAGES)}
-    eager_ms = sum(sevs[i][0].elapsed_time(sevs[i][-1]) for i in range(args.steps)) / args.steps
+    stage_ms = {s: stage_sum[j] / args.steps for j, s in enumerate(STAGES)}
+    stage_pass_ms = pass_ms / args.steps
     if layer.device_error() != 0:
         raise RuntimeError("device error during the stage pass")
 
@@ -573,7 +610,7 @@ def bench_ours(args, w):
         "timing": {"value_from": "median of K CUDA-graph replays of the whole step",
                    "ms_per_step_mean": round(total_ms / args.steps, 4),
                    "ms_per_step_min": round(min(replay_ms), 4), "ms_per_step_max": round(max(replay_ms), 4),
-                   "eager_ms_per_step": round(eager_ms, 4)},
+                   "stage_timing": stage_timing, "stage_pass_ms_per_step": round(stage_pass_ms, 4)},
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "F_shared": w.F_shared,
                    "router": ("softmax" if w.score_fn == 0 else "sigmoid") + (", renorm" if w.renorm else "")
                              + (f", {w.n_group} groups / top-{w.topk_group}" if w.n_group > 1 else "")
@@ -593,7 +630,8 @@ def bench_ours(args, w):
                      "traffic": traffic},
         "hbm_stages": hbm,
         "clocks": clocks,
-        "gpu_launches": launches_per_step(w, gather=args.gather, memory_efficient=args.memory_efficient) * args.steps,
+        "gpu_launches": launches_per_step(w, gather=args.gather, memory_efficient=args.memory_efficient,
+                                          nsm=torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
         "e2e": {"value": round(tokens / (e2e_ms / args.steps / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * X.numel() * 2, "d2h_bytes_per_step": 2 * X.numel() * 2},
     }

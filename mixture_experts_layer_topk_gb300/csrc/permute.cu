@@ -7,7 +7,9 @@
 // asks for sync-free execution of the dropless layer: here the expert sizes
 // never leave the device.  A per-chunk histogram, a one-CTA scan and a
 // scatter produce the permutation; the scan also writes the grouped GEMM's
-// M-tile schedule (tile_offsets), so no host round trip is needed.
+// M-tile schedule (tile_offsets), so no host round trip is needed.  A small
+// dropless layer (T*k <= 16K, E <= 32) takes one launch in all when its token
+// rows fit the copy CTAs' shared memory.
 //
 // Slot of assignment (t, j) routed to expert e:
 //   offsets[e] + #{t' < t : e selected by t'}     (tokens keep their order)
@@ -350,6 +352,163 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(const int32_t*
   __syncthreads();
   // the padding rows of expert e: slot_src -1 (k_copy_rows zeroes their Xperm rows)
   for (int r = s_off[e] + s_tot[e] + threadIdx.x; r < s_off[e + 1]; r += kSmallThreads) slot_src[r] = -1;
+}
+
+// The whole dispatch of a small dropless layer with its row copy, in one launch
+// (T*k <= kSmallAssign, E <= 32, each CTA's token rows fit in shared memory).  On such a
+// layer the copy moves ~100 MB and the maps kernel's latency, paid before the copy can
+// start, is what keeps the stage off the memory roofline.  Here CTA c owns tokens
+// [c*tpc, (c+1)*tpc) and
+//   1. one thread starts bulk copies of the CTA's X rows into shared memory;
+//   2. while they are in flight all threads count, from all of topk_idx, each expert's
+//      assignments before the CTA's first assignment and from it on (one match_any per
+//      32 assignments, the group leaders adding into shared counters);
+//   3. warp 0 derives the aligned segments (CTA 0 writes offsets, tile_offsets and kept
+//      and checks the totals against counts) and ranks the CTA's assignments in token
+//      order (row_id_map, slot_src);
+//   4. once the rows have arrived, warp 0 writes each to its slots of Xperm with bulk
+//      copies, while the other warps zero this CTA's share of all experts' padding rows
+//      (slot_src -1).
+// The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedMaxAssign = 1024;               // tpc*k: the CTA's slots kept in shared memory
+constexpr int kFusedRowBytes = 219 * 1024;          // tpc*H*2: the CTA's rows
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
+    const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ counts, int T,
+    int H, int E, int k, int align, int tpc, int32_t* __restrict__ offsets, int32_t* __restrict__ tile_offsets,
+    int32_t* __restrict__ kept, int32_t* __restrict__ row_id_map, int32_t* __restrict__ slot_src,
+    uint16_t* __restrict__ Xperm, int* err) {
+  extern __shared__ __align__(128) uint8_t s_rows[];  // the CTA's token rows of X
+  __shared__ uint64_t bar;
+  __shared__ int s_h[64];  // [e]: assignments to e before this CTA's first; [32 + e]: from it on
+  __shared__ int s_off[kSmallMaxE + 1], s_tot[kSmallMaxE], s_pad[kSmallMaxE + 1], s_cur[kSmallMaxE];
+  __shared__ int s_slot[kFusedMaxAssign];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = T * k;
+  const int t0 = (int)blockIdx.x * tpc, nt = min(tpc, T - t0);
+  const int a0 = t0 * k, n = nt * k;
+  const uint32_t row_bytes = (uint32_t)H * 2u;
+  if (threadIdx.x < 64) s_h[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, row_bytes * (uint32_t)nt);
+    for (int j = 0; j < nt; ++j) bulk_load_1d(s_rows + (size_t)j * row_bytes, X + (size_t)(t0 + j) * H, row_bytes, &bar);
+  }
+  __syncthreads();
+  // 2. counts: each warp loads its ids of all passes first
+  constexpr int NP = kSmallAssign / kFusedThreads;
+  int ids[NP];
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int i = q * kFusedThreads + (int)threadIdx.x;
+    ids[q] = i < S ? __ldg(topk_idx + i) : -1;
+  }
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int i = q * kFusedThreads + (int)threadIdx.x;
+    if (q * kFusedThreads + warp * 32 >= S) break;  // warp-uniform
+    const bool ok = i < S && (unsigned)ids[q] < (unsigned)E;
+    const int key = ok ? ids[q] + (i < a0 ? 0 : 32) : -1 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_h[key], __popc(peers));
+  }
+  __syncthreads();
+  // 3. segments and this CTA's ranks
+  if (warp == 0) {
+    const int before = lane < E ? s_h[lane] : 0;
+    const int tsum = lane < E ? before + s_h[32 + lane] : 0;
+    const int rows = (tsum + align - 1) / align * align, tiles = (tsum + 127) / 128, pad = rows - tsum;
+    int ir = rows, it = tiles, ip = pad;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ir, o), b = __shfl_up_sync(0xffffffffu, it, o),
+                c = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) {
+        ir += a;
+        it += b;
+        ip += c;
+      }
+    }
+    if (lane < E) {
+      s_off[lane + 1] = ir;
+      s_tot[lane] = tsum;
+      s_pad[lane + 1] = ip;
+      s_cur[lane] = ir - rows + before;
+    }
+    if (lane == 0) s_off[0] = s_pad[0] = 0;
+    if (blockIdx.x == 0) {
+      if (lane < E) {
+        offsets[lane + 1] = ir;
+        tile_offsets[lane + 1] = it;
+        kept[lane] = tsum;
+        if (tsum != counts[lane]) set_device_error(err, MOE_ERR_DEVICE, 1000 + lane);
+      }
+      if (lane == 0) offsets[0] = tile_offsets[0] = 0;
+    }
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b = 0; b < n; b += 32) {
+      const int i = b + lane;
+      int e = i < n ? __ldg(topk_idx + a0 + i) : -1 - lane;
+      const bool ok = i < n && (unsigned)e < (unsigned)E;
+      if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int base = ok ? s_cur[e] : 0;
+      __syncwarp();
+      const int slot = ok ? base + __popc(peers & lt) : -1;
+      if (i < n) {
+        row_id_map[a0 + i] = slot;
+        s_slot[i] = slot;
+        if (ok) slot_src[slot] = a0 + i;
+      }
+      if (ok && lane == __ffs(peers) - 1) s_cur[e] = base + __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // 4. the rows, once arrived, to their slots (each lane its share of the assignments)
+    bool ok = mbar_wait(&bar, 0);
+    if (!ok) {
+      if (lane == 0) set_device_error(err, MOE_ERR_TIMEOUT, 20);
+      ok = mbar_wait(&bar, 0);  // the copies still in flight write this CTA's shared memory
+    }
+    if (ok) {
+      fence_proxy_async_smem();
+      for (int i = lane; i < n; i += 32) {
+        const int slot = s_slot[i];
+        if (slot >= 0) bulk_store_1d(Xperm + (size_t)slot * H, s_rows + (size_t)(i / k) * row_bytes, row_bytes);
+      }
+      bulk_commit_group();
+      bulk_wait_group_read<0>();  // the stores have read the rows before the CTA exits
+    }
+  } else {
+    // this CTA's share of all experts' padding rows, one warp per row
+    const int P = s_pad[E];
+    const int p0 = (int)((int64_t)P * blockIdx.x / gridDim.x), p1 = (int)((int64_t)P * (blockIdx.x + 1) / gridDim.x);
+    const int nvec = H / 8;
+    for (int p = p0 + warp - 1; p < p1; p += kFusedThreads / 32 - 1) {
+      int e = 0;
+      while (s_pad[e + 1] <= p) ++e;
+      const int row = s_off[e] + s_tot[e] + (p - s_pad[e]);
+      uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)row * H);
+      for (int v = lane; v < nvec; v += 32) out[v] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) slot_src[row] = -1;
+    }
+  }
 }
 
 // Order-preserving key of a priority: a larger float gives a larger key; -0 and +0
@@ -749,7 +908,22 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
   // (every CTA counts all assignments with E ballots per 32 of them: bounded by kSmallWork)
   if (cap == INT_MAX && c.T > 0 && (int64_t)c.T * c.k <= kSmallAssign && c.E <= kSmallMaxE &&
       (int64_t)c.T * c.k * c.E <= kSmallWork) {
-    // a small dropless layer: the whole dispatch in one launch
+    // a small dropless layer: the whole dispatch, with the row copy when each CTA's rows
+    // fit in shared memory, in one launch
+    const int g0 = nsm < c.T ? nsm : c.T;
+    const int tpc = (c.T + g0 - 1) / g0;
+    if (Xperm && (int64_t)tpc * c.H * 2 <= kFusedRowBytes && tpc * c.k <= kFusedMaxAssign) {
+      const int grid = (c.T + tpc - 1) / tpc;
+      const size_t smem = (size_t)tpc * c.H * 2;
+      if (smem > 48 * 1024) {
+        static std::atomic<uint64_t> attr{0};
+        if ((e = raise_smem_limit(attr, k_dispatch_copy_small, kFusedRowBytes)) != cudaSuccess) return e;
+      }
+      k_dispatch_copy_small<<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k, c.align, tpc,
+                                                               offsets, tile_offsets, kept, row_id_map, slot_src,
+                                                               Xperm, err);
+      return cudaGetLastError();
+    }
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;
     k_dispatch_small<<<tb > c.E ? tb : c.E, kSmallThreads, 0, st>>>(topk_idx, counts, c.T, c.E, c.k, c.align, tb,
                                                                      offsets, tile_offsets, kept, row_id_map,

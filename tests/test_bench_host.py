@@ -56,3 +56,13 @@ def test_gathered_rows_accounting():
     w = S.WORKLOADS["dsv3"]
     assert bench.launches_per_step(w, gather=True) == bench.launches_per_step(w) - 1
     assert "permute" not in bench.hbm_bytes(w, gather=True)
+
+
+def test_small_dispatch_accounting():
+    """A small dropless layer whose token rows fit one CTA per SM: maps and row copy in one
+    launch, so gathered rows save no launch there; with more rows per CTA than shared memory
+    holds, the maps and the copy are two launches."""
+    w = S.WORKLOADS["mixtral"]
+    assert bench.launches_per_step(w, gather=True) == bench.launches_per_step(w)
+    big = S.Workload("rows-beyond-shared-memory", T=8000, H=4096, E=8, k=2, F=128)
+    assert bench.launches_per_step(big, gather=True) == bench.launches_per_step(big) - 1
