@@ -18,7 +18,7 @@
 // to 8 splits when the tiles alone would leave SMs idle; split s writes its own
 // partial [T,E] sum, added in a fixed order by the routing pass), 6 warps: warp 0
 // issues the TMA loads of X and the three W_r splits into a ring of stages, warp 1
-// allocates tensor memory (two BN-column block accumulators) and issues the MMAs
+// allocates tensor memory (four or eight BN-column block accumulators) and issues the MMAs
 // from one thread, warps 2-5 drain the block sums, one token row per thread.
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT in the device
 // error word and the CTA unwinds.
@@ -42,7 +42,11 @@ struct RtGeo {
   static constexpr int B = BN * 128;                    // bytes of one split's W tile
   static constexpr int STAGE = kRtA + 3 * B;            // 28, 40 or 64 KB
   static constexpr int ST = BN == 128 ? 3 : (BN == 64 ? 4 : 6);
+  // block-sum accumulators in tensor memory: the MMAs run up to NACC blocks ahead of the
+  // read-out (NACC * BN columns: 256 for BN 32, 256 for 64, 512 for 128)
+  static constexpr int NACC = BN == 32 ? 8 : 4;
   static constexpr size_t SMEM = 1024 + (size_t)ST * STAGE + 256;
+  static_assert((2 * ST + 2 * NACC + 1) * 8 + 4 <= 256, "barriers and the tensor-memory address fit");
 };
 
 struct RouterTcArgs {
@@ -62,14 +66,15 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   using G = RtGeo<BN>;
   constexpr int kRtBN = BN, kRtST = G::ST, kRtB = G::B, kRtStage = G::STAGE;
   constexpr uint32_t IDESC = idesc_bf16(kRtBM, kRtBN, 0, 0);
-  constexpr uint32_t TMEM_COLS = 2 * kRtBN;
+  constexpr int NACC = G::NACC;
+  constexpr uint32_t TMEM_COLS = NACC * kRtBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(tiles + kRtST * kRtStage);
   uint64_t* empty = full + kRtST;
   uint64_t* acc_full = empty + kRtST;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* done_bar = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint64_t* done_bar = acc_empty + NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
@@ -135,8 +140,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int i = 0; i < nk; ++i) {
-        const int b = i & 1;
-        if (!mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1, a.wait_ns) || !mbar_wait(&full[stage], phase, a.wait_ns)) {
+        const int b = i % NACC;
+        if (!mbar_wait(&acc_empty[b], ((i / NACC) & 1) ^ 1, a.wait_ns) || !mbar_wait(&full[stage], phase, a.wait_ns)) {
           set_device_error(a.err, MOE_ERR_TIMEOUT, 13);
           break;
         }
@@ -170,8 +175,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     for (int c = 0; c < kRtBN; ++c) acc[c] = 0.f;
     bool ok = true;
     for (int i = 0; i < nk; ++i) {
-      const int b = i & 1;
-      if (!mbar_wait(&acc_full[b], (i >> 1) & 1, a.wait_ns)) {
+      const int b = i % NACC;
+      if (!mbar_wait(&acc_full[b], (i / NACC) & 1, a.wait_ns)) {
         set_device_error(a.err, MOE_ERR_TIMEOUT, 15);
         ok = false;
         break;
