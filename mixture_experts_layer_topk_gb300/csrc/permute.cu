@@ -359,32 +359,37 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(const int32_t*
 // layer the copy moves ~100 MB and the maps kernel's latency, paid before the copy can
 // start, is what keeps the stage off the memory roofline.  Here CTA c owns tokens
 // [c*tpc, (c+1)*tpc) and
-//   1. one thread starts bulk copies of the CTA's X rows into shared memory;
+//   1. one thread starts bulk copies of the CTA's X rows (contiguous in X) into shared
+//      memory, in 16 KB pieces on one mbarrier, before any other load of the CTA;
 //   2. while they are in flight all threads count, from all of topk_idx, each expert's
-//      assignments before the CTA's first assignment and from it on (one match_any per
-//      32 assignments, the group leaders adding into shared counters);
+//      assignments before the CTA's first assignment and in total: each thread adds its
+//      ids into packed 16-bit counters (two experts per 32-bit word), each warp sums the
+//      words with one redux.sync apiece, and its lanes add them into shared counters;
 //   3. warp 0 derives the aligned segments (CTA 0 writes offsets, tile_offsets and kept
-//      and checks the totals against counts) and ranks the CTA's assignments in token
-//      order (row_id_map, slot_src);
-//   4. once the rows have arrived, warp 0 writes each to its slots of Xperm with bulk
-//      copies, while the other warps zero this CTA's share of all experts' padding rows
-//      (slot_src -1).
+//      and checks the totals against counts) and ranks the CTA's assignments, staged in
+//      shared memory during the count, in token order, into shared memory;
+//   4. once the rows have arrived, each warp takes its share of the CTA's assignments:
+//      it writes row_id_map and slot_src and copies the row from shared memory to its
+//      slot of Xperm (16-byte stores); then it zeroes its share of the CTA's part of all
+//      experts' padding rows (slot_src -1).
+// Reads and writes each keep HBM busy in turn (all CTAs load, then all store): a probe of
+// the phases on the Mixtral-style token shape found the rows arriving ~6 us after launch
+// whatever the order of the pieces, so per-piece barriers gained nothing.
 // The slots are those of the chunked path: offsets[e] + #{earlier assignments to e}.
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedMaxAssign = 1024;               // tpc*k: the CTA's slots kept in shared memory
 constexpr int kFusedRowBytes = 219 * 1024;          // tpc*H*2: the CTA's rows
+constexpr uint32_t kFusedPiece = 16384;             // bytes per bulk copy of the rows
 __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
 
+// EW: packed 32-bit counter words per thread, two experts each (4, for E <= 8), or 0 for
+// the ballot count (E <= 32).
+template <int EW>
 __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
     const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ counts, int T,
     int H, int E, int k, int align, int tpc, int32_t* __restrict__ offsets, int32_t* __restrict__ tile_offsets,
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
   extern __shared__ __align__(128) uint8_t s_rows[];  // the CTA's token rows of X
   __shared__ uint64_t bar;
   __shared__ int s_h[64];  // [e]: assignments to e before this CTA's first; [32 + e]: from it on
-  __shared__ int s_off[kSmallMaxE + 1], s_tot[kSmallMaxE], s_pad[kSmallMaxE + 1], s_cur[kSmallMaxE];
+  __shared__ int s_off[kSmallMaxE + 1], s_tot[kSmallMaxE], s_pad[kSmallMaxE + 1];
   __shared__ int s_slot[kFusedMaxAssign];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = T * k;
@@ -401,14 +406,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
   const int a0 = t0 * k, n = nt * k;
   const uint32_t row_bytes = (uint32_t)H * 2u;
   if (threadIdx.x < 64) s_h[threadIdx.x] = 0;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kFusedThreads - 32) {
+    // before this thread's first load: the release fence of the barrier's initialisation
+    // then has no load of its own to wait for
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, row_bytes * (uint32_t)nt);
-    for (int j = 0; j < nt; ++j) bulk_load_1d(s_rows + (size_t)j * row_bytes, X + (size_t)(t0 + j) * H, row_bytes, &bar);
+    const uint32_t bytes = row_bytes * (uint32_t)nt;
+    mbar_arrive_expect_tx(&bar, bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(X + (size_t)t0 * H);
+    for (uint32_t o = 0; o < bytes; o += kFusedPiece)
+      bulk_load_1d(s_rows + o, src + o, bytes - o < kFusedPiece ? bytes - o : kFusedPiece, &bar);
   }
-  __syncthreads();
-  // 2. counts: each warp loads its ids of all passes first
+  // the caller's totals, for the check by CTA 0 (loaded now, compared after the count)
+  const int cnt_in = blockIdx.x == 0 && (int)threadIdx.x < E ? __ldg(counts + threadIdx.x) : 0;
+  // 2. counts: each thread loads its ids of all passes first, then adds each into packed
+  // counters (expert x: word x/2, bits 16*(x%2); a field never carries, a warp sees at
+  // most 32 * NP = 512 ids), or (EW == 0) counts them with ballots; the CTA's own ids go
+  // to s_slot.
   constexpr int NP = kSmallAssign / kFusedThreads;
   int ids[NP];
 #pragma unroll
@@ -416,20 +430,72 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
     const int i = q * kFusedThreads + (int)threadIdx.x;
     ids[q] = i < S ? __ldg(topk_idx + i) : -1;
   }
+  uint32_t mt = 0u, mb = 0u;  // packed: lane w, experts 2w and 2w+1 (EW > 0)
+  int before = 0, total = 0;   // lane x, expert x (EW == 0)
+  if constexpr (EW > 0) {
+    uint32_t tot[EW], bef[EW];
 #pragma unroll
-  for (int q = 0; q < NP; ++q) {
-    const int i = q * kFusedThreads + (int)threadIdx.x;
-    if (q * kFusedThreads + warp * 32 >= S) break;  // warp-uniform
-    const bool ok = i < S && (unsigned)ids[q] < (unsigned)E;
-    const int key = ok ? ids[q] + (i < a0 ? 0 : 32) : -1 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_h[key], __popc(peers));
+    for (int w = 0; w < EW; ++w) tot[w] = bef[w] = 0u;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      if (q * kFusedThreads >= S) break;  // CTA-uniform
+      const int i = q * kFusedThreads + (int)threadIdx.x;
+      const int id = ids[q];
+      if (i >= a0 && i < a0 + n) s_slot[i - a0] = id;
+      const bool ok = (unsigned)id < (unsigned)E;  // (ids past S are -1)
+      const uint32_t inc = ok ? 1u << ((id & 1) << 4) : 0u, incb = i < a0 ? inc : 0u;
+      const int w0 = id >> 1;
+#pragma unroll
+      for (int w = 0; w < EW; ++w) {
+        tot[w] += w0 == w ? inc : 0u;
+        bef[w] += w0 == w ? incb : 0u;
+      }
+    }
+    // warp sums; lane w keeps word w (totals, and those before the CTA)
+#pragma unroll
+    for (int w = 0; w < EW; ++w) {
+      const uint32_t st = __reduce_add_sync(0xffffffffu, tot[w]), sb = __reduce_add_sync(0xffffffffu, bef[w]);
+      if (lane == w) {
+        mt = st;
+        mb = sb;
+      }
+    }
+  } else {
+    // one ballot per expert per pass, lane x of the warp keeping expert x
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      const int i0 = q * kFusedThreads + warp * 32;
+      if (i0 >= S) break;  // warp-uniform
+      const int i = i0 + lane;
+      if (i >= a0 && i < a0 + n) s_slot[i - a0] = ids[q];
+      const int nb = a0 - i0;  // lanes of this pass before the CTA's first assignment
+      const unsigned bmask = nb >= 32 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << nb) - 1u);
+      for (int x = 0; x < E; ++x) {
+        const unsigned m = __ballot_sync(0xffffffffu, ids[q] == x);
+        if (lane == x) {
+          total += __popc(m);
+          before += __popc(m & bmask);
+        }
+      }
+    }
+  }
+  __syncthreads();  // s_h is zeroed and s_slot holds the CTA's ids
+  if constexpr (EW > 0) {
+    if (lane < EW && mt != 0u) {
+      atomicAdd(&s_h[2 * lane], (int)(mb & 0xffffu));
+      atomicAdd(&s_h[2 * lane + 1], (int)(mb >> 16));
+      atomicAdd(&s_h[32 + 2 * lane], (int)((mt - mb) & 0xffffu));
+      atomicAdd(&s_h[32 + 2 * lane + 1], (int)((mt - mb) >> 16));
+    }
+  } else if (lane < E && total > 0) {
+    atomicAdd(&s_h[lane], before);
+    atomicAdd(&s_h[32 + lane], total - before);
   }
   __syncthreads();
   // 3. segments and this CTA's ranks
   if (warp == 0) {
-    const int before = lane < E ? s_h[lane] : 0;
-    const int tsum = lane < E ? before + s_h[32 + lane] : 0;
+    const int before_e = lane < E ? s_h[lane] : 0;
+    const int tsum = lane < E ? before_e + s_h[32 + lane] : 0;
     const int rows = (tsum + align - 1) / align * align, tiles = (tsum + 127) / 128, pad = rows - tsum;
     int ir = rows, it = tiles, ip = pad;
 #pragma unroll
@@ -446,7 +512,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
       s_off[lane + 1] = ir;
       s_tot[lane] = tsum;
       s_pad[lane + 1] = ip;
-      s_cur[lane] = ir - rows + before;
     }
     if (lane == 0) s_off[0] = s_pad[0] = 0;
     if (blockIdx.x == 0) {
@@ -454,60 +519,72 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
         offsets[lane + 1] = ir;
         tile_offsets[lane + 1] = it;
         kept[lane] = tsum;
-        if (tsum != counts[lane]) set_device_error(err, MOE_ERR_DEVICE, 1000 + lane);
+        if (tsum != cnt_in) set_device_error(err, MOE_ERR_DEVICE, 1000 + lane);
       }
       if (lane == 0) offsets[0] = tile_offsets[0] = 0;
     }
-    __syncwarp();
+    // ranks in token order: lane x holds expert x's next slot; one ballot per expert per 32
+    int cursor = lane < E ? ir - rows + before_e : 0;
     const unsigned lt = (1u << lane) - 1u;
     for (int b = 0; b < n; b += 32) {
       const int i = b + lane;
-      int e = i < n ? __ldg(topk_idx + a0 + i) : -1 - lane;
-      const bool ok = i < n && (unsigned)e < (unsigned)E;
-      if (i < n && !ok) e = -1 - lane;  // an id outside [0,E): no slot
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int base = ok ? s_cur[e] : 0;
-      __syncwarp();
-      const int slot = ok ? base + __popc(peers & lt) : -1;
-      if (i < n) {
-        row_id_map[a0 + i] = slot;
-        s_slot[i] = slot;
-        if (ok) slot_src[slot] = a0 + i;
+      const int e = i < n ? s_slot[i] : -1;
+      const bool ok = i < n && (unsigned)e < (unsigned)E;  // an id outside [0,E): no slot
+      int rank = 0, cnt = 0;
+      for (int x = 0; x < E; ++x) {
+        const unsigned m = __ballot_sync(0xffffffffu, ok && e == x);
+        if (ok && e == x) rank = __popc(m & lt);
+        if (lane == x) cnt = __popc(m);
       }
-      if (ok && lane == __ffs(peers) - 1) s_cur[e] = base + __popc(peers);
-      __syncwarp();
+      const int base = __shfl_sync(0xffffffffu, cursor, ok ? e : 0);
+      cursor += cnt;
+      if (i < n) s_slot[i] = ok ? base + rank : -1;  // the lane's own entry, read above by this lane only
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    // 4. the rows, once arrived, to their slots (each lane its share of the assignments)
-    bool ok = mbar_wait(&bar, 0);
-    if (!ok) {
-      if (lane == 0) set_device_error(err, MOE_ERR_TIMEOUT, 20);
-      ok = mbar_wait(&bar, 0);  // the copies still in flight write this CTA's shared memory
+  // 4. once the rows have arrived (every thread observes the barrier), warp w takes
+  // assignments w, w + 32, ...: their maps and their rows
+  bool ok = mbar_wait(&bar, 0);
+  const int nvec = H / 8;
+  constexpr int NW = kFusedThreads / 32;
+  for (int i = warp; i < n && ok; i += NW) {
+    const int slot = s_slot[i];
+    if (lane == 0) {
+      row_id_map[a0 + i] = slot;
+      if (slot >= 0) slot_src[slot] = a0 + i;
     }
-    if (ok) {
-      fence_proxy_async_smem();
-      for (int i = lane; i < n; i += 32) {
-        const int slot = s_slot[i];
-        if (slot >= 0) bulk_store_1d(Xperm + (size_t)slot * H, s_rows + (size_t)(i / k) * row_bytes, row_bytes);
+    if (slot < 0) continue;
+    const uint4* in = reinterpret_cast<const uint4*>(s_rows + (size_t)(i / k) * row_bytes);
+    uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)slot * H);
+    for (int v0 = 0; v0 < nvec; v0 += 4 * 32) {
+      uint4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < nvec) x[u] = in[v];
       }
-      bulk_commit_group();
-      bulk_wait_group_read<0>();  // the stores have read the rows before the CTA exits
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < nvec) out[v] = x[u];
+      }
     }
-  } else {
-    // this CTA's share of all experts' padding rows, one warp per row
-    const int P = s_pad[E];
-    const int p0 = (int)((int64_t)P * blockIdx.x / gridDim.x), p1 = (int)((int64_t)P * (blockIdx.x + 1) / gridDim.x);
-    const int nvec = H / 8;
-    for (int p = p0 + warp - 1; p < p1; p += kFusedThreads / 32 - 1) {
-      int e = 0;
-      while (s_pad[e + 1] <= p) ++e;
-      const int row = s_off[e] + s_tot[e] + (p - s_pad[e]);
-      uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)row * H);
-      for (int v = lane; v < nvec; v += 32) out[v] = make_uint4(0, 0, 0, 0);
-      if (lane == 0) slot_src[row] = -1;
-    }
+  }
+  if (!ok) {
+    // the wait ran out: record it, and let the copies still in flight land before the CTA exits
+    if (threadIdx.x == 0) set_device_error(err, MOE_ERR_TIMEOUT, 20);
+    mbar_wait(&bar, 0);
+  }
+  // this CTA's share of all experts' padding rows, one warp per row
+  const int P = s_pad[E];
+  const int p0 = (int)((int64_t)P * blockIdx.x / gridDim.x), p1 = (int)((int64_t)P * (blockIdx.x + 1) / gridDim.x);
+  for (int p = p0 + warp; p < p1; p += NW) {
+    int e = 0;
+    while (s_pad[e + 1] <= p) ++e;
+    const int row = s_off[e] + s_tot[e] + (p - s_pad[e]);
+    uint4* out = reinterpret_cast<uint4*>(Xperm + (size_t)row * H);
+    for (int v = lane; v < nvec; v += 32) out[v] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) slot_src[row] = -1;
   }
 }
 
@@ -917,11 +994,19 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
       const size_t smem = (size_t)tpc * c.H * 2;
       if (smem > 48 * 1024) {
         static std::atomic<uint64_t> attr{0};
-        if ((e = raise_smem_limit(attr, k_dispatch_copy_small, kFusedRowBytes)) != cudaSuccess) return e;
+        static std::atomic<uint64_t> attr0{0};
+        if ((e = c.E <= 8 ? raise_smem_limit(attr, k_dispatch_copy_small<4>, kFusedRowBytes)
+                          : raise_smem_limit(attr0, k_dispatch_copy_small<0>, kFusedRowBytes)) != cudaSuccess)
+          return e;
       }
-      k_dispatch_copy_small<<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k, c.align, tpc,
-                                                               offsets, tile_offsets, kept, row_id_map, slot_src,
-                                                               Xperm, err);
+      if (c.E <= 8)
+        k_dispatch_copy_small<4><<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k, c.align,
+                                                                    tpc, offsets, tile_offsets, kept, row_id_map,
+                                                                    slot_src, Xperm, err);
+      else
+        k_dispatch_copy_small<0><<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k,
+                                                                     c.align, tpc, offsets, tile_offsets, kept,
+                                                                     row_id_map, slot_src, Xperm, err);
       return cudaGetLastError();
     }
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;
