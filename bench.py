@@ -16,9 +16,11 @@ the per-stage times, the grouped GEMM's roofline and the HBM stages'
 bandwidths: the step captured again with a CUDA event between the stages (the
 events become nodes of the graph), replayed K times, so that the stage times
 hold no host launch gaps (K eager steps with the same events where the capture
-of events is unavailable).  Every eager step carries an NVTX range per stage.  `e2e` is the same metric through the C ABI with the step's inputs
-copied in from pinned host memory and its outputs (Y, dX) copied back inside
-the timed region.  --impl reference times the CPU oracle instead.
+of events is unavailable).  Every eager step carries an NVTX range per stage.
+`e2e` is the same metric through the C ABI with the step's inputs copied in
+from pinned host memory and its outputs (Y, dX) copied back inside the timed
+region (the step on each of two buffer sets replayed as a CUDA graph, the copies
+on a second stream).  --impl reference times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -524,7 +526,8 @@ def bench_ours(args, w):
     # end to end through the C ABI with host buffers: every step copies its inputs (X, dY)
     # up from pinned host memory and its results (Y, dX) back.  A copy stream moves the
     # next step's inputs and the previous step's results while the current step
-    # computes; inputs and outputs alternate between two device buffers each.
+    # computes; inputs and outputs alternate between two device buffers each, and the step
+    # on each pair of buffers is a CUDA graph of the C-ABI calls, as in the timed replays.
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     dYh = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
     Xh.copy_(X)
@@ -538,6 +541,17 @@ def bench_ours(args, w):
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b are on the device
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b has finished
     ev_out = [torch.cuda.Event() for _ in range(2)]   # results of buffer b are on the host
+    # the step on each buffer set, captured as a CUDA graph like the headline's step
+    egraphs = []
+    for b in range(2):
+        layer.Y, layer.dX = Yd[b], dXd[b]
+        eg = torch.cuda.CUDAGraph()
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(eg, stream=cs):
+                run_step(layer, Xd[b], dYd[b])
+        stream.wait_stream(cs)
+        egraphs.append(eg)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -552,8 +566,7 @@ def bench_ours(args, w):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])
-        layer.Y, layer.dX = Yd[b], dXd[b]
-        run_step(layer, Xd[b], dYd[b])
+        egraphs[b].replay()
         ev_done[b].record(stream)
         with torch.cuda.stream(cs):
             if i >= 1:  # the previous step's results, then the next step's inputs into its buffers
@@ -575,6 +588,7 @@ def bench_ours(args, w):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     layer.Y, layer.dX = Yd[0], dXd[0]
+    del egraphs
 
     med_ms = statistics.median(replay_ms)
     med_ms, total_ms, e2e_ms = max_over_ranks([med_ms, total_ms, e2e_ms], device=dev)

@@ -66,3 +66,4 @@ def test_small_dispatch_accounting():
     assert bench.launches_per_step(w, gather=True) == bench.launches_per_step(w)
     big = S.Workload("rows-beyond-shared-memory", T=8000, H=4096, E=8, k=2, F=128)
     assert bench.launches_per_step(big, gather=True) == bench.launches_per_step(big) - 1
+
