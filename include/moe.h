@@ -95,7 +95,8 @@ moe_status moe_workspace_init(const moe_config* cfg, void* ws, void* stream);
 moe_status moe_read_device_error(void* ws, int32_t* err, void* stream);
 
 /* Limit of every pipeline wait inside the tensor-core kernels (grouped GEMMs, router
- * projection), in nanoseconds; library-wide, read when each kernel is launched (a
+ * projection) and of the one-launch small dispatch's wait for its token rows, in
+ * nanoseconds; library-wide, read when each kernel is launched (a
  * captured graph keeps the value of its capture).  Default 4e9 (4 s).  The pages have
  * no counterpart: this is the library's failure detection.  A wait on another part of
  * the kernel's pipeline (a TMA copy landing, the MMAs of a tile, the epilogue freeing an

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
     const uint16_t* __restrict__ X, const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ counts, int T,
     int H, int E, int k, int align, int tpc, int32_t* __restrict__ offsets, int32_t* __restrict__ tile_offsets,
     int32_t* __restrict__ kept, int32_t* __restrict__ row_id_map, int32_t* __restrict__ slot_src,
-    uint16_t* __restrict__ Xperm, int* err) {
+    uint16_t* __restrict__ Xperm, int* err, uint64_t wait_ns) {
   extern __shared__ __align__(128) uint8_t s_rows[];  // the CTA's token rows of X
   __shared__ uint64_t bar;
   __shared__ int s_h[64];  // [e]: assignments to e before this CTA's first; [32 + e]: from it on
@@ -542,9 +542,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_dispatch_copy_small(
     }
   }
   __syncthreads();
-  // 4. once the rows have arrived (every thread observes the barrier), warp w takes
-  // assignments w, w + 32, ...: their maps and their rows
-  bool ok = mbar_wait(&bar, 0);
+  // 4. once the rows have arrived (every thread observes the barrier, within the library's
+  // wait limit), warp w takes assignments w, w + 32, ...: their maps and their rows
+  bool ok = mbar_wait(&bar, 0, wait_ns);
   const int nvec = H / 8;
   constexpr int NW = kFusedThreads / 32;
   for (int i = warp; i < n && ok; i += NW) {
@@ -1002,11 +1002,12 @@ cudaError_t launch_permute(const moe_config& c, const uint16_t* X, const int32_t
       if (c.E <= 8)
         k_dispatch_copy_small<4><<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k, c.align,
                                                                     tpc, offsets, tile_offsets, kept, row_id_map,
-                                                                    slot_src, Xperm, err);
+                                                                    slot_src, Xperm, err, pipeline_wait_ns());
       else
         k_dispatch_copy_small<0><<<grid, kFusedThreads, smem, st>>>(X, topk_idx, counts, c.T, c.H, c.E, c.k,
                                                                      c.align, tpc, offsets, tile_offsets, kept,
-                                                                     row_id_map, slot_src, Xperm, err);
+                                                                     row_id_map, slot_src, Xperm, err,
+                                                                     pipeline_wait_ns());
       return cudaGetLastError();
     }
     const int tb = (c.T + kSmallTok - 1) / kSmallTok;

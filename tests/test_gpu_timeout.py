@@ -13,8 +13,10 @@ same workspace run clean and reproduce a clean run's outputs bit for bit.
 
 Cases: CTA-pair and one-CTA bf16 tiles (F = 384 gives 128-wide tiles for FC2's
 dgrad and weight gradient), the dense shared-expert segment and the tensor-core
-router (E = 64), and the FP8 block-scaled one-CTA tiles with their scale-factor warps.
+router (E = 64), the FP8 block-scaled one-CTA tiles with their scale-factor warps,
+and the one-launch small dispatch's wait for its token rows.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -107,3 +109,54 @@ def test_wait_timeout_unwinds_and_the_next_call_is_clean(name):
     got = _snapshot(layer)
     for n in OUTPUTS:
         assert torch.equal(got[n], ref[n]), n
+
+
+def test_dispatch_wait_timeout_unwinds():
+    """The one-launch small dispatch waits for its token rows within the same limit.  With
+    the limit at 0 its single test usually comes before the 33.6 MB of rows of this
+    Mixtral-shaped layer have landed: the launch records MOE_ERR_TIMEOUT, waits (bounded)
+    for its copies and exits (or, if every CTA found its rows already there, finishes).
+    Either way the next dispatch on the same workspace reproduces a clean one bit for bit."""
+    w = S.Workload("dispatch-timeout", T=4096, H=4096, E=8, k=2, F=128)
+    cfg = M.config_from(w)
+    rng = np.random.default_rng(11)
+    idx = np.stack([rng.choice(w.E, size=w.k, replace=False) for _ in range(w.T)]).astype(np.int32)
+    X = torch.randn(w.T, w.H, device="cuda").to(torch.bfloat16)
+    topk = torch.from_numpy(idx).cuda()
+    counts = torch.from_numpy(np.bincount(idx.ravel(), minlength=w.E).astype(np.int32)).cuda()
+    R = M.moe_max_rows(cfg)
+    ws = torch.zeros(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    M.moe_workspace_init(cfg, ws)
+
+    def outputs():
+        i32 = torch.int32
+        return [torch.full((w.E + 1,), -7, dtype=i32, device="cuda"),
+                torch.full((w.E + 1,), -7, dtype=i32, device="cuda"),
+                torch.full((w.T, w.k), -7, dtype=i32, device="cuda"),
+                torch.full((R,), -7, dtype=i32, device="cuda"),
+                torch.full((R, w.H), 3.0, dtype=torch.bfloat16, device="cuda")]
+
+    ref = outputs()
+    M.moe_permute(cfg, X, topk, counts, *ref, ws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_error(ws) == 0
+    default = M.moe_get_wait_limit_ns()
+    try:
+        scratch = outputs()
+        M.moe_set_wait_limit_ns(0)
+        M.moe_permute(cfg, X, topk, counts, *scratch, ws)
+        M.moe_set_wait_limit_ns(default)
+        torch.cuda.synchronize()  # the launch ended by itself: the context is usable
+        assert M.moe_read_device_error(ws) in (0, MOE_ERR_TIMEOUT)
+    finally:
+        M.moe_set_wait_limit_ns(default)
+    M.moe_workspace_init(cfg, ws)  # clears the error word
+    got = outputs()
+    M.moe_permute(cfg, X, topk, counts, *got, ws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_error(ws) == 0
+    n_used = int(ref[0][-1])
+    for a, b in zip(got[:3], ref[:3]):
+        assert torch.equal(a, b)
+    assert torch.equal(got[3][:n_used], ref[3][:n_used])
+    assert torch.equal(got[4][:n_used].view(torch.int16), ref[4][:n_used].view(torch.int16))
