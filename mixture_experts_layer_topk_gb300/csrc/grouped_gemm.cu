@@ -113,12 +113,14 @@ struct GemmArgs {
 struct Tile {
   int e, m0, n0, k0, kb;
   bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
+  int krem;    // rows of K in the last k-block (bf16 CTA-pair weight gradients; else BK)
 };
 
 template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                             const int* s_cnt) {
   Tile r;
+  r.krem = BK;
   if constexpr (MODE != MODE_WGRAD) {
     int e = 0, m, n;
     if (g.dense_rows > 0) {
@@ -176,6 +178,7 @@ template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const int* s_seg, const int* s_tile,
                                                  const int* s_ptile, const int* s_cnt, int rank, int64_t oob_row) {
   Tile r;
+  r.krem = BK;
   if constexpr (MODE != MODE_WGRAD) {
     int e = 0, n, mp, mt;
     if (g.dense_rows > 0) {
@@ -215,13 +218,12 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& g, const
     r.valid = m < g.m_tiles;
     r.m0 = m * BM;  // past M when invalid: the MN-major A box reads zeros
     r.n0 = (g.n_fast ? local % g.n_tiles : local / mpairs) * BN;
-    if (g.dense_rows > 0) {
-      r.k0 = 0;
-      r.kb = (g.dense_rows + BK - 1) / BK;
-    } else {
-      r.k0 = s_seg[e];
-      r.kb = (s_cnt[e] + BK - 1) / BK;
-    }
+    const int rows = g.dense_rows > 0 ? g.dense_rows : s_cnt[e];
+    r.k0 = g.dense_rows > 0 ? 0 : s_seg[e];
+    r.kb = (rows + BK - 1) / BK;
+    // the rows past the expert's count in its last block are zero (padding rows of the
+    // 128-aligned segment): their MMA steps add nothing and are skipped
+    if (r.kb > 0) r.krem = rows - (r.kb - 1) * BK;
   }
   return r;
 }
@@ -621,8 +623,11 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           // K-major operands step 32 bytes per instruction inside the 128-byte swizzle row;
           // MN-major operands step KSTEP rows of 128 bytes, with MN atoms MN_BOX bytes apart
           constexpr uint32_t MN_STEP = G::KSTEP * 128;
+          // CTA-pair weight gradients: the last block's K steps past the expert's rows are skipped
+          const int nkk = PAIR && WROWS && kb + 1 == tl.kb ? (tl.krem + G::KSTEP - 1) / G::KSTEP : BK / G::KSTEP;
 #pragma unroll
           for (int kk = 0; kk < BK / G::KSTEP; ++kk) {
+            if (kk >= nkk) break;
             const uint64_t ad = MODE == MODE_WGRAD ? smem_desc_sw128(sa + kk * MN_STEP, MNB, 1024)
                                                    : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = MODE == MODE_FWD ? smem_desc_sw128(sb + kk * 32, 16, 1024)
