@@ -113,7 +113,7 @@ struct GemmArgs {
 struct Tile {
   int e, m0, n0, k0, kb;
   bool valid;  // CTA pairs: this CTA's half of the 256-row tile exists
-  int krem;    // rows of K in the last k-block (bf16 CTA-pair weight gradients; else BK)
+  int krem;    // weight gradients: rows of K in the last k-block (else BK)
 };
 
 template <int MODE, int EPI, int BN, int BK>
@@ -155,17 +155,24 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& g, const int*
     r.e = e;
     r.m0 = (g.n_fast ? local / g.n_tiles : local % g.m_tiles) * BM;
     r.n0 = (g.n_fast ? local % g.n_tiles : local / g.m_tiles) * BN;
+    int rows;
     if (g.dense_rows > 0 && g.ksplit_rows > 0) {
       r.k0 = e * g.ksplit_rows;
-      const int rows = g.dense_rows - r.k0 < g.ksplit_rows ? g.dense_rows - r.k0 : g.ksplit_rows;
+      rows = g.dense_rows - r.k0 < g.ksplit_rows ? g.dense_rows - r.k0 : g.ksplit_rows;
       r.kb = rows > 0 ? (rows + BK - 1) / BK : 0;
     } else if (g.dense_rows > 0) {
       r.k0 = 0;
+      rows = g.dense_rows;
       r.kb = (g.dense_rows + BK - 1) / BK;
     } else {
       r.k0 = s_seg[e];
+      rows = s_cnt[e];
       r.kb = (s_cnt[e] + BK - 1) / BK;
     }
+    // rows past the count in the last block are zero (segment padding, or past the dense
+    // tensor, read as zeros): their MMA steps are skipped.  A split of the dense rows ends
+    // on a block boundary unless it is the last one.
+    if (r.kb > 0) r.krem = rows - (r.kb - 1) * BK;
     r.valid = true;
   }
   return r;
@@ -623,8 +630,8 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           // K-major operands step 32 bytes per instruction inside the 128-byte swizzle row;
           // MN-major operands step KSTEP rows of 128 bytes, with MN atoms MN_BOX bytes apart
           constexpr uint32_t MN_STEP = G::KSTEP * 128;
-          // CTA-pair weight gradients: the last block's K steps past the expert's rows are skipped
-          const int nkk = PAIR && WROWS && kb + 1 == tl.kb ? (tl.krem + G::KSTEP - 1) / G::KSTEP : BK / G::KSTEP;
+          // weight gradients: the last block's K steps past the expert's rows are skipped
+          const int nkk = MODE == MODE_WGRAD && kb + 1 == tl.kb ? (tl.krem + G::KSTEP - 1) / G::KSTEP : BK / G::KSTEP;
 #pragma unroll
           for (int kk = 0; kk < BK / G::KSTEP; ++kk) {
             if (kk >= nkk) break;
