@@ -126,34 +126,56 @@ __device__ void route_token(const RouteArgs& a, int t, const float* lrow, int* h
 #pragma unroll
     for (int i = 0; i < V; ++i) gi[i] = (lane + 32 * i) / per;
     float my_gs = -FLT_MAX;
-    for (int g = 0; g < a.n_group; ++g) {
-      float v1 = -FLT_MAX;
-      int e1 = INT_MAX;
+    if (per == 32 && a.n_group == V) {
+      // each group is one register of every lane (expert lane + 32 g): its best two by one
+      // warp arg-max each, no scan over the lane's other registers
 #pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int e = lane + 32 * i;
-        if (!(excl >> i & 1) && gi[i] == g && (key[i] > v1 || (key[i] == v1 && e < e1))) {
-          v1 = key[i];
-          e1 = e;
+      for (int g = 0; g < V; ++g) {
+        const bool ok = !(excl >> g & 1);
+        const int eg = lane + 32 * g;
+        float v1 = ok ? key[g] : -FLT_MAX;
+        int e1 = ok ? eg : INT_MAX;
+        warp_argmax(v1, e1);
+        float gs = v1;
+        if (a.group_score == 0) {
+          const bool ok2 = ok && eg != e1;
+          float v2 = ok2 ? key[g] : -FLT_MAX;
+          int e2 = ok2 ? eg : INT_MAX;
+          warp_argmax(v2, e2);
+          gs = v1 + v2;
         }
+        if (lane == g) my_gs = gs;
       }
-      warp_argmax(v1, e1);
-      float gs = v1;
-      if (a.group_score == 0 && per > 1) {
-        float v2 = -FLT_MAX;
-        int e2 = INT_MAX;
+    } else {
+      for (int g = 0; g < a.n_group; ++g) {
+        float v1 = -FLT_MAX;
+        int e1 = INT_MAX;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
           const int e = lane + 32 * i;
-          if (!(excl >> i & 1) && gi[i] == g && e != e1 && (key[i] > v2 || (key[i] == v2 && e < e2))) {
-            v2 = key[i];
-            e2 = e;
+          if (!(excl >> i & 1) && gi[i] == g && (key[i] > v1 || (key[i] == v1 && e < e1))) {
+            v1 = key[i];
+            e1 = e;
           }
         }
-        warp_argmax(v2, e2);
-        gs = v1 + v2;
+        warp_argmax(v1, e1);
+        float gs = v1;
+        if (a.group_score == 0 && per > 1) {
+          float v2 = -FLT_MAX;
+          int e2 = INT_MAX;
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            const int e = lane + 32 * i;
+            if (!(excl >> i & 1) && gi[i] == g && e != e1 && (key[i] > v2 || (key[i] == v2 && e < e2))) {
+              v2 = key[i];
+              e2 = e;
+            }
+          }
+          warp_argmax(v2, e2);
+          gs = v1 + v2;
+        }
+        if (lane == g) my_gs = gs;
       }
-      if (lane == g) my_gs = gs;
     }
     uint32_t keep = 0;
     for (int r = 0; r < a.topk_group; ++r) {
@@ -694,23 +716,44 @@ __global__ void __launch_bounds__(256) k_reduce_splits(const float* __restrict__
 }
 
 // W_r [E,H] fp32 -> fwd [3*Ep,H] (row blocks hi, mid, lo) and/or bwd [3*Ep,H] (row blocks
-// hi, mid, hi); rows E..Ep-1 of each block zero.
+// hi, mid, hi); rows E..Ep-1 of each block zero.  Each thread splits 8 consecutive weights
+// of one row (H is a multiple of 8): two 16-byte loads, 16-byte stores of each term.
 __global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, int E, int H, int Ep,
                                                   uint16_t* __restrict__ fwd, uint16_t* __restrict__ bwd) {
-  const int64_t n = (int64_t)Ep * H;
-  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
-    const int e = (int)(i / H), h = (int)(i % H);
-    uint16_t hi = 0, mid = 0, lo = 0;
-    if (e < E) split3(Wr[i], hi, mid, lo);
+  const int n = Ep * H, n8 = n / 8;  // Ep * H < 2^31 (E <= 256, H < 2^23)
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n8; i += gridDim.x * 256) {
+    const int e = i * 8 / H;
+    float w[8];
+    if (e < E) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(Wr) + 2 * i);
+      const float4 b = __ldg(reinterpret_cast<const float4*>(Wr) + 2 * i + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+    }
+    uint32_t hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint16_t h0, m0, l0, h1, m1, l1;
+      split3(w[2 * j], h0, m0, l0);
+      split3(w[2 * j + 1], h1, m1, l1);
+      hi[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      mid[j] = (uint32_t)m0 | ((uint32_t)m1 << 16);
+      lo[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    const uint4 vh = make_uint4(hi[0], hi[1], hi[2], hi[3]), vm = make_uint4(mid[0], mid[1], mid[2], mid[3]),
+                vl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if (fwd) {
-      fwd[i] = hi;
-      fwd[n + i] = mid;
-      fwd[2 * n + i] = lo;
+      reinterpret_cast<uint4*>(fwd)[i] = vh;
+      reinterpret_cast<uint4*>(fwd + n)[i] = vm;
+      reinterpret_cast<uint4*>(fwd + 2 * (size_t)n)[i] = vl;
     }
     if (bwd) {
-      bwd[i] = hi;
-      bwd[n + i] = mid;
-      bwd[2 * n + i] = hi;
+      reinterpret_cast<uint4*>(bwd)[i] = vh;
+      reinterpret_cast<uint4*>(bwd + n)[i] = vm;
+      reinterpret_cast<uint4*>(bwd + 2 * (size_t)n)[i] = vh;
     }
   }
 }
@@ -737,7 +780,8 @@ cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const flo
   // sums added by the routing pass (one warp per token).
   if (w) {
     const int Ep = (c.E + 31) / 32 * 32;
-    int blocks = (int)(((int64_t)Ep * c.H + 255) / 256);
+    if ((int64_t)Ep * c.H >= (1LL << 31)) return cudaErrorInvalidValue;  // k_split_wr indexes in 32 bits
+    int blocks = (int)(((int64_t)Ep * c.H / 8 + 255) / 256);
     blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
     k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, Ep, w->wsplit, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -797,7 +841,8 @@ cudaError_t launch_router_bwd(const moe_config& c, const uint16_t* X, const floa
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (tc) {
-    int blocks = (int)(((int64_t)w.Ep * c.H + 255) / 256);
+    if ((int64_t)w.Ep * c.H >= (1LL << 31)) return cudaErrorInvalidValue;  // k_split_wr indexes in 32 bits
+    int blocks = (int)(((int64_t)w.Ep * c.H / 8 + 255) / 256);
     blocks = blocks < 4 * nsm ? blocks : 4 * nsm;
     k_split_wr<<<blocks, 256, 0, st>>>(Wr, c.E, c.H, w.Ep, nullptr, w.wb);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
