@@ -52,6 +52,8 @@ constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
 // bf16 weight gradients: token rows per stage (both operands MN-major, 128-byte rows of
 // 64 columns); 8 MMAs per stage wait and commit
 constexpr int kWgradRows = 128;
+// FP8: k-blocks whose scale words the scale-factor warps hold in registers ahead of use
+constexpr int kSfAhead = 4;
 constexpr int kEpiBarrier = 1;  // named barrier of the first epilogue warpgroup (the second uses 2)
 
 // Threads of a launch: 6 warps, plus 4 scale-factor warps (FP8) or a second epilogue
@@ -925,7 +927,6 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           const int left = (g.n_valid - tl.n0 + 31) / 32;
           nch = left < nch ? (left > 1 ? left : 1) : nch;
         }
-#pragma unroll 1
         if (grp >= nch) {  // no chunk for this group: hand the accumulator back at once
           tc_fence_before();
           __syncwarp();
@@ -970,50 +971,116 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
     const int q = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int t = t_first; t < total && ok; t += t_step) {
-      const Tile tl = decode(t);
-      for (int kb = 0; kb < tl.kb; ++kb) {
-        const bool w_ok =
-            __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : false, 0);
-        if (!w_ok) {
-          if (lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 7);
-          ok = false;
-          break;
+    auto wait_free = [&]() {  // the stage's previous MMAs have finished with its scale columns
+      const bool w_ok =
+          __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[stage], phase ^ 1, g.wait_ns) : false, 0);
+      if (!w_ok && lane == 0) set_device_error(g.err, MOE_ERR_TIMEOUT, 7);
+      return w_ok;
+    };
+    constexpr uint32_t R4 = 0x01010101u;  // a scale byte in all four bytes of its word
+    // writes the words into this warp's lanes of the stage's scale columns
+    auto put = [&](const uint32_t* wa, const uint32_t* wb) {
+      const uint32_t sf_addr = tmem + ((uint32_t)(q * 32) << 16) + SFC + 8 * stage;
+      tmem_st4(sf_addr, wa[0], wa[1], wa[2], wa[3]);
+      tmem_st4(sf_addr + 4, wb[0], wb[1], wb[2], wb[3]);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[stage]);
+      if (++stage == ST) {
+        stage = 0;
+        phase ^= 1;
+      }
+    };
+    if constexpr (MODE == MODE_FWD) {
+      // The forward GEMMs load each k-block's words once its stage is free: loading them
+      // ahead, as the other modes do, measured slower there.
+      bool ok = true;
+      for (int t = t_first; t < total && ok; t += t_step) {
+        const Tile tl = decode(t);
+        for (int kb = 0; kb < tl.kb; ++kb) {
+          if (!wait_free()) {
+            ok = false;
+            break;
+          }
+          uint32_t wa[4], wb[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = lane + 32 * j;  // tile row of this word
+            const int64_t row = tl.m0 + r;
+            // weights [E][N rows][K]: block (n/128, kb)
+            const int nrow = EPI == EPI_SWIGLU ? (r < BN / 2 ? tl.n0 + r : g.F + tl.n0 + r - BN / 2) : tl.n0 + r;
+            uint32_t a = 127;
+            if (g.dense_rows <= 0 || row < g.dense_rows) a = g.sfa[row * g.sfa_ld + kb];
+            wa[j] = a * R4;
+            wb[j] = g.sfb[((int64_t)tl.e * g.sfb_r + nrow / 128) * g.sfb_c + kb] * R4;
+          }
+          put(wa, wb);
         }
-        uint32_t wa[4], wb[4];
+      }
+    } else {
+      // The dgrads and weight gradients load the words of the next kSfAhead k-blocks into
+      // registers before their stages come free, so the loads' latency overlaps the waits
+      // instead of adding to every k-block (the weight gradients have one to a few k-blocks
+      // per tile).
+      // the bytes only: nothing here waits for the loads
+      auto load_words = [&](const Tile& tl, int kb, uint32_t* wa, uint32_t* wb) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = lane + 32 * j;  // tile row of this word
-          uint32_t a = 127, b = 127;
           if constexpr (MODE == MODE_WGRAD) {
             const int64_t blk = tl.k0 / 128 + kb;  // 128-row block of the token dimension
-            a = g.sfa[blk * g.sfa_ld + tl.m0 + r];
-            b = g.sfb[blk * g.sfb_ld + tl.n0 + r];
-          } else {
+            wa[j] = g.sfa[blk * g.sfa_ld + tl.m0 + r];
+            wb[j] = g.sfb[blk * g.sfb_ld + tl.n0 + r];
+          } else {  // weights [E][K rows][N]: block (kb, n/128)
             const int64_t row = tl.m0 + r;
-            if (g.dense_rows <= 0 || row < g.dense_rows) a = g.sfa[row * g.sfa_ld + kb];
-            if constexpr (MODE == MODE_FWD) {  // weights [E][N rows][K]: block (n/128, kb)
-              const int nrow =
-                  EPI == EPI_SWIGLU ? (r < BN / 2 ? tl.n0 + r : g.F + tl.n0 + r - BN / 2) : tl.n0 + r;
-              b = g.sfb[((int64_t)tl.e * g.sfb_r + nrow / 128) * g.sfb_c + kb];
-            } else {  // weights [E][K rows][N]: block (kb, n/128)
-              b = g.sfb[((int64_t)tl.e * g.sfb_r + kb) * g.sfb_c + (tl.n0 + r) / 128];
-            }
+            wa[j] = g.dense_rows <= 0 || row < g.dense_rows ? g.sfa[row * g.sfa_ld + kb] : 127;
+            wb[j] = g.sfb[((int64_t)tl.e * g.sfb_r + kb) * g.sfb_c + (tl.n0 + r) / 128];
           }
-          wa[j] = a * 0x01010101u;
-          wb[j] = b * 0x01010101u;
         }
-        const uint32_t sf_addr = tmem + ((uint32_t)(q * 32) << 16) + SFC + 8 * stage;
-        tmem_st4(sf_addr, wa[0], wa[1], wa[2], wa[3]);
-        tmem_st4(sf_addr + 4, wb[0], wb[1], wb[2], wb[3]);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_full[stage]);
-        if (++stage == ST) {
-          stage = 0;
-          phase ^= 1;
+      };
+      // the k-blocks in the order the producer and the MMA issuer walk them
+      int t = t_first, kb = 0;
+      Tile tl{};
+      auto seek = [&]() {  // from tile t on, the first tile with a k-block
+        for (; t < total; t += t_step) {
+          tl = decode(t);
+          if (tl.kb > 0) return true;
+        }
+        return false;
+      };
+      bool more = seek();
+      auto fetch = [&](uint32_t* wa, uint32_t* wb) {  // loads the next k-block's words
+        load_words(tl, kb, wa, wb);
+        if (++kb == tl.kb) {
+          kb = 0;
+          t += t_step;
+          more = seek();
+        }
+      };
+      uint32_t wa[kSfAhead][4], wb[kSfAhead][4];
+      bool have[kSfAhead];
+#pragma unroll
+      for (int d = 0; d < kSfAhead; ++d) {
+        have[d] = more;
+        if (more) fetch(wa[d], wb[d]);
+      }
+      for (bool go = true; go;) {
+#pragma unroll
+        for (int d = 0; d < kSfAhead; ++d) {  // slot d holds the k-blocks d, d + kSfAhead, ...
+          if (!have[d] || !wait_free()) {
+            go = false;
+            break;
+          }
+          uint32_t ra[4], rb[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ra[j] = wa[d][j] * R4;
+            rb[j] = wb[d][j] * R4;
+          }
+          put(ra, rb);
+          have[d] = more;
+          if (more) fetch(wa[d], wb[d]);
         }
       }
     }
