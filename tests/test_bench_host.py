@@ -67,3 +67,30 @@ def test_small_dispatch_accounting():
     big = S.Workload("rows-beyond-shared-memory", T=8000, H=4096, E=8, k=2, F=128)
     assert bench.launches_per_step(big, gather=True) == bench.launches_per_step(big) - 1
 
+
+
+@pytest.mark.parametrize("fixed_s,per_token_s", [(0.5, 0.01), (0.0, 0.2), (3.0, 0.001)])
+def test_cpu_baseline_sample_fills_its_budget(monkeypatch, fixed_s, per_token_s):
+    """The oracle sample is re-sized from each timed run until one takes most of the budget,
+    never past 256 tokens or the workload's T, whatever the fixed and per-token costs."""
+    clock = [0.0]
+    sizes = []
+
+    def fake_sample(w, inp, off, n):
+        sizes.append(n)
+        clock[0] += fixed_s + per_token_s * n
+
+    monkeypatch.setattr(bench, "oracle_inputs", lambda w, seed, rows: None)
+    monkeypatch.setattr(bench, "oracle_sample", fake_sample)
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: clock[0])
+    w = S.WORKLOADS["dsv3"]
+    budget = 15.0
+    rec = bench.cpu_baseline(w, 0, budget_s=budget)
+    n = sizes[-1]
+    assert 1 <= n <= min(w.T, 256)
+    t = fixed_s + per_token_s * n
+    assert rec["value"] == pytest.approx(n / t)
+    assert f"the first {n} of {w.T} tokens" in rec["sample"]
+    # the last run takes most of the budget unless the 256-token cap stops it first
+    assert t >= 0.6 * budget or n == 256
+    assert len(sizes) <= 5
