@@ -135,6 +135,10 @@ WORKLOADS = {
     "dsv3-mid": Workload("dsv3-mid", T=8192, H=2048, E=256, k=8, F=512, F_shared=512, score_fn=1,
                          renorm=1, gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True,
                          wr_std=0.02 * math.sqrt(7168 / 2048)),
+    # the same stand-in with FP8 expert GEMMs
+    "dsv3-mid-fp8": Workload("dsv3-mid-fp8", T=8192, H=2048, E=256, k=8, F=512, F_shared=512, score_fn=1,
+                             renorm=1, gate_scale=2.5, n_group=8, topk_group=4, sel_bias=True,
+                             wr_std=0.02 * math.sqrt(7168 / 2048), fp8=True),
     # profiling stand-in with DeepSeek-V3-style routing and small expert segments
     # (about 64 rows per expert): 2.8 GB of expert weights, small enough for a full capture
     "dsv3-small": Workload("dsv3-small", T=2048, H=7168, E=256, k=8, F=256, F_shared=256, score_fn=1,
