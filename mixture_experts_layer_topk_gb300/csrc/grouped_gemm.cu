@@ -44,9 +44,7 @@ struct Geo {
   static constexpr int EB = FP8 ? 1 : 2;          // element bytes
   static constexpr int BKE = 128 / EB;            // K elements per stage
   static constexpr int MN_INNER = 128 / EB;       // elements of one 128-byte MN-major row
-  static constexpr int MN_BOX = 128 * BKE;        // bytes of one MN-major box (MN_INNER x BKE)
   static constexpr int KSTEP = FP8 ? 32 : 16;     // K of one MMA instruction
-  static constexpr int THREADS = FP8 ? 320 : 192; // + 4 scale-factor warps for FP8
 };
 constexpr int kStagingBytes = 16384;  // per epilogue warpgroup
 // bf16 weight gradients: token rows per stage (both operands MN-major, 128-byte rows of
@@ -630,7 +628,7 @@ __global__ void __launch_bounds__(threads_of<FP8, NEPI>(), 1)
           const uint32_t sa = smem_u32(tiles + stage * STAGE);
           const uint32_t sb = sa + A_BYTES;
           // K-major operands step 32 bytes per instruction inside the 128-byte swizzle row;
-          // MN-major operands step KSTEP rows of 128 bytes, with MN atoms MN_BOX bytes apart
+          // MN-major operands step KSTEP rows of 128 bytes, with MN atoms MNB bytes apart
           constexpr uint32_t MN_STEP = G::KSTEP * 128;
           // weight gradients: the last block's K steps past the expert's rows are skipped
           const int nkk = MODE == MODE_WGRAD && kb + 1 == tl.kb ? (tl.krem + G::KSTEP - 1) / G::KSTEP : BK / G::KSTEP;

@@ -758,11 +758,6 @@ __global__ void __launch_bounds__(256) k_split_wr(const float* __restrict__ Wr, 
   }
 }
 
-struct Bf16In {
-  uint16_t v;
-  __device__ __forceinline__ explicit operator float() const { return __uint_as_float((uint32_t)v << 16); }
-};
-
 }  // namespace
 
 cudaError_t launch_router_topk(const moe_config& c, const uint16_t* X, const float* Wr, const float* logit_bias,
